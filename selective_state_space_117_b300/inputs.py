@@ -1,0 +1,198 @@
+"""Seeded synthetic inputs for the selective scan workloads.
+
+This module only draws random tensors with the shapes and distributions of
+the five workloads; it contains none of the scan's arithmetic.  The CUDA
+library's tests, the benchmark and the oracle checks all take their inputs
+from here, so both sides always see the same bytes.
+
+Shapes (row-major): u, delta, z (batch, dim, L); B, C (batch, N, L);
+A (dim, N); D, delta_bias (dim,).  Decode draws u, delta, z as (batch, dim)
+and B, C as (batch, N) per step.
+
+Draw order for a full-sequence problem is fixed: u, delta_raw, the uniform
+behind delta_bias, B, C, D, z.  delta_bias = log(expm1(U[1e-3, 1e-1])) is the
+inverse softplus of a uniform initial step size, so softplus(0 + bias) lies in
+[1e-3, 1e-1].
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+F32, BF16 = 0, 1
+
+
+@dataclass
+class Problem:
+    """One selective-scan problem: every tensor the scan reads, on one device."""
+    name: str
+    u: torch.Tensor
+    delta: torch.Tensor
+    A: torch.Tensor
+    B: torch.Tensor
+    C: torch.Tensor
+    D: Optional[torch.Tensor]
+    z: Optional[torch.Tensor]
+    delta_bias: Optional[torch.Tensor]
+    softplus: bool = True
+    chunk_len: int = 0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def batch(self):
+        return self.u.shape[0]
+
+    @property
+    def dim(self):
+        return self.u.shape[1]
+
+    @property
+    def dstate(self):
+        return self.A.shape[1]
+
+    @property
+    def seqlen(self):
+        return self.u.shape[2]
+
+    @property
+    def in_dtype(self):
+        return BF16 if self.u.dtype == torch.bfloat16 else F32
+
+    def to(self, device):
+        mv = lambda t: None if t is None else t.to(device)
+        return Problem(self.name, mv(self.u), mv(self.delta), mv(self.A), mv(self.B), mv(self.C),
+                       mv(self.D), mv(self.z), mv(self.delta_bias), self.softplus, self.chunk_len,
+                       dict(self.extra))
+
+
+def _gen(seed: int, device: str) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _normal(shape, std, g, device):
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std
+
+
+def _bias(dim, g, device):
+    dt0 = torch.rand((dim,), generator=g, device=device, dtype=torch.float64) * (1e-1 - 1e-3) + 1e-3
+    return torch.log(torch.expm1(dt0)).to(torch.float32)
+
+
+def a_s4d_real(dim: int, dstate: int, device: str = "cpu", via_log: bool = False) -> torch.Tensor:
+    """A[d, n] = -(n + 1) for every channel (optionally spelled -exp(log(n + 1)))."""
+    n1 = torch.arange(1, dstate + 1, device=device, dtype=torch.float32)
+    row = -torch.exp(torch.log(n1)) if via_log else -n1
+    return row.unsqueeze(0).expand(dim, dstate).contiguous()
+
+
+def selective_problem(name, *, seed, batch, dim, dstate, seqlen, dtype=torch.float32, bc_std=1.0,
+                      d_mode="normal", gate=True, a_via_log=False, device="cpu", gen_device=None,
+                      chunk_len=0) -> Problem:
+    """Draw one problem.  ``gen_device`` is where the random numbers are drawn
+    (``"cpu"`` or ``"cuda"``); the tensors are then moved to ``device``."""
+    gd = gen_device or device
+    g = _gen(seed, gd)
+    u = _normal((batch, dim, seqlen), 1.0, g, gd)
+    draw = _normal((batch, dim, seqlen), 1.0, g, gd)
+    bias = _bias(dim, g, gd)
+    B = _normal((batch, dstate, seqlen), bc_std, g, gd)
+    C = _normal((batch, dstate, seqlen), bc_std, g, gd)
+    D = _normal((dim,), 1.0, g, gd) if d_mode == "normal" else torch.ones((dim,), device=gd)
+    z = _normal((batch, dim, seqlen), 1.0, g, gd) if gate else None
+    A = a_s4d_real(dim, dstate, gd, via_log=a_via_log)
+    cast = lambda t: None if t is None else t.to(dtype).contiguous()
+    p = Problem(name, cast(u), cast(draw), A, cast(B), cast(C), D, cast(z), bias, True, chunk_len)
+    return p.to(device) if device != gd else p
+
+
+def lti_problem(name="medium_fp32_gate_lti", *, seed=1, batch=2, dim=256, dstate=16, seqlen=2048,
+                device="cpu", gen_device=None) -> Problem:
+    """The time-invariant variant of the medium workload: delta_raw (per channel),
+    B and C (per batch row) are drawn once and repeated over every t."""
+    gd = gen_device or device
+    g = _gen(seed, gd)
+    u = _normal((batch, dim, seqlen), 1.0, g, gd)
+    draw = _normal((batch, dim, 1), 1.0, g, gd).expand(batch, dim, seqlen).contiguous()
+    bias = _bias(dim, g, gd)
+    B = _normal((batch, dstate, 1), 0.25, g, gd).expand(batch, dstate, seqlen).contiguous()
+    C = _normal((batch, dstate, 1), 0.25, g, gd).expand(batch, dstate, seqlen).contiguous()
+    D = torch.ones((dim,), device=gd)
+    z = _normal((batch, dim, seqlen), 1.0, g, gd)
+    A = a_s4d_real(dim, dstate, gd)
+    p = Problem(name, u, draw, A, B, C, D, z, bias, True)
+    return p.to(device) if device != gd else p
+
+
+# The five workloads.  Sizes and distributions follow the problem statement;
+# where it is silent (A and D of the long-sequence and decode workloads) A is
+# -(n+1) and D is 1, as in the medium and 130M-shaped workloads.
+WORKLOADS = {
+    "tiny_fp32": dict(seed=0, batch=1, dim=16, dstate=4, seqlen=64, dtype=torch.float32, bc_std=1.0,
+                      d_mode="normal", gate=False),
+    "medium_fp32_gate": dict(seed=1, batch=2, dim=256, dstate=16, seqlen=2048, dtype=torch.float32,
+                             bc_std=0.25, d_mode="ones", gate=True),
+    "mamba130m_layer_bf16": dict(seed=2, batch=8, dim=1536, dstate=16, seqlen=2048, dtype=torch.bfloat16,
+                                 bc_std=0.25, d_mode="ones", gate=True, a_via_log=True),
+    "mamba2p8b_long_bf16": dict(seed=3, batch=1, dim=5120, dstate=16, seqlen=65536, dtype=torch.bfloat16,
+                                bc_std=0.25, d_mode="ones", gate=True, chunk_len=2048),
+}
+
+DECODE = dict(name="decode_256x5120", seed=4, batch=256, dim=5120, dstate=16, steps=1024)
+
+
+def workload(name: str, device="cpu", gen_device=None, **over) -> Problem:
+    kw = dict(WORKLOADS[name])
+    kw.update(over)
+    return selective_problem(name, device=device, gen_device=gen_device, **kw)
+
+
+@dataclass
+class DecodeStream:
+    """Inputs of a multi-step decode: fixed A, D, delta_bias and per-step draws."""
+    A: torch.Tensor
+    D: torch.Tensor
+    delta_bias: torch.Tensor
+    u: torch.Tensor        # (steps, batch, dim)
+    delta: torch.Tensor    # (steps, batch, dim)
+    B: torch.Tensor        # (steps, batch, N)
+    C: torch.Tensor        # (steps, batch, N)
+    z: torch.Tensor        # (steps, batch, dim)
+
+
+def decode_stream(*, seed=4, batch=256, dim=5120, dstate=16, steps=1024, dtype=torch.bfloat16,
+                  device="cpu", gen_device=None) -> DecodeStream:
+    """Per-step draws as the long-sequence workload: u, z ~ N(0,1); delta_raw ~
+    N(0,1) plus a per-channel bias; B, C ~ N(0, 1/16).  Drawn step-major in the
+    order u, delta_raw, B, C, z after the bias."""
+    gd = gen_device or device
+    g = _gen(seed, gd)
+    bias = _bias(dim, g, gd)
+    A = a_s4d_real(dim, dstate, gd)
+    D = torch.ones((dim,), device=gd)
+    us, ds, Bs, Cs, zs = [], [], [], [], []
+    for _ in range(steps):
+        us.append(_normal((batch, dim), 1.0, g, gd).to(dtype))
+        ds.append(_normal((batch, dim), 1.0, g, gd).to(dtype))
+        Bs.append(_normal((batch, dstate), 0.25, g, gd).to(dtype))
+        Cs.append(_normal((batch, dstate), 0.25, g, gd).to(dtype))
+        zs.append(_normal((batch, dim), 1.0, g, gd).to(dtype))
+    st = DecodeStream(A, D, bias, torch.stack(us), torch.stack(ds), torch.stack(Bs), torch.stack(Cs),
+                      torch.stack(zs))
+    if device != gd:
+        st = DecodeStream(*(t.to(device) for t in (st.A, st.D, st.delta_bias, st.u, st.delta, st.B, st.C, st.z)))
+    return st
+
+
+def to_wire(t: Optional[torch.Tensor]):
+    """Host numpy view of a tensor in the oracle's wire format (fp32, or bf16 as uint16 bits)."""
+    import numpy as np
+    if t is None:
+        return None
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
