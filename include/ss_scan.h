@@ -1,0 +1,145 @@
+/*
+ * ss_scan.h -- C ABI of the B300 selective state space scan (Mamba S6).
+ *
+ * The operation (from "State Space Models and Mamba", multigrid.ai/learn/
+ * mamba-ssm, section "Selective state", equations delta_t, A_t and h_t, and
+ * the readout y_t = C h_t of section "It is a linear recurrence"; the
+ * selection parameters as listed in "Mamba: Linear-Time Sequence Modeling
+ * with Selective State Spaces", azimuth.plus, section on S6):
+ *
+ *   for every batch row b, channel d, step t and state n < N:
+ *     dt      = softplus(delta[b,d,t] + delta_bias[d])   (or without softplus)
+ *     Abar    = exp(dt * A[d,n])
+ *     h[n]    = Abar * h[n] + dt * B[b,n,t] * u[b,d,t]
+ *     y[b,d,t]= (sum_n C[b,n,t] * h[n] + D[d] * u[b,d,t]) * silu(z[b,d,t])
+ *
+ * D (the skip term of the four-matrix model, "State space models and Mamba:
+ * reading long sequences without attention", ai-trend.me, "Core idea") and
+ * the SiLU gate z (branch B of the Mamba block, "What a Mamba block actually
+ * contains", multigrid.ai) are optional.  The state h starts at zero.
+ *
+ * Layouts (row-major, C order; every array dense and contiguous):
+ *   u, delta, z, y : (batch, dim, seqlen)   -- time is the fastest index
+ *   B, C           : (batch, dstate, seqlen) -- shared by all channels of a row
+ *   A              : (dim, dstate)  fp32
+ *   D, delta_bias  : (dim)          fp32
+ *   last_state     : (batch, dim, dstate) fp32
+ * u, delta, B, C and z share one element type (ss_dims.in_dtype): fp32 or
+ * bf16.  A, D, delta_bias, y and every state are always fp32.
+ *
+ * Pointers are DEVICE pointers (cudaMalloc'd or otherwise device-accessible
+ * memory of the current device).  The caller owns every buffer, including
+ * the chunked workspace; the library allocates nothing, never synchronises,
+ * and enqueues all work on the given stream (NULL = legacy default stream).
+ *
+ * Errors: each call returns an ss_status.  Argument errors are detected on
+ * the host before anything is launched (nothing is written then).  A failed
+ * launch returns SS_ECUDA; ss_last_cuda_error() gives the CUDA error code.
+ * Nothing aborts and nothing throws.
+ */
+#ifndef SS_SCAN_H
+#define SS_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (same underlying type); NULL selects the legacy default stream. */
+typedef struct CUstream_st* ss_stream_t;
+
+typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
+
+typedef enum {
+    SS_OK = 0,
+    SS_EINVAL = -1,      /* bad size, missing required pointer, unsupported dstate */
+    SS_EALIGN = -2,      /* a pointer is not aligned to its element size */
+    SS_EDTYPE = -3,      /* in_dtype is neither SS_F32 nor SS_BF16 */
+    SS_EWORKSPACE = -4,  /* chunked workspace missing, too small or misaligned */
+    SS_ECUDA = -5,       /* a CUDA launch or call failed (see ss_last_cuda_error) */
+    SS_ETIMEOUT = -6     /* reserved for bounded device-side waits */
+} ss_status;
+
+/* Largest supported state size N. */
+#define SS_MAX_DSTATE 64
+
+typedef struct {
+    int64_t batch;     /* >= 0; at most 65535 */
+    int64_t dim;       /* channels D, >= 0 */
+    int64_t dstate;    /* state size N, 0 .. SS_MAX_DSTATE */
+    int64_t seqlen;    /* sequence length L, >= 0 (ignored by ss_state_update) */
+    int32_t in_dtype;  /* ss_dtype of u, delta, B, C, z */
+} ss_dims;
+
+/*
+ * Full-sequence scan (the "parallel" training/prefill face of the layer;
+ * "The same layer has two faces", multigrid.ai, section "Why a linear
+ * recurrence can be trained in parallel").  One pass over L per channel with
+ * the state kept on chip; the (batch, L, dim, N) expanded state is never
+ * written ("never materializing the large expanded state", ai-trend.me,
+ * "How it works"; "Kernel fusion", azimuth.plus).
+ *   u, delta, B, C, A, y   required (unless the corresponding size is 0)
+ *   D, z, delta_bias       optional (NULL = absent: D = 0, no gate, bias 0)
+ *   softplus_flag          nonzero: dt = softplus(delta + bias); zero: dt = delta + bias
+ *   last_state             optional output: h after the last step (zeros if L = 0)
+ */
+int ss_scan_fwd(const ss_dims* dims, const void* u, const void* delta, const float* A,
+                const void* B, const void* C, const float* D, const void* z,
+                const float* delta_bias, int softplus_flag, float* y, float* last_state,
+                ss_stream_t stream);
+
+/*
+ * Bytes of caller-provided device workspace that ss_scan_chunked needs for
+ * these dims and chunk length (0 on invalid arguments).
+ */
+size_t ss_scan_chunked_workspace_bytes(const ss_dims* dims, int64_t chunk_len);
+
+/*
+ * Chunked scan for long sequences: the same result as ss_scan_fwd, computed
+ * as (1) a local zero-start scan of every chunk of chunk_len steps, giving the
+ * chunk's end state and its decay product, (2) an exclusive scan across chunks
+ * of the (decay product, state) pairs under the associative operator
+ * (a1,b1) o (a2,b2) = (a1*a2, a2*b1 + b2), which gives each chunk its true
+ * starting state, and (3) a fix-up pass that runs every chunk from that state
+ * and writes y.  The recurrence is associative ("Parallel scan", azimuth.plus),
+ * which is what makes chunks independent.
+ *   chunk_len        >= 1
+ *   workspace        device memory of at least ss_scan_chunked_workspace_bytes,
+ *                    256-byte aligned; its contents on entry are ignored
+ * Other arguments as ss_scan_fwd.  Three kernels are launched on `stream`.
+ */
+int ss_scan_chunked(const ss_dims* dims, const void* u, const void* delta, const float* A,
+                    const void* B, const void* C, const float* D, const void* z,
+                    const float* delta_bias, int softplus_flag, float* y, float* last_state,
+                    int64_t chunk_len, void* workspace, size_t workspace_bytes,
+                    ss_stream_t stream);
+
+/*
+ * One decode step on a persistent state (the recurrence face: "each new token
+ * only updates a fixed-size state", mernstackdev.com, FAQ; the state of
+ * shape (batch, dim, N) is the fixed-size memory of "The state, in bytes",
+ * multigrid.ai).  dims->seqlen is ignored.
+ *   state   (batch, dim, dstate) fp32, read and updated in place
+ *   u, delta, z, y : (batch, dim)      B, C : (batch, dstate)
+ * Other arguments as ss_scan_fwd.  Running L steps from a zero state gives
+ * the same y and final state as ss_scan_fwd over those L steps.
+ */
+int ss_state_update(const ss_dims* dims, float* state, const void* u, const void* delta,
+                    const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* delta_bias, int softplus_flag, float* y,
+                    ss_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* ss_status_string(int status);
+
+/* The CUDA error code (cudaError_t value) behind the last SS_ECUDA returned on
+ * this host thread, or 0. */
+int ss_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SS_SCAN_H */

@@ -1,0 +1,214 @@
+"""B300-native selective state space scan (Mamba S6).
+
+Python binding of the C ABI in ``include/ss_scan.h`` (``libssscan.so``, built
+in-tree by ``python -m selective_state_space_117_b300.build``).  The binding
+only checks tensor shapes and dtypes, allocates outputs with PyTorch and
+passes device pointers and the current CUDA stream to the library; every step
+of the scan runs in the library's CUDA kernels.  There is no CPU path: when
+the library is missing or a tensor is not on a CUDA device, calls raise.
+
+Entry points (same names as the C ABI, without the ``ss_`` prefix):
+  scan_fwd        full-sequence scan
+  scan_chunked    full-sequence scan as local scan / carry / fix-up over chunks
+  state_update    one decode step on a persistent (batch, dim, N) fp32 state
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = ["scan_fwd", "scan_chunked", "state_update", "chunked_workspace_bytes", "SSError", "library_path",
+           "F32", "BF16", "MAX_DSTATE", "LAUNCHES"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libssscan.so")
+_lib = None
+
+F32, BF16 = 0, 1
+MAX_DSTATE = 64
+# Kernels launched per call (for launch accounting): chunked = local + carry + fix-up.
+LAUNCHES = {"scan_fwd": 1, "scan_chunked": 3, "state_update": 1}
+
+SS_OK, SS_EINVAL, SS_EALIGN, SS_EDTYPE, SS_EWORKSPACE, SS_ECUDA, SS_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
+
+
+class SSError(RuntimeError):
+    """A non-zero ss_status returned by the library."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("dstate", ctypes.c_int64),
+                ("seqlen", ctypes.c_int64), ("in_dtype", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libssscan.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"{_LIB_PATH} is missing; build it with `python -m selective_state_space_117_b300.build`")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        dp = ctypes.POINTER(Dims)
+        L.ss_scan_fwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp]
+        L.ss_scan_fwd.restype = ctypes.c_int
+        L.ss_scan_chunked_workspace_bytes.argtypes = [dp, i64]
+        L.ss_scan_chunked_workspace_bytes.restype = ctypes.c_size_t
+        L.ss_scan_chunked.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, i64, vp,
+                                      ctypes.c_size_t, vp]
+        L.ss_scan_chunked.restype = ctypes.c_int
+        L.ss_state_update.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
+        L.ss_state_update.restype = ctypes.c_int
+        L.ss_status_string.argtypes = [ctypes.c_int]
+        L.ss_status_string.restype = ctypes.c_char_p
+        L.ss_last_cuda_error.argtypes = []
+        L.ss_last_cuda_error.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != SS_OK:
+        msg = lib().ss_status_string(status).decode()
+        if status == SS_ECUDA:
+            msg += f" (cudaError {lib().ss_last_cuda_error()})"
+        raise SSError(status, f"{what}: {msg}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device, stream):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"inputs must be float32 or bfloat16, got {t.dtype}")
+
+
+def _need(t, name, shape, dtype, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state):
+    if not isinstance(u, torch.Tensor) or u.dim() != 3:
+        raise ValueError("u must be a (batch, dim, seqlen) tensor")
+    if u.device.type != "cuda":
+        raise ValueError("the selective scan runs on a CUDA device only; u is on " + str(u.device))
+    batch, dim, L = u.shape
+    if not isinstance(A, torch.Tensor) or A.dim() != 2:
+        raise ValueError("A must be a (dim, dstate) tensor")
+    N = A.shape[1]
+    dev, dt = u.device, u.dtype
+    code = _dtype_code(u)
+    _need(u, "u", (batch, dim, L), dt, dev)
+    _need(delta, "delta", (batch, dim, L), dt, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    _need(B, "B", (batch, N, L), dt, dev)
+    _need(C, "C", (batch, N, L), dt, dev)
+    _need(D, "D", (dim,), torch.float32, dev)
+    _need(z, "z", (batch, dim, L), dt, dev)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev)
+    if y is None:
+        y = torch.empty((batch, dim, L), dtype=torch.float32, device=dev)
+    _need(y, "y", (batch, dim, L), torch.float32, dev)
+    _need(last_state, "last_state", (batch, dim, N), torch.float32, dev)
+    return Dims(batch, dim, N, L, code), y
+
+
+def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, y=None, last_state=None,
+             return_last_state=False, stream=None):
+    """Full-sequence selective scan.  Returns y (fp32, (batch, dim, L)), or
+    (y, last_state) when ``return_last_state`` or ``last_state`` is given."""
+    dims, y = _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state)
+    if return_last_state and last_state is None:
+        last_state = torch.empty((dims.batch, dims.dim, dims.dstate), dtype=torch.float32, device=u.device)
+    st = lib().ss_scan_fwd(ctypes.byref(dims), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                           _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(last_state),
+                           _stream(u.device, stream))
+    _check(st, "ss_scan_fwd")
+    return (y, last_state) if last_state is not None else y
+
+
+def chunked_workspace_bytes(batch, dim, dstate, seqlen, chunk_len, dtype=F32) -> int:
+    dims = Dims(batch, dim, dstate, seqlen, dtype)
+    return int(lib().ss_scan_chunked_workspace_bytes(ctypes.byref(dims), int(chunk_len)))
+
+
+def scan_chunked(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, chunk_len=2048, y=None,
+                 last_state=None, return_last_state=False, workspace=None, stream=None):
+    """Chunked selective scan (local scan, carry across chunks, fix-up).  Same
+    result and return convention as ``scan_fwd``.  ``workspace`` is an optional
+    uint8 CUDA tensor of at least ``chunked_workspace_bytes`` bytes."""
+    dims, y = _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state)
+    if return_last_state and last_state is None:
+        last_state = torch.empty((dims.batch, dims.dim, dims.dstate), dtype=torch.float32, device=u.device)
+    need = int(lib().ss_scan_chunked_workspace_bytes(ctypes.byref(dims), int(chunk_len)))
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=u.device)
+    if workspace.device != u.device or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
+    st = lib().ss_scan_chunked(ctypes.byref(dims), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                               _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(last_state),
+                               int(chunk_len), _ptr(workspace), workspace.numel(), _stream(u.device, stream))
+    _check(st, "ss_scan_chunked")
+    return (y, last_state) if last_state is not None else y
+
+
+def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, y=None,
+                 stream=None):
+    """One decode step.  state (batch, dim, N) fp32 is updated in place;
+    u, delta, z are (batch, dim); B, C are (batch, N).  Returns y (batch, dim) fp32."""
+    if not isinstance(u, torch.Tensor) or u.dim() != 2:
+        raise ValueError("u must be a (batch, dim) tensor")
+    if u.device.type != "cuda":
+        raise ValueError("the selective scan runs on a CUDA device only; u is on " + str(u.device))
+    batch, dim = u.shape
+    N = A.shape[1]
+    dev, dt = u.device, u.dtype
+    code = _dtype_code(u)
+    _need(state, "state", (batch, dim, N), torch.float32, dev)
+    _need(delta, "delta", (batch, dim), dt, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    _need(B, "B", (batch, N), dt, dev)
+    _need(C, "C", (batch, N), dt, dev)
+    _need(D, "D", (dim,), torch.float32, dev)
+    _need(z, "z", (batch, dim), dt, dev)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev)
+    if y is None:
+        y = torch.empty((batch, dim), dtype=torch.float32, device=dev)
+    _need(y, "y", (batch, dim), torch.float32, dev)
+    dims = Dims(batch, dim, N, 1, code)
+    st = lib().ss_state_update(ctypes.byref(dims), _ptr(state), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                               _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(y),
+                               _stream(u.device, stream))
+    _check(st, "ss_state_update")
+    return y

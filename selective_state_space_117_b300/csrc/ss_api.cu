@@ -1,0 +1,185 @@
+// C ABI of the selective scan library: argument validation on the host, then
+// kernel launches on the caller's stream.  See include/ss_scan.h for the
+// contract of every entry point.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ss_launch.h"
+#include "ss_scan.h"
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda = (int)e;
+  return SS_ECUDA;
+}
+
+// After enqueueing kernels: report launch errors (non-sticky errors are cleared).
+int launched() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SS_OK : cuda_fail(e);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t in_size(int32_t dtype) { return dtype == SS_BF16 ? 2 : 4; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+constexpr int64_t kMaxGridX = 2147483647;
+constexpr int64_t kMaxGridY = 65535;
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shape, dtype and pointer checks shared by the two full-sequence entry points.
+int check_scan(const ss_dims* dims, const void* u, const void* delta, const float* A, const void* B,
+               const void* C, const float* D, const void* z, const float* delta_bias, const float* y,
+               const float* last_state) {
+  if (!dims) return SS_EINVAL;
+  const ss_dims& d = *dims;
+  if (d.in_dtype != SS_F32 && d.in_dtype != SS_BF16) return SS_EDTYPE;
+  if (d.batch < 0 || d.dim < 0 || d.dstate < 0 || d.seqlen < 0) return SS_EINVAL;
+  if (d.dstate > SS_MAX_DSTATE || d.batch > kMaxGridY) return SS_EINVAL;
+  if (ceil_div(d.dim, ssk::kThreads) > kMaxGridX) return SS_EINVAL;
+  const size_t es = in_size(d.in_dtype);
+  const bool rows = d.batch > 0 && d.dim > 0 && d.seqlen > 0;
+  if (rows && (!u || !delta || !y)) return SS_EINVAL;
+  if (rows && d.dstate > 0 && (!B || !C || !A)) return SS_EINVAL;
+  if (!aligned(u, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) || !aligned(z, es))
+    return SS_EALIGN;
+  if (!aligned(A, 4) || !aligned(D, 4) || !aligned(delta_bias, 4) || !aligned(y, 4) || !aligned(last_state, 4))
+    return SS_EALIGN;
+  return SS_OK;
+}
+
+ssk::ScanArgs make_scan_args(const ss_dims& d, const void* u, const void* delta, const float* A, const void* B,
+                             const void* C, const float* D, const void* z, const float* delta_bias,
+                             int softplus_flag, float* y, float* last_state, int64_t chunk_len) {
+  ssk::ScanArgs a{};
+  a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias;
+  a.y = y; a.last_state = last_state;
+  a.batch = d.batch; a.dim = d.dim; a.dstate = d.dstate; a.seqlen = d.seqlen;
+  a.chunk_len = chunk_len;
+  a.nchunks = ceil_div(d.seqlen, chunk_len);
+  a.ctiles = (int)ceil_div(d.dim, ssk::kThreads);
+  a.softplus = softplus_flag ? 1 : 0;
+  // 16-byte vector loads along a row need every row start and every group start aligned.
+  const size_t es = in_size(d.in_dtype);
+  const bool rows16 = (d.seqlen * (int64_t)es) % 16 == 0 && (d.seqlen * 4) % 16 == 0;
+  const bool ptr16 = aligned(u, 16) && aligned(delta, 16) && aligned(z, 16) && aligned(y, 16);
+  a.vec = (rows16 && ptr16 && chunk_len % ssk::kGroup == 0) ? 1 : 0;
+  return a;
+}
+
+// Zero the final state when there is nothing to scan (L = 0: h stays at its zero start).
+int zero_state(const ss_dims& d, float* last_state, cudaStream_t s) {
+  if (!last_state) return SS_OK;
+  const size_t n = (size_t)(d.batch * d.dim * d.dstate);
+  if (n == 0) return SS_OK;
+  const cudaError_t e = cudaMemsetAsync(last_state, 0, n * sizeof(float), s);
+  return e == cudaSuccess ? SS_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int ss_scan_fwd(const ss_dims* dims, const void* u, const void* delta, const float* A, const void* B,
+                const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                float* y, float* last_state, ss_stream_t stream) {
+  const int st = check_scan(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
+  if (st != SS_OK) return st;
+  const ss_dims& d = *dims;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d.batch == 0 || d.dim == 0) return SS_OK;
+  if (d.seqlen == 0) return zero_state(d, last_state, s);
+  const ssk::ScanArgs a = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
+                                         d.seqlen);
+  const dim3 grid((unsigned)a.ctiles, (unsigned)d.batch);
+  if (ssk::launch_scan_full(a, d.in_dtype == SS_BF16, z != nullptr, grid, s) != 0) return SS_EINVAL;
+  return launched();
+}
+
+size_t ss_scan_chunked_workspace_bytes(const ss_dims* dims, int64_t chunk_len) {
+  if (!dims || chunk_len < 1 || dims->batch < 0 || dims->dim < 0 || dims->dstate < 0 || dims->seqlen < 0)
+    return 0;
+  const int64_t K = ceil_div(dims->seqlen, chunk_len);
+  const size_t s_bytes = (size_t)(dims->batch * dims->dim * K) * sizeof(float);
+  const size_t h_bytes = (size_t)(dims->batch * dims->dim * K * dims->dstate) * sizeof(float);
+  return align_up(s_bytes, kWsAlign) + h_bytes;
+}
+
+int ss_scan_chunked(const ss_dims* dims, const void* u, const void* delta, const float* A, const void* B,
+                    const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                    float* y, float* last_state, int64_t chunk_len, void* workspace, size_t workspace_bytes,
+                    ss_stream_t stream) {
+  const int st = check_scan(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
+  if (st != SS_OK) return st;
+  if (chunk_len < 1) return SS_EINVAL;
+  const ss_dims& d = *dims;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d.batch == 0 || d.dim == 0) return SS_OK;
+  if (d.seqlen == 0) return zero_state(d, last_state, s);
+  const size_t need = ss_scan_chunked_workspace_bytes(dims, chunk_len);
+  if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes < need) return SS_EWORKSPACE;
+  ssk::ScanArgs a = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
+                                   chunk_len);
+  if ((int64_t)a.ctiles * a.nchunks > kMaxGridX) return SS_EINVAL;
+  a.ws_S = static_cast<float*>(workspace);
+  a.ws_H = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                    align_up((size_t)(d.batch * d.dim * a.nchunks) * sizeof(float), kWsAlign));
+  const dim3 grid((unsigned)(a.ctiles * a.nchunks), (unsigned)d.batch);
+  const bool bf = d.in_dtype == SS_BF16;
+  if (ssk::launch_scan_local(a, bf, grid, s) != 0) return SS_EINVAL;
+  ssk::launch_carry(a, s);
+  ssk::launch_scan_fixup(a, bf, z != nullptr, grid, s);
+  return launched();
+}
+
+int ss_state_update(const ss_dims* dims, float* state, const void* u, const void* delta, const float* A,
+                    const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                    int softplus_flag, float* y, ss_stream_t stream) {
+  if (!dims) return SS_EINVAL;
+  const ss_dims& d = *dims;
+  if (d.in_dtype != SS_F32 && d.in_dtype != SS_BF16) return SS_EDTYPE;
+  if (d.batch < 0 || d.dim < 0 || d.dstate < 0 || d.dstate > SS_MAX_DSTATE || d.batch > kMaxGridY)
+    return SS_EINVAL;
+  if (ceil_div(d.dim, ssk::kThreads) > kMaxGridX) return SS_EINVAL;
+  if (d.batch == 0 || d.dim == 0) return SS_OK;
+  if (!u || !delta || !y) return SS_EINVAL;
+  if (d.dstate > 0 && (!state || !A || !B || !C)) return SS_EINVAL;
+  const size_t es = in_size(d.in_dtype);
+  if (!aligned(u, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) || !aligned(z, es))
+    return SS_EALIGN;
+  if (!aligned(state, 4) || !aligned(A, 4) || !aligned(D, 4) || !aligned(delta_bias, 4) || !aligned(y, 4))
+    return SS_EALIGN;
+  ssk::DecodeArgs a{};
+  a.state = state; a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+  a.delta_bias = delta_bias; a.y = y;
+  a.batch = d.batch; a.dim = d.dim; a.dstate = d.dstate;
+  a.softplus = softplus_flag ? 1 : 0;
+  const dim3 grid((unsigned)ceil_div(d.dim, ssk::kThreads), (unsigned)d.batch);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (ssk::launch_decode(a, d.in_dtype == SS_BF16, z != nullptr, grid, s) != 0) return SS_EINVAL;
+  return launched();
+}
+
+const char* ss_status_string(int status) {
+  switch (status) {
+    case SS_OK: return "SS_OK";
+    case SS_EINVAL: return "SS_EINVAL: invalid size or missing required pointer";
+    case SS_EALIGN: return "SS_EALIGN: pointer not aligned to its element size";
+    case SS_EDTYPE: return "SS_EDTYPE: unsupported input dtype";
+    case SS_EWORKSPACE: return "SS_EWORKSPACE: workspace missing, misaligned or too small";
+    case SS_ECUDA: return "SS_ECUDA: CUDA launch or call failed";
+    case SS_ETIMEOUT: return "SS_ETIMEOUT: a bounded device wait ran out";
+    default: return "unknown ss_status";
+  }
+}
+
+int ss_last_cuda_error(void) { return g_last_cuda; }
+
+}  // extern "C"

@@ -1,0 +1,18 @@
+// Host-side launchers of the selective scan kernels (one translation unit per
+// kernel family so the template instantiations compile in parallel).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "ss_types.h"
+
+namespace ssk {
+
+// Each returns 0 when a kernel was launched, -1 when dstate is unsupported.
+int launch_scan_full(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
+int launch_scan_local(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s);
+int launch_scan_fixup(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
+int launch_carry(const ScanArgs& a, cudaStream_t s);
+int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
+
+}  // namespace ssk

@@ -1,0 +1,49 @@
+// Argument blocks and launch constants shared by the host launchers and the kernels.
+#pragma once
+
+#include <cstdint>
+
+namespace ssk {
+
+constexpr int kThreads = 128;  // channels per block
+constexpr int kTile = 32;      // time steps per shared-memory tile
+constexpr int kGroup = 8;      // time steps per vector load
+
+enum Mode { kFull = 0, kLocal = 1, kFixup = 2 };
+
+struct ScanArgs {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* delta_bias;
+  float* y;
+  float* last_state;
+  float* ws_S;       // (batch, dim, nchunks): sum of dt over each chunk
+  float* ws_H;       // (batch, dim, nchunks, N): chunk end state, then carry-in
+  int64_t batch, dim, dstate, seqlen, chunk_len, nchunks;
+  int ctiles;        // channel tiles (blocks) per (b, chunk)
+  int softplus;
+  int vec;           // 1: every row start is 16-byte aligned for u, delta, z and y
+};
+
+// One decode step, one thread per (b, d).
+struct DecodeArgs {
+  float* state;
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* delta_bias;
+  float* y;
+  int64_t batch, dim, dstate;
+  int softplus;
+};
+
+}  // namespace ssk

@@ -1,0 +1,127 @@
+"""The C ABI on the host (no GPU): the library loads, exports every entry point
+that include/ss_scan.h declares, and rejects bad arguments before launching.
+Only calls that fail validation are made, so nothing here touches a device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import selective_state_space_117_b300 as ss
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(HEADER_DIR):
+        if f.endswith(".h"):
+            src = open(os.path.join(HEADER_DIR, f)).read()
+            names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(ss_\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("ss_scan_fwd", "ss_scan_chunked", "ss_scan_chunked_workspace_bytes", "ss_state_update",
+                 "ss_status_string", "ss_last_cuda_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ss.lib()
+    out = subprocess.run(["nm", "-D", "--defined-only", ss.library_path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (ss_\w+)", out))
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in exported, name
+
+
+def _dims(b=1, d=4, n=4, L=16, dt=ss.F32):
+    return ss.Dims(b, d, n, L, dt)
+
+
+P = 4096  # a fake, 256-byte aligned "device" address: never dereferenced, validation fails first
+
+
+def _fwd(dims, **over):
+    a = dict(u=P, delta=P, A=P, B=P, C=P, D=None, z=None, bias=None, y=P, last=None)
+    a.update(over)
+    return ss.lib().ss_scan_fwd(ctypes.byref(dims), a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                a["bias"], 1, a["y"], a["last"], None)
+
+
+def _chunked(dims, chunk=8, ws=P, ws_bytes=1 << 30, **over):
+    a = dict(u=P, delta=P, A=P, B=P, C=P, D=None, z=None, bias=None, y=P, last=None)
+    a.update(over)
+    return ss.lib().ss_scan_chunked(ctypes.byref(dims), a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                    a["bias"], 1, a["y"], a["last"], chunk, ws, ws_bytes, None)
+
+
+def test_validation_status_codes():
+    assert _fwd(_dims(dt=7)) == ss.SS_EDTYPE
+    assert _fwd(_dims(L=-1)) == ss.SS_EINVAL
+    assert _fwd(_dims(n=65)) == ss.SS_EINVAL
+    assert _fwd(_dims(b=70000)) == ss.SS_EINVAL
+    assert _fwd(_dims(), u=None) == ss.SS_EINVAL
+    assert _fwd(_dims(), y=None) == ss.SS_EINVAL
+    assert _fwd(_dims(), B=None) == ss.SS_EINVAL
+    assert _fwd(_dims(), u=P + 2) == ss.SS_EALIGN           # fp32 input at a 2-byte offset
+    assert _fwd(_dims(dt=ss.BF16), u=P + 1) == ss.SS_EALIGN  # bf16 input at an odd address
+    assert _fwd(_dims(), A=P + 1) == ss.SS_EALIGN
+    assert _fwd(_dims(), y=P + 2) == ss.SS_EALIGN
+    assert ss.lib().ss_scan_fwd(None, P, P, P, P, P, None, None, None, 1, P, None, None) == ss.SS_EINVAL
+    # sizes of zero are valid no-ops and return before any launch
+    assert _fwd(_dims(b=0), u=None, delta=None, y=None) == ss.SS_OK
+    assert _fwd(_dims(d=0), u=None, delta=None, y=None, A=None) == ss.SS_OK
+
+
+def test_chunked_validation():
+    assert _chunked(_dims(), chunk=0) == ss.SS_EINVAL
+    assert _chunked(_dims(), ws=None) == ss.SS_EWORKSPACE
+    assert _chunked(_dims(), ws=P + 16) == ss.SS_EWORKSPACE            # not 256-byte aligned
+    need = ss.chunked_workspace_bytes(1, 4, 4, 16, 8)
+    assert _chunked(_dims(), ws_bytes=need - 1) == ss.SS_EWORKSPACE
+    assert _chunked(_dims(dt=3)) == ss.SS_EDTYPE
+
+
+def test_workspace_bytes():
+    # S: batch*dim*K floats padded to 256 B, then H: batch*dim*K*N floats
+    assert ss.chunked_workspace_bytes(1, 4, 4, 16, 8) == 256 + 1 * 4 * 2 * 4 * 4
+    K = 65536 // 2048
+    assert ss.chunked_workspace_bytes(1, 5120, 16, 65536, 2048) == 5120 * K * 4 + 5120 * K * 16 * 4
+    assert ss.chunked_workspace_bytes(1, 4, 4, 16, 0) == 0
+    assert ss.chunked_workspace_bytes(2, 3, 5, 7, 3) == 256 + 2 * 3 * 3 * 5 * 4
+
+
+def test_state_update_validation():
+    lib = ss.lib()
+    d = _dims()
+    call = lambda dims, st=P, u=P, A=P: lib.ss_state_update(ctypes.byref(dims), st, u, P, A, P, P, None, None, None,
+                                                            1, P, None)
+    assert call(_dims(dt=9)) == ss.SS_EDTYPE
+    assert call(_dims(n=100)) == ss.SS_EINVAL
+    assert call(d, st=None) == ss.SS_EINVAL
+    assert call(d, u=None) == ss.SS_EINVAL
+    assert call(d, st=P + 1) == ss.SS_EALIGN
+    assert call(_dims(b=0)) == ss.SS_OK
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        s = ss.lib().ss_status_string(code).decode()
+        assert s.startswith("SS_")
+    assert "unknown" in ss.lib().ss_status_string(42).decode()
+    assert ss.lib().ss_last_cuda_error() == 0
+
+
+def test_binding_refuses_host_tensors():
+    u = torch.zeros((1, 4, 16))
+    with pytest.raises(ValueError, match="CUDA device only"):
+        ss.scan_fwd(u, u, torch.zeros((4, 4)), torch.zeros((1, 4, 16)), torch.zeros((1, 4, 16)))
+    with pytest.raises(ValueError, match="CUDA device only"):
+        ss.state_update(torch.zeros((1, 4, 4)), u[:, :, 0], u[:, :, 0], torch.zeros((4, 4)), torch.zeros((1, 4)),
+                        torch.zeros((1, 4)))

@@ -1,0 +1,321 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Every case draws seeded inputs from selective_state_space_117_b300.inputs,
+runs the library on the GPU, runs the oracle on the host on the same bytes,
+and compares element by element under the tolerances of tests/parity.py.
+Large workloads run at full size on the GPU in the launch configuration the
+benchmark times; the oracle then computes a sample of channels one by one.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_117_b300 as ss
+from selective_state_space_117_b300 import inputs as I
+from parity import check, host
+from pins import read_golden
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+# ------------------------------------------------------------------ helpers
+
+def oracle_scan(p: I.Problem, h0=None):
+    w = I.to_wire
+    return oracle.scan(w(p.u), w(p.delta), w(p.A), w(p.B), w(p.C), D=w(p.D), z=w(p.z), delta_bias=w(p.delta_bias),
+                       softplus=p.softplus, dtype="bf16" if p.in_dtype == I.BF16 else "f32", h0=h0)
+
+
+def subproblem(p: I.Problem, ds) -> I.Problem:
+    """The same problem restricted to channels ds (channels are independent)."""
+    ds = torch.as_tensor(ds, device=p.u.device)
+    pick = lambda t: None if t is None else t.index_select(1, ds).contiguous()
+    pick0 = lambda t: None if t is None else t.index_select(0, ds).contiguous()
+    return I.Problem(p.name + "_sub", pick(p.u), pick(p.delta), pick0(p.A), p.B, p.C, pick0(p.D), pick(p.z),
+                     pick0(p.delta_bias), p.softplus, p.chunk_len)
+
+
+def run(p: I.Problem, impl: str, chunk_len=None):
+    kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, softplus=p.softplus, return_last_state=True)
+    if impl == "fwd":
+        return ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, **kw)
+    return ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, chunk_len=chunk_len, **kw)
+
+
+def compare(p: I.Problem, y, hl, what, ds=None):
+    bf = p.in_dtype == I.BF16
+    ref_p = p if ds is None else subproblem(p, ds)
+    yr, hr = oracle_scan(ref_p.to("cpu"))
+    if ds is not None:
+        y = y[:, ds]
+        hl = hl[:, ds]
+    B, Dm, L = ref_p.u.shape
+    N = ref_p.A.shape[1]
+    ey = check(host(y).reshape(B * Dm, L), yr, bf, what + " y")
+    eh = check(host(hl).reshape(B * Dm, N), hr, bf, what + " last_state")
+    return ey, eh
+
+
+def custom(seed, batch, dim, N, L, dtype=torch.float32, gate=True, with_D=True, with_bias=True, softplus=True):
+    p = I.selective_problem("custom", seed=seed, batch=batch, dim=dim, dstate=N, seqlen=L, dtype=dtype, bc_std=0.5,
+                            d_mode="normal", gate=gate, device=DEV, gen_device="cpu")
+    # vary A across channels as well as states
+    g = torch.Generator().manual_seed(seed + 1000)
+    p.A = (-torch.exp(torch.rand((dim, N), generator=g) * 2.5 - 1.0)).to(DEV)
+    if not with_D:
+        p.D = None
+    if not with_bias:
+        p.delta_bias = None
+    p.softplus = softplus
+    if not softplus:   # raw step sizes must stay small and positive without the softplus
+        p.delta = (torch.rand(p.u.shape, generator=g) * 0.2).to(dtype).to(DEV)
+        p.delta_bias = None
+    return p
+
+
+# ------------------------------------------------------------ worked examples
+
+@pytest.mark.parametrize("impl", ["fwd", "chunked3", "decode"])
+def test_worked_examples(impl):
+    g = read_golden("tiny_example.txt")
+    sig = torch.tensor(g["signal"], dtype=torch.float32, device=DEV).view(1, 1, -1)
+    L = sig.shape[-1]
+    one = torch.ones((1, 1, L), device=DEV)
+    for key in ("a=0.9", "a=0.3"):
+        A = torch.tensor([[math.log(float(key.split("=")[1]))]], device=DEV)
+        if impl == "decode":
+            st = torch.zeros((1, 1, 1), device=DEV)
+            ys = [ss.state_update(st, sig[:, :, t].contiguous(), one[:, :, t].contiguous(), A, one[:, 0, t:t + 1].contiguous(),
+                                  one[:, 0, t:t + 1].contiguous(), softplus=False)[0, 0].item() for t in range(L)]
+        elif impl == "fwd":
+            ys = host(ss.scan_fwd(sig, one, A, one, one, softplus=False))[0, 0]
+        else:
+            ys = host(ss.scan_chunked(sig, one, A, one, one, softplus=False, chunk_len=3))[0, 0]
+        assert np.max(np.abs(np.asarray(ys) - np.asarray(g[key]))) <= g["tolerance"][0], (key, ys)
+    t = read_golden("selective_toy.txt")
+    vals = torch.tensor(t["values"], device=DEV).view(1, 1, -1)
+    imp = torch.tensor(t["important"], device=DEV).view(1, 1, -1) > 0
+    lo = math.log(0.95) / math.log(0.2)
+    dt = torch.where(imp, torch.tensor(1.0, device=DEV), torch.tensor(lo, device=DEV)).float()
+    Bv = torch.where(imp, torch.tensor(1.0, device=DEV), torch.tensor(0.05 / lo, device=DEV)).float()
+    A = torch.tensor([[math.log(0.2)]], device=DEV)
+    one4 = torch.ones_like(vals)
+    if impl == "chunked3":
+        y = ss.scan_chunked(vals, dt, A, Bv, one4, softplus=False, chunk_len=3)
+    else:
+        y = ss.scan_fwd(vals, dt, A, Bv, one4, softplus=False)
+    assert np.max(np.abs(host(y)[0, 0] - np.asarray(t["outputs"]))) <= t["tolerance"][0]
+
+
+# ------------------------------------------------------------ the workloads
+
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("chunked", 1), ("chunked", 7), ("chunked", 16), ("chunked", 64)])
+def test_tiny_fp32(impl, chunk):
+    p = I.workload("tiny_fp32", device=DEV, gen_device="cpu")
+    y, hl = run(p, impl, chunk)
+    compare(p, y, hl, f"tiny_fp32/{impl}{chunk or ''}")
+
+
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("chunked", 2048), ("chunked", 256), ("chunked", 100)])
+def test_medium_fp32_gate(impl, chunk):
+    p = I.workload("medium_fp32_gate", device=DEV, gen_device="cpu")
+    y, hl = run(p, impl, chunk)
+    compare(p, y, hl, f"medium_fp32_gate/{impl}{chunk or ''}")
+
+
+def test_medium_lti_closed_form():
+    """Time-invariant variant: library vs oracle, and library vs the convolution closed form
+    y_t = silu(z_t) * (sum_k K_k u_{t-k} + D u_t),  K_k = sum_n C_n exp(k dt A_n) dt B_n."""
+    p = I.lti_problem(device=DEV, gen_device="cpu")
+    y, hl = run(p, "fwd")
+    compare(p, y, hl, "medium_lti/fwd")
+    yc, _ = run(p, "chunked", 256)
+    compare(p, yc, hl, "medium_lti/chunked256")
+    pc = p.to("cpu")
+    Bn, Dm, L = pc.u.shape
+    yh = host(y)
+    k = np.arange(L, dtype=np.float64)
+    worst = 0.0
+    for b in range(Bn):
+        for d in range(0, Dm, 8):
+            x = float(pc.delta[b, d, 0]) + float(pc.delta_bias[d])
+            dt = math.log1p(math.exp(-abs(x))) + max(x, 0.0)
+            K = np.zeros(L)
+            for n in range(pc.A.shape[1]):
+                K += float(pc.C[b, n, 0]) * np.exp(k * dt * float(pc.A[d, n])) * dt * float(pc.B[b, n, 0])
+            u = pc.u[b, d].double().numpy()
+            z = pc.z[b, d].double().numpy()
+            want = (np.convolve(u, K)[:L] + float(pc.D[d]) * u) * (z / (1.0 + np.exp(-z)))
+            from parity import err_f32
+            worst = max(worst, err_f32(yh[b, d], want))
+    assert worst <= 1e-4, worst
+
+
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("chunked", 512)])
+def test_mamba130m_layer_bf16(impl, chunk):
+    p = I.workload("mamba130m_layer_bf16", device=DEV, gen_device="cuda")
+    y, hl = run(p, impl, chunk)
+    ds = list(range(0, 1536, 37)) + [1535]
+    compare(p, y, hl, f"mamba130m/{impl}{chunk or ''}", ds=ds)
+
+
+@pytest.mark.parametrize("impl,chunk", [("chunked", 2048), ("fwd", None)])
+def test_mamba2p8b_long_bf16(impl, chunk):
+    p = I.workload("mamba2p8b_long_bf16", device=DEV, gen_device="cuda")
+    y, hl = run(p, impl, chunk)
+    ds = list(range(3, 5120, 331)) + [5119]
+    compare(p, y, hl, f"mamba2p8b_long/{impl}{chunk or ''}", ds=ds)
+    del y, hl, p
+    torch.cuda.empty_cache()
+
+
+def test_decode_stream_256x5120():
+    """1024 sequential decode steps on a (256, 5120, 16) fp32 state; sampled channels of every
+    step's y and the final state against the oracle's recurrence."""
+    cfg = I.DECODE
+    st_in = I.decode_stream(seed=cfg["seed"], batch=cfg["batch"], dim=cfg["dim"], dstate=cfg["dstate"],
+                            steps=cfg["steps"], device=DEV, gen_device="cuda")
+    state = torch.zeros((cfg["batch"], cfg["dim"], cfg["dstate"]), device=DEV)
+    bs = torch.tensor([0, 173], device=DEV)
+    ds = torch.arange(5, 5120, 80, device=DEV)
+    ys = []
+    y = torch.empty((cfg["batch"], cfg["dim"]), device=DEV)
+    for t in range(cfg["steps"]):
+        ss.state_update(state, st_in.u[t], st_in.delta[t], st_in.A, st_in.B[t], st_in.C[t], D=st_in.D, z=st_in.z[t],
+                        delta_bias=st_in.delta_bias, y=y)
+        ys.append(y.index_select(0, bs).index_select(1, ds).clone())
+    yg = torch.stack(ys).cpu().numpy()                         # (steps, 2, nd)
+    sg = state.index_select(0, bs).index_select(1, ds).cpu().numpy().reshape(-1, cfg["dstate"])
+    # oracle: the same sub-problem, one step at a time
+    w = I.to_wire
+    A = st_in.A.index_select(0, ds).cpu().numpy()
+    Dv = st_in.D.index_select(0, ds).cpu().numpy()
+    bias = st_in.delta_bias.index_select(0, ds).cpu().numpy()
+    sub = lambda x: w(x.index_select(1, bs).index_select(2, ds))
+    u, dl, z = sub(st_in.u), sub(st_in.delta), sub(st_in.z)
+    Bw, Cw = w(st_in.B.index_select(1, bs)), w(st_in.C.index_select(1, bs))
+    sref = np.zeros((2 * len(ds), cfg["dstate"]))
+    yref = np.empty((cfg["steps"], 2 * len(ds)))
+    for t in range(cfg["steps"]):
+        yref[t] = oracle.state_update(sref, u[t], dl[t], A, Bw[t], Cw[t], D=Dv, z=z[t], delta_bias=bias, dtype="bf16")
+    check(yg.reshape(cfg["steps"], -1), yref, True, "decode y (all steps)")
+    check(sg, sref, True, "decode final state")
+    del st_in, state
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------ edge cases
+
+RAGGED = [
+    # seed, batch, dim, N, L, dtype, gate, with_D, with_bias, softplus
+    (21, 1, 130, 1, 63, torch.float32, True, True, True, True),
+    (22, 3, 33, 5, 100, torch.float32, False, True, False, True),
+    (23, 2, 17, 17, 1, torch.float32, True, False, True, True),
+    (24, 1, 257, 33, 77, torch.bfloat16, True, True, True, True),
+    (25, 2, 5, 64, 40, torch.float32, True, True, True, False),
+    (26, 1, 9, 3, 1000, torch.bfloat16, False, False, True, True),
+    (27, 2, 129, 16, 333, torch.bfloat16, True, True, True, True),
+    (28, 1, 64, 8, 257, torch.float32, True, True, True, True),
+]
+
+
+@pytest.mark.parametrize("case", RAGGED, ids=[f"b{c[1]}d{c[2]}n{c[3]}L{c[4]}{'bf' if c[5] == torch.bfloat16 else 'f'}"
+                                              for c in RAGGED])
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("chunked", 7), ("chunked", 32)])
+def test_ragged(case, impl, chunk):
+    seed, batch, dim, N, L, dt, gate, wd, wb, sp = case
+    p = custom(seed, batch, dim, N, L, dt, gate, wd, wb, sp)
+    y, hl = run(p, impl, chunk)
+    compare(p, y, hl, f"ragged/{impl}{chunk or ''}")
+
+
+@pytest.mark.parametrize("impl", ["fwd", "chunked"])
+def test_unaligned_rows_and_pointers(impl):
+    """Tensors that start 1 element past an allocation (not 16-byte aligned) take the scalar path."""
+    p = custom(31, 2, 40, 16, 96, torch.bfloat16)
+    def shift(t):
+        if t is None:
+            return None
+        flat = torch.empty(t.numel() + 1, dtype=t.dtype, device=DEV)
+        v = flat[1:].view(t.shape)
+        v.copy_(t)
+        return v
+    q = I.Problem("shifted", shift(p.u), shift(p.delta), p.A, shift(p.B), shift(p.C), p.D, shift(p.z), p.delta_bias)
+    y, hl = run(q, impl, 16)
+    compare(q, y, hl, f"unaligned/{impl}")
+
+
+@pytest.mark.parametrize("impl", ["fwd", "chunked"])
+def test_empty_and_degenerate(impl):
+    # L = 0: nothing to scan; the final state is the zero start
+    p = custom(41, 2, 8, 4, 0)
+    hl = torch.full((2, 8, 4), 7.0, device=DEV)
+    y = run_out = (ss.scan_fwd if impl == "fwd" else ss.scan_chunked)(
+        p.u, p.delta, p.A, p.B, p.C, D=p.D, z=p.z, delta_bias=p.delta_bias, last_state=hl)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(hl).item() == 0 and run_out[0].numel() == 0
+    # batch = 0 and dim = 0: no-ops
+    for bsz, dim in ((0, 8), (2, 0)):
+        q = custom(42, max(bsz, 1), max(dim, 1), 4, 16)
+        u = torch.empty((bsz, dim, 16), device=DEV)
+        A = torch.empty((dim, 4), device=DEV)
+        BC = torch.empty((bsz, 4, 16), device=DEV)
+        out = ss.scan_fwd(u, u, A, BC, BC)
+        assert out.shape == (bsz, dim, 16)
+    # N = 0: only the gated skip term remains
+    q = custom(43, 2, 12, 0, 50)
+    y, hl = run(q, impl, 8)
+    compare(q, y, hl, f"N=0/{impl}")
+
+
+def test_two_faces_agree():
+    """L decode steps from a zero state == scan_fwd == scan_chunked at several chunk lengths."""
+    p = custom(51, 2, 70, 16, 129, torch.float32)
+    yf, hf = run(p, "fwd")
+    for c in (1, 7, 64, 2048):
+        yc, hc = run(p, "chunked", c)
+        check(host(yc), host(yf), False, f"chunked{c} vs fwd y")
+        check(host(hc), host(hf), False, f"chunked{c} vs fwd state")
+    st = torch.zeros((2, 70, 16), device=DEV)
+    ys = []
+    for t in range(p.seqlen):
+        ys.append(ss.state_update(st, p.u[:, :, t].contiguous(), p.delta[:, :, t].contiguous(), p.A,
+                                  p.B[:, :, t].contiguous(), p.C[:, :, t].contiguous(), D=p.D, z=p.z[:, :, t].contiguous(),
+                                  delta_bias=p.delta_bias))
+    yd = torch.stack(ys, dim=2)
+    check(host(yd), host(yf), False, "decode x L vs fwd y")
+    check(host(st), host(hf), False, "decode x L vs fwd state")
+    compare(p, yf, hf, "two-faces/fwd")
+
+
+def test_zero_step_keeps_state_bitwise():
+    """dt = 0 (softplus off, raw delta 0, no bias): Abar = 1 and nothing is written into the state."""
+    g = torch.Generator(device=DEV).manual_seed(61)
+    st = torch.randn((4, 300, 16), device=DEV, generator=g)
+    before = st.clone()
+    u = torch.randn((4, 300), device=DEV, generator=g)
+    BC = torch.randn((4, 16), device=DEV, generator=g)
+    A = -torch.rand((300, 16), device=DEV, generator=g) - 0.5
+    y = ss.state_update(st, u, torch.zeros_like(u), A, BC, BC, D=torch.ones(300, device=DEV), softplus=False)
+    torch.cuda.synchronize()
+    assert torch.equal(st, before)
+    want = torch.einsum("bdn,bn->bd", before.double(), BC.double()) + u.double()
+    assert torch.max(torch.abs(y.double() - want)).item() <= 1e-5 * torch.max(torch.abs(want)).item()
+
+
+def test_status_codes_on_device():
+    p = custom(71, 1, 16, 16, 64)
+    with pytest.raises(ss.SSError) as e:
+        ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, chunk_len=16, workspace=torch.empty(8, dtype=torch.uint8, device=DEV))
+    assert e.value.status == ss.SS_EWORKSPACE
+    A65 = torch.zeros((16, 65), device=DEV)
+    BC65 = torch.zeros((1, 65, 64), device=DEV)
+    with pytest.raises(ss.SSError) as e:
+        ss.scan_fwd(p.u, p.delta, A65, BC65, BC65)
+    assert e.value.status == ss.SS_EINVAL
