@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark of the B300 selective scan (Mamba S6).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One "step" is one chunked forward scan (local pass, carry, fix-up: every row
+of the forward hot path) over the Mamba-2.8B-shaped long-sequence workload:
+batch 1, D = 5120 channels, N = 16 states, L = 65536 steps, chunk 2048, bf16
+u/delta/B/C/z, fp32 A/D/delta_bias/state/y, synthetic seeded inputs resident
+in HBM.  The inputs (3.4 GB) are far larger than the 126 MB L2, so no flush
+is needed between steps.
+
+Rank 0 prints one JSON line.  `value` is B*D*L elements per second for the
+whole job (every rank runs its own replica of the workload: the scan shards
+over independent channels and batch rows, with no collective on the data
+path).  The line also carries the roofline of the dominant kernel, the whole
+step's roofline, per-kernel times measured with CUDA events inside the timed
+region, the end-to-end figure through host buffers, clocks sampled during the
+timed region, a decode measurement, and the fp64 oracle timed on the host
+cores as a CPU baseline.
+
+`--impl reference` times the fp64 CPU oracle instead (the reference arm):
+same metric and workload, a bounded sample of channels per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+
+METRIC = "scan throughput (B·D·L elems/s, HBM GB/s) and % of HBM/SFU roofline, 1×B300"
+WORKLOAD = "mamba2p8b_long_bf16"
+CHUNK = 2048
+SMS = 148
+SM_MAX_MHZ = 2032.0
+EX2_PER_CLK_PER_SM = 32          # MUFU.EX2 issue rate of sm_103 (31.85/clk/SM measured on this machine's B300)
+
+
+# ----------------------------------------------------------------- roofline model
+
+def workload_counts(batch, dim, dstate, seqlen, in_bytes=2, gate=True):
+    """Algorithmic bytes and exponentials of one forward scan.
+    bytes: u, delta (and z) read once, y written once (fp32), B and C read once per
+    batch row, A, D, delta_bias read once, the final state written once.
+    exps: N discretization exps per element, one in the softplus, one in the SiLU gate."""
+    elems = batch * dim * seqlen
+    per_elem = in_bytes * (3 if gate else 2) + 4
+    byts = elems * per_elem + batch * 2 * dstate * seqlen * in_bytes + dim * dstate * 4 + 2 * dim * 4 \
+        + batch * dim * dstate * 4
+    exps = elems * (dstate + 1 + (1 if gate else 0))
+    return elems, byts, exps
+
+
+def peaks():
+    path = os.path.join(HERE, "MEASURED_PEAKS.json")
+    hbm, src = 6400.0, "fallback"
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        hbm, src = float(pk.get("hbm_gbs", hbm)), "measured"
+    sfu = SMS * EX2_PER_CLK_PER_SM * SM_MAX_MHZ * 1e6 / 1e12     # Texp/s at the maximum SM clock
+    return {"hbm_gbs": hbm, "hbm_src": src, "sfu_texps": sfu}
+
+
+def roofline_terms(byts, exps, ms, pk):
+    t = ms * 1e-3
+    gbs = byts / t / 1e9
+    texps = exps / t / 1e12
+    t_hbm = byts / (pk["hbm_gbs"] * 1e9)
+    t_sfu = exps / (pk["sfu_texps"] * 1e12)
+    if t_sfu >= t_hbm:
+        return {"bound": "alu", "achieved": round(texps, 4), "peak": round(pk["sfu_texps"], 4), "unit": "Texp/s",
+                "frac": round(texps / pk["sfu_texps"], 4), "hbm_gbs": round(gbs, 1),
+                "hbm_frac": round(gbs / pk["hbm_gbs"], 4)}
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / pk["hbm_gbs"], 4), "texps": round(texps, 4)}
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 50 ms) while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.idx = device_index
+        self.out = ""
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.idx is not None:
+            cmd += ["-i", str(self.idx)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), float(f[2]), float(f[3]), f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [r for r in rows if r[3] >= 50] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(busy), "power_w_max": max(r[2] for r in busy)}
+
+
+def device_index_for_smi(torch):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    local = torch.cuda.current_device()
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids):
+            return ids[local]
+    return local
+
+
+# ----------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def barrier_and_max(value: float, world: int):
+    """The maximum of `value` over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- CPU baseline (oracle)
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(p, nchan):
+    """Host copies of the first `nchan` channels of a problem (wire format for the oracle)."""
+    from selective_state_space_117_b300 import inputs as I
+    sub = lambda t: I.to_wire(t[:, :nchan].contiguous()) if t is not None else None
+    sub0 = lambda t: I.to_wire(t[:nchan].contiguous()) if t is not None else None
+    return dict(u=sub(p.u), delta=sub(p.delta), z=sub(p.z), A=sub0(p.A), D=sub0(p.D), delta_bias=sub0(p.delta_bias),
+                B=I.to_wire(p.B), C=I.to_wire(p.C))
+
+
+def time_oracle(sample, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.scan(sample["u"], sample["delta"], sample["A"], sample["B"], sample["C"], D=sample["D"], z=sample["z"],
+                delta_bias=sample["delta_bias"], softplus=True, dtype="bf16", nthreads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(p, budget_s=15.0):
+    """The oracle on the host cores over a bounded channel sample (about `budget_s` of wall time)."""
+    import oracle
+    oracle.build()
+    threads = host_threads()
+    L = p.seqlen
+    probe = oracle_sample(p, min(threads, p.dim))
+    per_chan = time_oracle(probe, threads) / min(threads, p.dim)
+    nchan = int(min(p.dim, max(threads, budget_s / max(per_chan, 1e-9))))
+    nchan = min(p.dim, max(threads, (nchan // threads) * threads))
+    sample = oracle_sample(p, nchan)
+    dt = time_oracle(sample, threads)
+    elems = p.batch * nchan * L
+    return {"value": elems / dt, "unit": "elem/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nchan} of {p.dim} channels x L={L} (fp64 C oracle, OpenMP over channels), {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------- the reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from selective_state_space_117_b300 import inputs as I
+    import oracle
+    oracle.build()
+    p = I.workload(WORKLOAD, device="cpu", gen_device="cpu", dim=512)   # the channels the samples draw from
+    threads = host_threads()
+    probe = oracle_sample(p, threads)
+    per_chan = time_oracle(probe, threads) / threads
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    nchan = max(1, int(min(512, max(threads, budget / max(per_chan, 1e-9)))))
+    sample = oracle_sample(p, nchan)
+    for _ in range(args.warmup):
+        time_oracle(sample, threads)
+    t = [time_oracle(sample, threads) for _ in range(args.steps)]
+    tot = sum(t)
+    elems = nchan * p.seqlen
+    value = elems * args.steps / tot
+    cfg = {"workload": f"{WORKLOAD}: batch=1, D=5120, N=16, L=65536, chunk {CHUNK}; bf16 inputs, fp32 state",
+           "sample_per_step": f"{nchan} channels x L={p.seqlen}"}
+    line = {"metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "elem/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{nchan} channels x L={p.seqlen} per step"},
+            "e2e": {"value": value, "unit": "elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl")
+    import selective_state_space_117_b300 as ss
+    from selective_state_space_117_b300 import inputs as I
+
+    pk = peaks()
+    p = I.workload(WORKLOAD, device="cuda", gen_device="cuda", dim=args.dim)
+    Bt, Dm, N, L = p.batch, p.dim, p.dstate, p.seqlen
+    elems, byts, exps = workload_counts(Bt, Dm, N, L)
+    y = torch.empty((Bt, Dm, L), dtype=torch.float32, device="cuda")
+    hl = torch.empty((Bt, Dm, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty((ss.chunked_workspace_bytes(Bt, Dm, N, L, CHUNK),), dtype=torch.uint8, device="cuda")
+    kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, chunk_len=CHUNK, y=y, last_state=hl, workspace=ws)
+    phases = [(ss.PHASE_LOCAL, "local"), (ss.PHASE_CARRY, "carry"), (ss.PHASE_FIXUP, "fixup")]
+
+    def step(evs=None):
+        for i, (ph, _) in enumerate(phases):
+            ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, phase=ph, **kw)
+            if evs is not None:
+                evs[i + 1].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device_index_for_smi(torch)) as clk:
+        time.sleep(0.3)                  # let the sampler start before the timed region
+        barrier(world)
+        torch.cuda.synchronize()
+        t0.record()
+        for k in range(args.steps):
+            ev[k][0].record()
+            step(ev[k])
+        t1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    total_ms = barrier_and_max(t0.elapsed_time(t1), world)
+    ms = total_ms / args.steps
+    per_kernel = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps))
+                  for i, (_, name) in enumerate(phases)}
+    ksum = sum(per_kernel.values())
+    dominant = max(per_kernel, key=per_kernel.get)
+    value = elems * world / (ms * 1e-3)
+
+    # Roofline of the dominant kernel.  The fix-up pass produces every output, so its algorithmic
+    # work is the whole forward scan's; the local and carry passes are the overhead of chunking.
+    line_kernels = {n: {"ms": round(v, 4), "share": round(v / ksum, 4)} for n, v in per_kernel.items()}
+    roof_dom = roofline_terms(byts, exps, per_kernel[dominant], pk)
+    roof_dom.update({"kernel": f"{dominant} pass", "traffic": None,
+                     "peak_src": ("derived: 148 SMs x 32 MUFU.EX2/clk/SM x 2032 MHz" if roof_dom["bound"] == "alu"
+                                  else pk["hbm_src"])})
+    roof_step = roofline_terms(byts, exps, ms, pk)
+
+    e2e = None if args.no_e2e else bench_e2e(ss, torch, p, y, hl, ws, world, elems, min(5, args.steps))
+    dec = None if args.no_decode else bench_decode(ss, I, torch, pk)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: batch=1, D={Dm}, N=16, L=65536, chunk {CHUNK}",
+                   "entry_point": "ss_scan_chunked (phases local, carry, fixup)",
+                   "inputs": "bf16 u/delta/B/C/z; fp32 A/D/delta_bias/state/y; arithmetic fp32",
+                   "l2": f"no flush: inputs {byts / 1e9:.2f} GB per step >> 126 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs": round(byts / (ms * 1e-3) / 1e9, 1),
+        "roofline": roof_dom,
+        "roofline_step": roof_step,
+        "kernels": line_kernels,
+        "e2e": e2e,
+        "gpu_launches": args.steps * len(phases),
+        "clocks": clk.summary(),
+        "peaks": pk,
+    }
+    if dec is not None:
+        line["decode"] = dec
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_e2e(ss, torch, p, y, hl, ws, world, elems, e2e_steps):
+    """The same scan through the public API with pinned host buffers: every step copies its
+    inputs host->device and its outputs (y, final state) device->host inside the timed region."""
+    e2e_steps = max(1, e2e_steps)
+    Bt, Dm, N, L = p.batch, p.dim, p.dstate, p.seqlen
+    hp = {k: getattr(p, k).cpu().pin_memory() for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias")}
+    hy = torch.empty((Bt, Dm, L), dtype=torch.float32).pin_memory()
+    hh = torch.empty((Bt, Dm, N), dtype=torch.float32).pin_memory()
+    dp = {k: torch.empty_like(v, device="cuda") for k, v in hp.items()}
+    h2d = sum(v.numel() * v.element_size() for v in hp.values())
+    d2h = hy.numel() * 4 + hh.numel() * 4
+
+    def e2e_step():
+        for k, v in hp.items():
+            dp[k].copy_(v, non_blocking=True)
+        ss.scan_chunked(dp["u"], dp["delta"], dp["A"], dp["B"], dp["C"], D=dp["D"], z=dp["z"],
+                        delta_bias=dp["delta_bias"], chunk_len=CHUNK, y=y, last_state=hl, workspace=ws)
+        hy.copy_(y, non_blocking=True)
+        hh.copy_(hl, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record()
+    torch.cuda.synchronize()
+    e2e_ms = barrier_and_max(a0.elapsed_time(a1), world) / e2e_steps
+    del dp, hp, hy, hh
+    return {"value": elems * world / (e2e_ms * 1e-3), "unit": "elem/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
+
+
+def bench_decode(ss, I, torch, pk, steps=1024, batch=256, dim=5120, dstate=16):
+    """The recurrence face: 1024 sequential decode steps on a (256, 5120, 16) fp32 state,
+    captured once in a CUDA graph and replayed."""
+    s = I.decode_stream(batch=batch, dim=dim, dstate=dstate, steps=steps, device="cuda", gen_device="cuda")
+    state = torch.zeros((batch, dim, dstate), dtype=torch.float32, device="cuda")
+    y = torch.empty((batch, dim), dtype=torch.float32, device="cuda")
+
+    def run_all():
+        for t in range(steps):
+            ss.state_update(state, s.u[t], s.delta[t], s.A, s.B[t], s.C[t], D=s.D, z=s.z[t], delta_bias=s.delta_bias,
+                            y=y)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run_all()                                   # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run_all()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    state.zero_()
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    per_step_bytes = batch * dim * (2 * dstate * 4 + 3 * 2 + 4) + batch * 2 * dstate * 2 + dim * (dstate + 2) * 4
+    us = ms * 1e3 / steps
+    gbs = per_step_bytes / (us * 1e-6) / 1e9
+    del s
+    return {"workload": f"decode_256x5120: batch={batch}, D={dim}, N={dstate}, {steps} sequential steps, bf16 "
+                        "inputs drawn per step, fp32 state", "entry_point": "ss_state_update (CUDA-graph replay)",
+            "us_per_step": round(us, 2), "algorithmic_bytes_per_step": per_step_bytes,
+            "gbs": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm_gbs"], 4),
+            "note": "the 83.9 MB state fits in the 126 MB L2, so steps can exceed the HBM roofline",
+            "gpu_launches": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dim", type=int, default=5120, help="channels (5120 = the workload; smaller only for profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

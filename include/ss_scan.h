@@ -117,6 +117,22 @@ int ss_scan_chunked(const ss_dims* dims, const void* u, const void* delta, const
                     ss_stream_t stream);
 
 /*
+ * One phase of ss_scan_chunked, for callers that schedule the phases
+ * themselves (for example to time them, or to run other work between them).
+ * Calling phases SS_PHASE_LOCAL, SS_PHASE_CARRY and SS_PHASE_FIXUP in this
+ * order on one stream, with the same arguments and workspace, is exactly
+ * ss_scan_chunked.  Each phase launches one kernel.  The carry phase writes
+ * last_state; the fix-up phase writes y.
+ */
+typedef enum { SS_PHASE_LOCAL = 1, SS_PHASE_CARRY = 2, SS_PHASE_FIXUP = 3 } ss_phase;
+
+int ss_scan_chunked_phase(int phase, const ss_dims* dims, const void* u, const void* delta, const float* A,
+                          const void* B, const void* C, const float* D, const void* z,
+                          const float* delta_bias, int softplus_flag, float* y, float* last_state,
+                          int64_t chunk_len, void* workspace, size_t workspace_bytes,
+                          ss_stream_t stream);
+
+/*
  * One decode step on a persistent state (the recurrence face: "each new token
  * only updates a fixed-size state", mernstackdev.com, FAQ; the state of
  * shape (batch, dim, N) is the fixed-size memory of "The state, in bytes",

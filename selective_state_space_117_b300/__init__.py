@@ -68,6 +68,9 @@ def lib():
         L.ss_scan_chunked.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, i64, vp,
                                       ctypes.c_size_t, vp]
         L.ss_scan_chunked.restype = ctypes.c_int
+        L.ss_scan_chunked_phase.argtypes = [ctypes.c_int, dp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp,
+                                            i64, vp, ctypes.c_size_t, vp]
+        L.ss_scan_chunked_phase.restype = ctypes.c_int
         L.ss_state_update.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
         L.ss_state_update.restype = ctypes.c_int
         L.ss_status_string.argtypes = [ctypes.c_int]
@@ -163,11 +166,16 @@ def chunked_workspace_bytes(batch, dim, dstate, seqlen, chunk_len, dtype=F32) ->
     return int(lib().ss_scan_chunked_workspace_bytes(ctypes.byref(dims), int(chunk_len)))
 
 
+PHASE_LOCAL, PHASE_CARRY, PHASE_FIXUP = 1, 2, 3
+
+
 def scan_chunked(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, chunk_len=2048, y=None,
-                 last_state=None, return_last_state=False, workspace=None, stream=None):
+                 last_state=None, return_last_state=False, workspace=None, stream=None, phase=None):
     """Chunked selective scan (local scan, carry across chunks, fix-up).  Same
     result and return convention as ``scan_fwd``.  ``workspace`` is an optional
-    uint8 CUDA tensor of at least ``chunked_workspace_bytes`` bytes."""
+    uint8 CUDA tensor of at least ``chunked_workspace_bytes`` bytes.  With
+    ``phase`` in (1, 2, 3) only that phase runs (ss_scan_chunked_phase); the
+    three phases in order on one stream, sharing a workspace, are the full call."""
     dims, y = _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state)
     if return_last_state and last_state is None:
         last_state = torch.empty((dims.batch, dims.dim, dims.dstate), dtype=torch.float32, device=u.device)
@@ -176,10 +184,13 @@ def scan_chunked(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=Tr
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=u.device)
     if workspace.device != u.device or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
-    st = lib().ss_scan_chunked(ctypes.byref(dims), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                               _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(last_state),
-                               int(chunk_len), _ptr(workspace), workspace.numel(), _stream(u.device, stream))
-    _check(st, "ss_scan_chunked")
+    args = (ctypes.byref(dims), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            int(bool(softplus)), _ptr(y), _ptr(last_state), int(chunk_len), _ptr(workspace), workspace.numel(),
+            _stream(u.device, stream))
+    if phase is None:
+        _check(lib().ss_scan_chunked(*args), "ss_scan_chunked")
+    else:
+        _check(lib().ss_scan_chunked_phase(int(phase), *args), f"ss_scan_chunked_phase({phase})")
     return (y, last_state) if last_state is not None else y
 
 

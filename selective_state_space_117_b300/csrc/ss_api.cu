@@ -112,17 +112,18 @@ size_t ss_scan_chunked_workspace_bytes(const ss_dims* dims, int64_t chunk_len) {
   return align_up(s_bytes, kWsAlign) + h_bytes;
 }
 
-int ss_scan_chunked(const ss_dims* dims, const void* u, const void* delta, const float* A, const void* B,
-                    const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
-                    float* y, float* last_state, int64_t chunk_len, void* workspace, size_t workspace_bytes,
-                    ss_stream_t stream) {
+int ss_scan_chunked_phase(int phase, const ss_dims* dims, const void* u, const void* delta, const float* A,
+                          const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                          int softplus_flag, float* y, float* last_state, int64_t chunk_len, void* workspace,
+                          size_t workspace_bytes, ss_stream_t stream) {
+  if (phase < SS_PHASE_LOCAL || phase > SS_PHASE_FIXUP) return SS_EINVAL;
   const int st = check_scan(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
   if (st != SS_OK) return st;
   if (chunk_len < 1) return SS_EINVAL;
   const ss_dims& d = *dims;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (d.batch == 0 || d.dim == 0) return SS_OK;
-  if (d.seqlen == 0) return zero_state(d, last_state, s);
+  if (d.seqlen == 0) return phase == SS_PHASE_CARRY ? zero_state(d, last_state, s) : SS_OK;
   const size_t need = ss_scan_chunked_workspace_bytes(dims, chunk_len);
   if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes < need) return SS_EWORKSPACE;
   ssk::ScanArgs a = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
@@ -133,10 +134,24 @@ int ss_scan_chunked(const ss_dims* dims, const void* u, const void* delta, const
                                     align_up((size_t)(d.batch * d.dim * a.nchunks) * sizeof(float), kWsAlign));
   const dim3 grid((unsigned)(a.ctiles * a.nchunks), (unsigned)d.batch);
   const bool bf = d.in_dtype == SS_BF16;
-  if (ssk::launch_scan_local(a, bf, grid, s) != 0) return SS_EINVAL;
-  ssk::launch_carry(a, s);
-  ssk::launch_scan_fixup(a, bf, z != nullptr, grid, s);
+  int rc = 0;
+  if (phase == SS_PHASE_LOCAL) rc = ssk::launch_scan_local(a, bf, grid, s);
+  else if (phase == SS_PHASE_CARRY) rc = ssk::launch_carry(a, s);
+  else rc = ssk::launch_scan_fixup(a, bf, z != nullptr, grid, s);
+  if (rc != 0) return SS_EINVAL;
   return launched();
+}
+
+int ss_scan_chunked(const ss_dims* dims, const void* u, const void* delta, const float* A, const void* B,
+                    const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                    float* y, float* last_state, int64_t chunk_len, void* workspace, size_t workspace_bytes,
+                    ss_stream_t stream) {
+  for (int phase = SS_PHASE_LOCAL; phase <= SS_PHASE_FIXUP; ++phase) {
+    const int st = ss_scan_chunked_phase(phase, dims, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y,
+                                         last_state, chunk_len, workspace, workspace_bytes, stream);
+    if (st != SS_OK) return st;
+  }
+  return SS_OK;
 }
 
 int ss_state_update(const ss_dims* dims, float* state, const void* u, const void* delta, const float* A,
