@@ -176,7 +176,11 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
   a.delta_bias = delta_bias; a.y = y;
   a.batch = d.batch; a.dim = d.dim; a.dstate = d.dstate;
   a.softplus = softplus_flag ? 1 : 0;
-  const dim3 grid((unsigned)ceil_div(d.dim, ssk::kThreads), (unsigned)d.batch);
+  const uintptr_t bc_align = d.in_dtype == SS_BF16 ? 8 : 16;
+  a.vec = (d.dstate % 4 == 0 && aligned(state, 16) && aligned(A, 16) && aligned(B, bc_align) && aligned(C, bc_align))
+              ? 1 : 0;
+  if (ceil_div(d.batch * d.dim * 16, ssk::kDecodeThreads) > kMaxGridX) return SS_EINVAL;
+  const dim3 grid(1);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (ssk::launch_decode(a, d.in_dtype == SS_BF16, z != nullptr, grid, s) != 0) return SS_EINVAL;
   return launched();

@@ -1,37 +1,49 @@
-// Launchers of the chunked scan's first two phases: the zero-start local scan
-// of every chunk (mode kLocal) and the carry pass across chunks.
+// Launchers of the chunked scan's first two phases: the zero-start end state
+// of every chunk (local_kernel) and the carry pass across chunks.
 #include "ss_dispatch.cuh"
 #include "ss_kernels.cuh"
 #include "ss_launch.h"
 
 namespace ssk {
 
-// Exclusive scan over chunks of the pairs (P_k, H_k) = (exp(A * sum_k dt), chunk end state),
-// one thread per (b, d, n):  carry_0 = 0,  carry_{k+1} = P_k * carry_k + H_k.
-// Overwrites ws_H[k] with carry_k (the true state entering chunk k) and writes
-// the final state after the last chunk.
+// Exclusive scan over chunks of the pairs (P_k, H_k) = (exp(A * S_k), chunk end state) under
+// (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2), one thread per (b, d, n):
+//   carry_0 = 0,   carry_{k+1} = P_k * carry_k + H_k.
+// Overwrites the workspace's H_k with carry_k (the true state entering chunk k) and writes the
+// final state after the last chunk.  Loads are issued 8 chunks ahead of the dependent chain.
 __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t N = a.dstate;
   if (i >= a.batch * a.dim * N) return;
   const int64_t n = i % N, bd = i / N, d = bd % a.dim;
   const float A2 = a.A[d * N + n] * kLog2e;
-  float H = 0.f;
-  for (int64_t k = 0; k < a.nchunks; ++k) {
-    const int64_t o = (bd * a.nchunks + k) * N + n;
-    const float he = a.ws_H[o];
-    const float S = a.ws_S[bd * a.nchunks + k];
-    a.ws_H[o] = H;
-    H = fmaf(ex2(A2 * S), H, he);
+  const int64_t K = a.nchunks;
+  float* H = a.ws_H + bd * K * N + n;
+  const float* S = a.ws_S + bd * K;
+  float c = 0.f;
+  for (int64_t k0 = 0; k0 < K; k0 += 8) {
+    float he[8], sk[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool ok = k0 + u < K;
+      he[u] = ok ? H[(k0 + u) * N] : 0.f;
+      sk[u] = ok ? S[k0 + u] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (k0 + u < K) {
+        H[(k0 + u) * N] = c;
+        c = fmaf(ex2(A2 * sk[u]), c, he[u]);
+      }
+    }
   }
-  if (a.last_state) a.last_state[bd * N + n] = H;
+  if (a.last_state) a.last_state[bd * N + n] = c;
 }
-
 
 int launch_scan_local(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s) {
   SSK_DISPATCH_NT(a.dstate, {
-    if (bf16) scan_kernel<NT, true, false, kLocal><<<grid, kThreads, 0, s>>>(a);
-    else scan_kernel<NT, false, false, kLocal><<<grid, kThreads, 0, s>>>(a);
+    if (bf16) local_kernel<NT, true><<<grid, kThreads, 0, s>>>(a);
+    else local_kernel<NT, false><<<grid, kThreads, 0, s>>>(a);
   });
   return 0;
 }

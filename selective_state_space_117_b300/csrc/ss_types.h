@@ -6,10 +6,10 @@
 namespace ssk {
 
 constexpr int kThreads = 128;  // channels per block
-constexpr int kTile = 32;      // time steps per shared-memory tile
 constexpr int kGroup = 8;      // time steps per vector load
+constexpr int kDecodeThreads = 256;
 
-enum Mode { kFull = 0, kLocal = 1, kFixup = 2 };
+enum Mode { kFull = 0, kFixup = 2 };
 
 struct ScanArgs {
   const void* u;
@@ -44,6 +44,7 @@ struct DecodeArgs {
   float* y;
   int64_t batch, dim, dstate;
   int softplus;
+  int vec;           // 1: N % 4 == 0 and state, A, B, C rows allow 16/8-byte vector access
 };
 
 }  // namespace ssk

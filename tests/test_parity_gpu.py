@@ -319,3 +319,48 @@ def test_status_codes_on_device():
     with pytest.raises(ss.SSError) as e:
         ss.scan_fwd(p.u, p.delta, A65, BC65, BC65)
     assert e.value.status == ss.SS_EINVAL
+
+
+@pytest.mark.parametrize("N", [1, 5, 16, 20, 33, 64])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("shift", [False, True], ids=["aligned", "unaligned"])
+def test_decode_ragged(N, dtype, shift):
+    """Several decode steps from a random state, for state sizes that pad to the next
+    supported width, against the oracle's recurrence step by step."""
+    g = torch.Generator().manual_seed(80 + N)
+    batch, dim, steps = 3, 70, 6
+    st0 = torch.randn((batch, dim, N), generator=g)
+    if shift:                                  # state rows not 16-byte aligned: scalar path
+        flat = torch.empty(st0.numel() + 1, device=DEV)
+        state = flat[1:].view(batch, dim, N)
+        state.copy_(st0.to(DEV))
+    else:
+        state = st0.to(DEV).clone()
+    A = (-torch.exp(torch.rand((dim, N), generator=g) * 2.0 - 1.0)).to(DEV)
+    D = torch.randn((dim,), generator=g).to(DEV)
+    bias = (torch.rand((dim,), generator=g) * 2.0 - 3.0).to(DEV)
+    sref = st0.double().numpy().reshape(batch * dim, N).copy()
+    w = I.to_wire
+    for t in range(steps):
+        u = torch.randn((batch, dim), generator=g).to(dtype).to(DEV)
+        dl = torch.randn((batch, dim), generator=g).to(dtype).to(DEV)
+        z = torch.randn((batch, dim), generator=g).to(dtype).to(DEV)
+        Bm = (torch.randn((batch, N), generator=g) * 0.5).to(dtype).to(DEV)
+        Cm = (torch.randn((batch, N), generator=g) * 0.5).to(dtype).to(DEV)
+        y = ss.state_update(state, u, dl, A, Bm, Cm, D=D, z=z, delta_bias=bias)
+        yr = oracle.state_update(sref, w(u), w(dl), w(A), w(Bm), w(Cm), D=w(D), z=w(z), delta_bias=w(bias),
+                                 dtype="bf16" if dtype == torch.bfloat16 else "f32")
+        bf = dtype == torch.bfloat16
+        check(host(y).reshape(-1), yr, bf, f"decode N={N} step {t} y")
+    check(host(state).reshape(batch * dim, N), sref, dtype == torch.bfloat16, f"decode N={N} state")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_chunked_local_pass_cutoff(dtype):
+    """Large steps (dt ~ 2..5): every state's weight underflows a few dozen steps back from a
+    chunk's end, so the local pass stops early; the result must still match the oracle."""
+    p = custom(91, 2, 200, 16, 1024, dtype)
+    p.delta_bias = torch.full((200,), 2.5, device=DEV)
+    for chunk in (256, 64):
+        y, hl = run(p, "chunked", chunk)
+        compare(p, y, hl, f"cutoff/chunked{chunk}")
