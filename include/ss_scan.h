@@ -147,6 +147,38 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
                     const void* z, const float* delta_bias, int softplus_flag, float* y,
                     ss_stream_t stream);
 
+/*
+ * ss_scan_chunked without a caller-provided workspace, for callers that cannot
+ * allocate device memory themselves: code running where cudaMalloc is not
+ * allowed or not wanted (inside a custom allocator or memory pool, a plugin
+ * host that owns all device allocations, or a deployment that forbids
+ * allocation after start-up).  The pages have no counterpart of this entry
+ * point; it only changes who owns the workspace.
+ *
+ * The workspace is a fixed array of SS_STATIC_WORKSPACE_BYTES bytes inside the
+ * library: every GPU that loads the library holds it until the process exits.
+ * The caller still passes every input and output, as for ss_scan_chunked.
+ *   - Returns SS_EWORKSPACE, without touching the device, when
+ *     ss_scan_chunked_workspace_bytes(dims, chunk_len) exceeds
+ *     SS_STATIC_WORKSPACE_BYTES (16 MiB: for example batch 1, dim 5120, N 16,
+ *     L 65536 with chunk 2048 needs 11.2 MB).
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (under a lock, with that device current) and keeps
+ *     it; make that first call before capturing any stream on that device.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Every call, on every stream, uses the same array, which keeps the last
+ *     call's contents (nothing in it needs clearing: each call writes every
+ *     entry before reading it).  Calls that overlap on the GPU (on different
+ *     streams, or from several host threads) race on it: serialise them.
+ * Other arguments, results and errors as ss_scan_chunked.
+ */
+#define SS_STATIC_WORKSPACE_BYTES (16u << 20)
+
+int ss_scan_chunked_static(const ss_dims* dims, const void* u, const void* delta, const float* A,
+                           const void* B, const void* C, const float* D, const void* z,
+                           const float* delta_bias, int softplus_flag, float* y, float* last_state,
+                           int64_t chunk_len, ss_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* ss_status_string(int status);
 

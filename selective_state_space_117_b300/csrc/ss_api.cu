@@ -2,6 +2,8 @@
 // kernel launches on the caller's stream.  See include/ss_scan.h for the
 // contract of every entry point.
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "ss_launch.h"
@@ -202,3 +204,53 @@ const char* ss_status_string(int status) {
 int ss_last_cuda_error(void) { return g_last_cuda; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// ss_scan_chunked_static: the chunked scan on a workspace that the library owns.
+//
+// The workspace is one file-scope __device__ array of SS_STATIC_WORKSPACE_BYTES.
+// In host code the name g_static_ws is only a host-side handle for the symbol,
+// not a device address, so it is never passed to a kernel; its device address
+// is looked up once per device with cudaGetSymbolAddress (with that device
+// current) and cached.
+namespace {
+
+__device__ __align__(256) unsigned char g_static_ws[SS_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxStaticDevices = 256;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxStaticDevices];
+
+int static_workspace(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxStaticDevices) return SS_EINVAL;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_ws);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return SS_OK;
+}
+
+}  // namespace
+
+extern "C" int ss_scan_chunked_static(const ss_dims* dims, const void* u, const void* delta, const float* A,
+                                      const void* B, const void* C, const float* D, const void* z,
+                                      const float* delta_bias, int softplus_flag, float* y, float* last_state,
+                                      int64_t chunk_len, ss_stream_t stream) {
+  if (!dims || chunk_len < 1) return SS_EINVAL;
+  // Reject problems whose workspace does not fit before touching the device.
+  if (ss_scan_chunked_workspace_bytes(dims, chunk_len) > (size_t)SS_STATIC_WORKSPACE_BYTES) return SS_EWORKSPACE;
+  void* ws = nullptr;
+  const int st = static_workspace(&ws);
+  if (st != SS_OK) return st;
+  // The chunked phases write every workspace entry before reading it, so the
+  // previous call's contents need no clearing.
+  return ss_scan_chunked(dims, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, chunk_len, ws,
+                         (size_t)SS_STATIC_WORKSPACE_BYTES, stream);
+}
