@@ -260,7 +260,7 @@ def run_ours(args):
     from selective_state_space_117_b300 import inputs as I
 
     pk = peaks()
-    p = I.workload(WORKLOAD, device="cuda", gen_device="cuda", dim=args.dim)
+    p = I.workload(WORKLOAD, device="cuda", gen_device="cuda", dim=args.dim, seqlen=args.seqlen)
     Bt, Dm, N, L = p.batch, p.dim, p.dstate, p.seqlen
     elems, byts, exps = workload_counts(Bt, Dm, N, L)
     y = torch.empty((Bt, Dm, L), dtype=torch.float32, device="cuda")
@@ -315,7 +315,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: batch=1, D={Dm}, N=16, L=65536, chunk {CHUNK}",
+        "config": {"workload": f"{WORKLOAD}: batch=1, D={Dm}, N=16, L={L}, chunk {CHUNK}",
                    "entry_point": "ss_scan_chunked (phases local, carry, fixup)",
                    "inputs": "bf16 u/delta/B/C/z; fp32 A/D/delta_bias/state/y; arithmetic fp32",
                    "l2": f"no flush: inputs {byts / 1e9:.2f} GB per step >> 126 MB L2",
@@ -427,6 +427,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dim", type=int, default=5120, help="channels (5120 = the workload; smaller only for profiling)")
+    ap.add_argument("--seqlen", type=int, default=65536, help="steps (65536 = the workload; shorter only for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -45,7 +45,7 @@ int check_scan(const ss_dims* dims, const void* u, const void* delta, const floa
   if (d.in_dtype != SS_F32 && d.in_dtype != SS_BF16) return SS_EDTYPE;
   if (d.batch < 0 || d.dim < 0 || d.dstate < 0 || d.seqlen < 0) return SS_EINVAL;
   if (d.dstate > SS_MAX_DSTATE || d.batch > kMaxGridY) return SS_EINVAL;
-  if (ceil_div(d.dim, ssk::kThreads) > kMaxGridX) return SS_EINVAL;
+  if (ceil_div(d.dim, ssk::kCh) > kMaxGridX) return SS_EINVAL;
   const size_t es = in_size(d.in_dtype);
   const bool rows = d.batch > 0 && d.dim > 0 && d.seqlen > 0;
   if (rows && (!u || !delta || !y)) return SS_EINVAL;
@@ -66,13 +66,16 @@ ssk::ScanArgs make_scan_args(const ss_dims& d, const void* u, const void* delta,
   a.batch = d.batch; a.dim = d.dim; a.dstate = d.dstate; a.seqlen = d.seqlen;
   a.chunk_len = chunk_len;
   a.nchunks = ceil_div(d.seqlen, chunk_len);
-  a.ctiles = (int)ceil_div(d.dim, ssk::kThreads);
+  a.ctiles = (int)ceil_div(d.dim, ssk::kCh);
   a.softplus = softplus_flag ? 1 : 0;
   // 16-byte vector loads along a row need every row start and every group start aligned.
   const size_t es = in_size(d.in_dtype);
   const bool rows16 = (d.seqlen * (int64_t)es) % 16 == 0 && (d.seqlen * 4) % 16 == 0;
   const bool ptr16 = aligned(u, 16) && aligned(delta, 16) && aligned(z, 16) && aligned(y, 16);
   a.vec = (rows16 && ptr16 && chunk_len % ssk::kGroup == 0) ? 1 : 0;
+  // B/C rows are staged in 8-step segments from tile starts that are multiples of 8 steps.
+  const bool bc16 = (d.seqlen * (int64_t)es) % 16 == 0 && aligned(B, 16) && aligned(C, 16);
+  a.vec_bc = (bc16 && chunk_len % ssk::kGroup == 0) ? 1 : 0;
   return a;
 }
 
@@ -164,7 +167,7 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
   if (d.in_dtype != SS_F32 && d.in_dtype != SS_BF16) return SS_EDTYPE;
   if (d.batch < 0 || d.dim < 0 || d.dstate < 0 || d.dstate > SS_MAX_DSTATE || d.batch > kMaxGridY)
     return SS_EINVAL;
-  if (ceil_div(d.dim, ssk::kThreads) > kMaxGridX) return SS_EINVAL;
+  if (ceil_div(d.dim, ssk::kCh) > kMaxGridX) return SS_EINVAL;
   if (d.batch == 0 || d.dim == 0) return SS_OK;
   if (!u || !delta || !y) return SS_EINVAL;
   if (d.dstate > 0 && (!state || !A || !B || !C)) return SS_EINVAL;

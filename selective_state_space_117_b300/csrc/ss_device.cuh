@@ -5,9 +5,10 @@
 // ex2(x * log2(e)); A is pre-multiplied by log2(e) once per thread so the
 // per-state discretization exp(dt * A) is one multiply and one MUFU.EX2.
 //
-// Pairs of fp32 values travel in one 64-bit register ("f2") and are combined
-// with the packed fma/mul/add.rn.f32x2 instructions of sm_100+, which issue
-// two FP32 operations per instruction slot.
+// Pairs of fp32 values travel as float2 ("f2") in an aligned register pair and
+// are combined with the packed f32x2 fma/mul/add of sm_100+ (the __ffma2_rn,
+// __fmul2_rn and __fadd2_rn builtins), which issue two FP32 operations per
+// instruction slot.
 #pragma once
 
 #include <cstdint>
@@ -29,40 +30,34 @@ __device__ __forceinline__ float rcp(float x) {
   return r;
 }
 
+// Per-thread asynchronous 16-byte copy global -> shared (L2 only), its group
+// fences, and a 16-byte shared load.  All four are volatile asm statements, so
+// the compiler keeps them in program order relative to each other (a ring
+// slot is read only after the wait that covers its copy) while it may still
+// schedule ordinary arithmetic around them.
+__device__ __forceinline__ unsigned smem_addr(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void cp_async16(unsigned sa, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N)); }
+__device__ __forceinline__ uint4 lds16(unsigned sa) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(sa));
+  return v;
+}
+
 // ---------------------------------------------------------------- packed pairs
 
-typedef unsigned long long f2;
+typedef float2 f2;
 
-__device__ __forceinline__ f2 pk(float lo, float hi) {
-  f2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float lo(f2 v) {
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-  return a;
-}
-__device__ __forceinline__ float hi(f2 v) {
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-  return b;
-}
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-  f2 r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-  f2 r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f2 add2(f2 a, f2 b) {
-  f2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
+__device__ __forceinline__ f2 pk(float lo, float hi) { return make_float2(lo, hi); }
+__device__ __forceinline__ float lo(f2 v) { return v.x; }
+__device__ __forceinline__ float hi(f2 v) { return v.y; }
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ f2 add2(f2 a, f2 b) { return __fadd2_rn(a, b); }
 // ex2 of both halves.
 __device__ __forceinline__ f2 ex2x2(f2 x) { return pk(ex2(lo(x)), ex2(hi(x))); }
 
@@ -121,6 +116,12 @@ __device__ __forceinline__ f2 softplus2(f2 x) {
 // silu(z) = z * sigmoid(z) = z / (1 + e^-z).  For z -> -inf, e^-z -> inf and rcp -> 0.
 __device__ __forceinline__ float silu(float z) { return z * rcp(1.f + ex2(-z * kLog2e)); }
 
+// silu of both halves.
+__device__ __forceinline__ f2 silu2(f2 z) {
+  const f2 d = add2(ex2x2(mul2(z, splat(-kLog2e))), splat(1.f));
+  return mul2(z, pk(rcp(lo(d)), rcp(hi(d))));
+}
+
 // ---------------------------------------------------------------- bf16
 
 // bf16 bit pattern (low 16 bits of `bits`) widened exactly to fp32.
@@ -135,6 +136,8 @@ struct In;
 
 template <>
 struct In<false> {
+  static constexpr unsigned kBytes = 4;
+  static __device__ __forceinline__ const void* addr(const void* p, int64_t i) { return static_cast<const float*>(p) + i; }
   static __device__ __forceinline__ float one(const void* p, int64_t i) { return __ldg(static_cast<const float*>(p) + i); }
   // Raw storage of 8 consecutive elements (two 16-byte loads from a 16-byte aligned offset).
   struct Raw8 { float4 a, b; };
@@ -147,10 +150,24 @@ struct In<false> {
     const float4& q = j < 2 ? r.a : r.b;
     return (j & 1) ? pk(q.z, q.w) : pk(q.x, q.y);
   }
+  static __device__ __forceinline__ Raw8 pack8(const float (&v)[8]) {
+    return Raw8{make_float4(v[0], v[1], v[2], v[3]), make_float4(v[4], v[5], v[6], v[7])};
+  }
+  // 8 elements live in kVec 16-byte chunks; chunk v at shared address sa + v * stride_bytes.
+  static constexpr int kVec = 2;
+  static __device__ __forceinline__ Raw8 from_smem(unsigned sa, unsigned stride_bytes) {
+    const uint4 a = lds16(sa), b = lds16(sa + stride_bytes);
+    return Raw8{make_float4(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z), __uint_as_float(a.w)),
+                make_float4(__uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z), __uint_as_float(b.w))};
+  }
 };
 
 template <>
 struct In<true> {
+  static constexpr unsigned kBytes = 2;
+  static __device__ __forceinline__ const void* addr(const void* p, int64_t i) {
+    return static_cast<const unsigned short*>(p) + i;
+  }
   static __device__ __forceinline__ float one(const void* p, int64_t i) {
     return bf16_lo(__ldg(static_cast<const unsigned short*>(p) + i));
   }
@@ -161,6 +178,46 @@ struct In<true> {
   static __device__ __forceinline__ f2 pair(const Raw8& r, int j) {
     const uint32_t w = j == 0 ? r.a.x : j == 1 ? r.a.y : j == 2 ? r.a.z : r.a.w;
     return bf16x2(w);
+  }
+  // Values that are exact bf16 numbers (widened by one()), back to their bit patterns.
+  static __device__ __forceinline__ Raw8 pack8(const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) w[p] = (__float_as_uint(v[2 * p]) >> 16) | (__float_as_uint(v[2 * p + 1]) & 0xffff0000u);
+    return Raw8{make_uint4(w[0], w[1], w[2], w[3])};
+  }
+  static constexpr int kVec = 1;
+  static __device__ __forceinline__ Raw8 from_smem(unsigned sa, unsigned) { return Raw8{lds16(sa)}; }
+};
+
+// A per-thread ring of 8-step input groups in shared memory, filled by
+// cp.async ahead of use.  Slot s holds, for each of NA input arrays, this
+// thread's kVec 16-byte chunks; chunk v of array k of thread i sits at byte
+// ((s * NA + k) * kVec + v) * kThreads * 16 + i * 16, so a warp's reads of one
+// chunk are 512 contiguous bytes.  `src[k]` is the global address of this
+// thread's group 0 of array k and `step` the byte distance between groups
+// (negative to walk backward).
+template <bool BF, int NA, int kThreads, int kSlots>
+struct Ring {
+  using L = In<BF>;
+  static constexpr unsigned kChunkStride = kThreads * 16;
+  static constexpr unsigned kArr = L::kVec * kChunkStride;
+  static constexpr unsigned kSlot = NA * kArr;
+  static constexpr unsigned kBytes = kSlots * kSlot;
+  unsigned base;
+  const char* src[NA];
+  int64_t step;
+
+  __device__ __forceinline__ void put(int gi) const {
+    const unsigned s = base + (unsigned)(gi % kSlots) * kSlot;
+    const int64_t off = (int64_t)gi * step;
+#pragma unroll
+    for (int k = 0; k < NA; ++k)
+#pragma unroll
+      for (int v = 0; v < L::kVec; ++v) cp_async16(s + k * kArr + v * kChunkStride, src[k] + off + 16 * v);
+  }
+  __device__ __forceinline__ typename L::Raw8 get(int gi, int k) const {
+    return L::from_smem(base + (unsigned)(gi % kSlots) * kSlot + k * kArr, kChunkStride);
   }
 };
 

@@ -1,21 +1,22 @@
-// Selective scan kernels (sm_103a).
+// Selective scan kernels over (batch row, channel, chunk) units (sm_103a).
 //
 // Work decomposition: one thread owns one (batch row b, channel d, chunk k)
 // and keeps that channel's N states in registers for the whole chunk, so the
 // (batch, L, dim, N) expanded state never leaves the SM ("Kernel fusion",
 // "Mamba: Linear-Time Sequence Modeling with Selective State Spaces").  A
-// block is 128 consecutive channels of one (b, k).  All of them read the same
-// B_t and C_t, which the block stages through shared memory (converted to
-// fp32, double-buffered: the next tile is loaded into registers while the
-// current one is consumed) and every thread reads as broadcast 16-byte loads.
-// u, delta and z are read along each thread's own row with 16-byte vector
-// loads, one group of 8 steps ahead of use; y is written the same way.
+// block is kCh consecutive channels of one (b, k).  All of them read the same
+// B_t and C_t, which the block stages through shared memory as fp32 tiles of
+// Tile<NT>::kSteps steps (double-buffered; the next tile's raw values are
+// fetched into registers while the current tile is consumed) and every thread
+// reads as broadcast 16-byte loads.  u, delta and z are read along each
+// thread's own row as 16-byte vectors, one group of 8 steps ahead of use; y is
+// written the same way.
 //
-// Arithmetic runs on state pairs with the packed f32x2 instructions: per
-// pair and step one mul (dt*A), two MUFU.EX2, one mul (du*B), one fma (the
-// state) and one fma (the readout C*h).
+// Arithmetic runs on state pairs with the packed f32x2 instructions: per pair
+// and step one mul (dt*A'), two MUFU.EX2, one mul (du*B), one fma (the state)
+// and one fma (the readout C*h), where A' = A*log2(e).
 //
-// Modes of scan_kernel:
+// scan_kernel modes:
 //   kFull   start from h = 0, write y and (optionally) the final state
 //   kFixup  start from the carried-in state in the workspace, write y
 // local_kernel is the first phase of the chunked scan (see its comment).
@@ -26,208 +27,245 @@
 
 namespace ssk {
 
-// Time steps per shared-memory tile: NT * tile = 1024 keeps the staging work
-// at 8 values per thread and array for every state count.
+// B/C tile geometry: kSteps * NT = 512 values per array, so one tile is one
+// 8-step segment of B and one of C per thread (kCh = 64 threads).
 template <int NT>
-struct TileOf {
-  static constexpr int kSteps = 1024 / NT;
-  static constexpr int kRow = NT + 4;  // fp32 row stride: a 16-byte multiple
-  static constexpr int kPerThread = NT * kSteps / kThreads;
+struct Tile {
+  static constexpr int kSteps = 512 / NT;
+  static constexpr int kSegs = kSteps / kGroup;  // 8-step segments per state row
+  static_assert(NT * kSegs == kCh, "one B segment and one C segment per thread");
 };
 
-// Cooperative load of one tile of B (and C) rows [tt0, tt0 + tn) into registers,
-// and its store (transposed to [t][n], fp32) into shared memory.
-template <int NT, bool BF, bool WITH_C>
-struct Stager {
+// Shared-memory ring of 8-step input groups: slots, and how many groups ahead they are filled.
+constexpr int kStages = 4;
+constexpr int kAhead = kStages - 1;
+
+// Register ceiling: the state count decides how many blocks of kCh threads
+// must fit on an SM.  NT <= 16: 8 blocks (16 warps, 4 per scheduler) leave
+// 128 registers per thread; the launcher may run fewer blocks per SM to even
+// out the last wave (ss_occupancy.cuh).
+#ifndef SSK_MINB16
+#define SSK_MINB16 8
+#endif
+template <int NT, bool BF>
+struct MinBlocks {
+  static constexpr int value = NT <= 16 ? SSK_MINB16 : (NT == 32 ? 5 : 3);
+};
+
+// One 8-step segment of a B or C state row, fetched raw into registers and
+// stored transposed ([t][n], fp32) into a shared-memory tile.
+template <int NT, bool BF>
+struct Segment {
   using L = In<BF>;
-  using T = TileOf<NT>;
-  float b[T::kPerThread], c[WITH_C ? T::kPerThread : 1];
+  typename L::Raw8 raw;
 
-  __device__ __forceinline__ void load(const ScanArgs& a, int64_t bc_row, int64_t tt0, int tn, int N, int tid) {
+  // Row n of `src` (offset `row0` = (b, n, 0)), steps [t, t + 8) clipped to t_end.
+  __device__ __forceinline__ void load(const void* src, int64_t off, bool ok_row, int64_t t, int64_t t_end, bool vec) {
+    if (ok_row && vec && t + kGroup <= t_end) {
+      raw = L::load8(src, off);
+    } else {
+      float v[kGroup];
 #pragma unroll
-    for (int k = 0; k < T::kPerThread; ++k) {
-      const int e = tid + k * kThreads;
-      const int n = e / T::kSteps, j = e % T::kSteps;
-      const bool ok = n < N && j < tn;
-      const int64_t off = bc_row + (int64_t)n * a.seqlen + tt0 + j;
-      b[k] = ok ? L::one(a.B, off) : 0.f;
-      if (WITH_C) c[k] = ok ? L::one(a.C, off) : 0.f;
+      for (int j = 0; j < kGroup; ++j) v[j] = (ok_row && t + j < t_end) ? L::one(src, off + j) : 0.f;
+      raw = L::pack8(v);
     }
   }
-  __device__ __forceinline__ void store(float* sB, float* sC, int tid) const {
+  __device__ __forceinline__ void store(float* tile, int n, int tseg) const {
 #pragma unroll
-    for (int k = 0; k < T::kPerThread; ++k) {
-      const int e = tid + k * kThreads;
-      const int n = e / T::kSteps, j = e % T::kSteps;
-      sB[j * T::kRow + n] = b[k];
-      if (WITH_C) sC[j * T::kRow + n] = c[k];
+    for (int p = 0; p < kGroup / 2; ++p) {
+      const f2 v = L::pair(raw, p);
+      tile[(tseg * kGroup + 2 * p) * NT + n] = lo(v);
+      tile[(tseg * kGroup + 2 * p + 1) * NT + n] = hi(v);
     }
   }
 };
+
+// The unit of work of this block: rows, time range and channel.
+struct Unit {
+  int64_t b, d, k, bd, row, bc_row, t_begin, t_end;
+  bool active;
+};
+
+__device__ __forceinline__ Unit unit_of(const ScanArgs& a) {
+  Unit w;
+  const int ct = blockIdx.x % a.ctiles;
+  w.k = blockIdx.x / a.ctiles;
+  w.b = blockIdx.y;
+  w.d = (int64_t)ct * kCh + threadIdx.x;
+  w.active = w.d < a.dim;
+  w.t_begin = w.k * a.chunk_len;
+  w.t_end = min(a.seqlen, w.t_begin + a.chunk_len);
+  w.bd = w.b * a.dim + (w.active ? w.d : 0);
+  w.row = w.bd * a.seqlen;
+  w.bc_row = w.b * a.dstate * a.seqlen;
+  return w;
+}
+
+// Per-step scalars of one 8-step group: dt, du = dt*u as pairs (steps 2p, 2p+1).
+template <bool BF>
+__device__ __forceinline__ void step_scalars(const typename In<BF>::Raw8& ru, const typename In<BF>::Raw8& rd,
+                                             f2 bias2, int softplus, f2 (&dt2)[4], f2 (&du2)[4]) {
+  using L = In<BF>;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const f2 x = add2(L::pair(rd, p), bias2);
+    dt2[p] = softplus ? softplus2(x) : x;
+    du2[p] = mul2(dt2[p], L::pair(ru, p));
+  }
+}
 
 template <int NT, bool BF, bool HAS_Z, int MODE>
-__global__ void __launch_bounds__(kThreads) scan_kernel(const ScanArgs a) {
+__global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(const ScanArgs a) {
   using L = In<BF>;
-  using T = TileOf<NT>;
+  using T = Tile<NT>;
   constexpr int NP = NT / 2;
-  __shared__ __align__(16) float sB[2][T::kSteps * T::kRow];
-  __shared__ __align__(16) float sC[2][T::kSteps * T::kRow];
+  constexpr int NA = HAS_Z ? 3 : 2;             // input arrays in the ring: u, delta (, z)
+  using RingT = Ring<BF, NA, kCh, kStages>;
+  __shared__ __align__(16) float sB[2][T::kSteps * NT];
+  __shared__ __align__(16) float sC[2][T::kSteps * NT];
+  __shared__ __align__(16) unsigned char sIn[RingT::kBytes];
 
   const int tid = threadIdx.x;
-  const int ct = blockIdx.x % a.ctiles;
-  const int64_t k = blockIdx.x / a.ctiles;
-  const int64_t b = blockIdx.y;
-  const int64_t d = (int64_t)ct * kThreads + tid;
-  const bool active = d < a.dim;
+  const Unit w = unit_of(a);
   const int N = (int)a.dstate;
-  const int64_t t_begin = k * a.chunk_len;
-  const int64_t t_end = min(a.seqlen, t_begin + a.chunk_len);
-  const int64_t bd = b * a.dim + (active ? d : 0);
-  const int64_t row = bd * a.seqlen;                 // (b, d, 0)
-  const int64_t bc_row = b * (int64_t)N * a.seqlen;  // (b, 0, 0)
 
   // Padding states n >= N keep B = C = 0 (their staged values are zero), A = 0 and h = 0.
   f2 A2[NP], h[NP];
-  const float* Arow = a.A + (active ? d : 0) * N;
+  const float* Arow = a.A + (w.active ? w.d : 0) * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     const int n0 = 2 * q, n1 = 2 * q + 1;
-    A2[q] = pk((active && n0 < N) ? Arow[n0] * kLog2e : 0.f, (active && n1 < N) ? Arow[n1] * kLog2e : 0.f);
+    A2[q] = pk((w.active && n0 < N) ? Arow[n0] * kLog2e : 0.f, (w.active && n1 < N) ? Arow[n1] * kLog2e : 0.f);
     float h0 = 0.f, h1 = 0.f;
-    if (MODE == kFixup && active) {
-      const float* H = a.ws_H + (bd * a.nchunks + k) * N;
+    if (MODE == kFixup && w.active) {
+      const float* H = a.ws_H + (w.bd * a.nchunks + w.k) * N;
       if (n0 < N) h0 = H[n0];
       if (n1 < N) h1 = H[n1];
     }
     h[q] = pk(h0, h1);
   }
-  const float bias = (a.delta_bias && active) ? a.delta_bias[d] : 0.f;
-  const float Dd = (a.D && active) ? a.D[d] : 0.f;
+  const float bias = (a.delta_bias && w.active) ? a.delta_bias[w.d] : 0.f;
+  const float Dd = (a.D && w.active) ? a.D[w.d] : 0.f;
   const f2 bias2 = pk(bias, bias), D2 = pk(Dd, Dd);
 
-  // Prefetch of the first group of 8 steps (vector path only).
-  typename L::Raw8 ru{}, rd{}, rz{};
-  bool have = active && a.vec && t_begin + kGroup <= t_end;
-  if (have) {
-    ru = L::load8(a.u, row + t_begin);
-    rd = L::load8(a.delta, row + t_begin);
-    if (HAS_Z) rz = L::load8(a.z, row + t_begin);
-  }
+  // This thread's B and C segment of every tile.
+  const int sn = tid % NT, tseg = tid / NT;
+  const bool srow = sn < N;
+  const int64_t soff = w.bc_row + (int64_t)sn * a.seqlen + tseg * kGroup;
+  Segment<NT, BF> segB, segC;
+  segB.load(a.B, soff + w.t_begin, srow, w.t_begin + tseg * kGroup, w.t_end, a.vec_bc);
+  segC.load(a.C, soff + w.t_begin, srow, w.t_begin + tseg * kGroup, w.t_end, a.vec_bc);
+  segB.store(sB[0], sn, tseg);
+  segC.store(sC[0], sn, tseg);
 
-  Stager<NT, BF, true> st;
-  st.load(a, bc_row, t_begin, (int)min((int64_t)T::kSteps, t_end - t_begin), N, tid);
-  st.store(sB[0], sC[0], tid);
+  // Full 8-step groups go through the ring (vector path); the rest is scalar.
+  const int nfull = (w.active && a.vec) ? (int)((w.t_end - w.t_begin) / kGroup) : 0;
+  RingT ring;
+  ring.base = smem_addr(sIn) + tid * 16;
+  ring.src[0] = static_cast<const char*>(L::addr(a.u, w.row + w.t_begin));
+  ring.src[1] = static_cast<const char*>(L::addr(a.delta, w.row + w.t_begin));
+  if (HAS_Z) ring.src[NA - 1] = static_cast<const char*>(L::addr(a.z, w.row + w.t_begin));
+  ring.step = kGroup * L::kBytes;
+  if (nfull > 0)
+    for (int gi = 0; gi < kAhead; ++gi) {
+      if (gi < nfull) ring.put(gi);
+      cp_async_commit();
+    }
   __syncthreads();
 
   int buf = 0;
-  for (int64_t tt0 = t_begin; tt0 < t_end; tt0 += T::kSteps) {
-    const int tn = (int)min((int64_t)T::kSteps, t_end - tt0);
+  for (int64_t tt0 = w.t_begin; tt0 < w.t_end; tt0 += T::kSteps) {
+    const int tn = (int)min((int64_t)T::kSteps, w.t_end - tt0);
     const int64_t nx0 = tt0 + T::kSteps;
-    const bool more = nx0 < t_end;
-    if (more) st.load(a, bc_row, nx0, (int)min((int64_t)T::kSteps, t_end - nx0), N, tid);
-
-    if (active) {
+    const bool more = nx0 < w.t_end;
+    if (more) {
+      segB.load(a.B, soff + nx0, srow, nx0 + tseg * kGroup, w.t_end, a.vec_bc);
+      segC.load(a.C, soff + nx0, srow, nx0 + tseg * kGroup, w.t_end, a.vec_bc);
+    }
+    if (w.active) {
       const float* cB = sB[buf];
       const float* cC = sC[buf];
       for (int g = 0; g < tn; g += kGroup) {
         const int64_t t = tt0 + g;
-        const int nv = min(kGroup, tn - g);
-        // ---- this group's inputs as pairs
-        f2 u2[4], x2[4], z2[4];
-        if (have) {
+        const int gi = (int)((t - w.t_begin) / kGroup);
+        if (gi < nfull) {
+          if (gi + kAhead < nfull) ring.put(gi + kAhead);
+          cp_async_commit();
+          cp_async_wait<kAhead>();
+          const typename L::Raw8 cu = ring.get(gi, 0);
+          const typename L::Raw8 rd = ring.get(gi, 1);
+          typename L::Raw8 cz{};
+          if (HAS_Z) cz = ring.get(gi, NA - 1);
+          f2 dt2[4], du2[4];
+          step_scalars<BF>(cu, rd, bias2, a.softplus, dt2, du2);
+          // ---- the recurrence over 8 steps, no bounds checks
+          float yo[kGroup];
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            u2[p] = L::pair(ru, p);
-            x2[p] = L::pair(rd, p);
-            z2[p] = HAS_Z ? L::pair(rz, p) : pk(0.f, 0.f);
-          }
-        } else {
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            float v[3][2];
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-              const int j = 2 * p + s;
-              const bool ok = j < nv;
-              v[0][s] = ok ? L::one(a.u, row + t + j) : 0.f;
-              v[1][s] = ok ? L::one(a.delta, row + t + j) : 0.f;
-              v[2][s] = (HAS_Z && ok) ? L::one(a.z, row + t + j) : 0.f;
-            }
-            u2[p] = pk(v[0][0], v[0][1]);
-            x2[p] = pk(v[1][0], v[1][1]);
-            z2[p] = pk(v[2][0], v[2][1]);
-          }
-        }
-        // ---- prefetch the next group
-        const int64_t tq = t + kGroup;
-        have = a.vec && tq + kGroup <= t_end;
-        if (have) {
-          ru = L::load8(a.u, row + tq);
-          rd = L::load8(a.delta, row + tq);
-          if (HAS_Z) rz = L::load8(a.z, row + tq);
-        }
-        // ---- per-step scalars for the group
-        f2 dt2[4], du2[4], y2[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const f2 x = add2(x2[p], bias2);
-          dt2[p] = a.softplus ? softplus2(x) : x;
-          du2[p] = mul2(dt2[p], u2[p]);
-          y2[p] = mul2(D2, u2[p]);
-        }
-        // ---- the recurrence, one step at a time
-        float yo[kGroup];
-#pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
-          yo[j] = 0.f;
-          if (j < nv) {
+          for (int j = 0; j < kGroup; ++j) {
             const float dt = (j & 1) ? hi(dt2[j >> 1]) : lo(dt2[j >> 1]);
             const float du = (j & 1) ? hi(du2[j >> 1]) : lo(du2[j >> 1]);
             const f2 dtp = pk(dt, dt), dup = pk(du, du);
-            f2 acc = pk((j & 1) ? hi(y2[j >> 1]) : lo(y2[j >> 1]), 0.f);
-            const float* rb = cB + (g + j) * T::kRow;
-            const float* rc = cC + (g + j) * T::kRow;
+            const float* rb = cB + (g + j) * NT;
+            const float* rc = cC + (g + j) * NT;
+            f2 acc;
 #pragma unroll
             for (int q = 0; q < NP; q += 2) {
               const float4 bv = *reinterpret_cast<const float4*>(rb + 2 * q);
               const float4 cv = *reinterpret_cast<const float4*>(rc + 2 * q);
-              const f2 e0 = ex2x2(mul2(dtp, A2[q]));
-              h[q] = fma2(e0, h[q], mul2(dup, pk(bv.x, bv.y)));
-              acc = fma2(pk(cv.x, cv.y), h[q], acc);
-              const f2 e1 = ex2x2(mul2(dtp, A2[q + 1]));
-              h[q + 1] = fma2(e1, h[q + 1], mul2(dup, pk(bv.z, bv.w)));
+              h[q] = fma2(ex2x2(mul2(dtp, A2[q])), h[q], mul2(dup, pk(bv.x, bv.y)));
+              acc = q == 0 ? mul2(pk(cv.x, cv.y), h[q]) : fma2(pk(cv.x, cv.y), h[q], acc);
+              h[q + 1] = fma2(ex2x2(mul2(dtp, A2[q + 1])), h[q + 1], mul2(dup, pk(bv.z, bv.w)));
               acc = fma2(pk(cv.z, cv.w), h[q + 1], acc);
             }
             yo[j] = lo(acc) + hi(acc);
           }
-        }
-        if (HAS_Z) {
+          // ---- skip term, gate, store
+          f2 y2[4];
 #pragma unroll
-          for (int j = 0; j < kGroup; ++j) {
-            const float z = (j & 1) ? hi(z2[j >> 1]) : lo(z2[j >> 1]);
-            yo[j] *= silu(z);
+          for (int p = 0; p < 4; ++p) {
+            y2[p] = fma2(D2, L::pair(cu, p), pk(yo[2 * p], yo[2 * p + 1]));
+            if (HAS_Z) y2[p] = mul2(y2[p], silu2(L::pair(cz, p)));
           }
-        }
-        if (nv == kGroup && a.vec) {
-          float4* qy = reinterpret_cast<float4*>(a.y + row + t);
-          qy[0] = make_float4(yo[0], yo[1], yo[2], yo[3]);
-          qy[1] = make_float4(yo[4], yo[5], yo[6], yo[7]);
+          float4* qy = reinterpret_cast<float4*>(a.y + w.row + t);
+          qy[0] = make_float4(lo(y2[0]), hi(y2[0]), lo(y2[1]), hi(y2[1]));
+          qy[1] = make_float4(lo(y2[2]), hi(y2[2]), lo(y2[3]), hi(y2[3]));
         } else {
+          // ---- scalar path: unaligned rows or the ragged end of the sequence
+          const int nv = min(kGroup, tn - g);
+          for (int j = 0; j < nv; ++j) {
+            const int64_t ix = w.row + t + j;
+            const float uu = L::one(a.u, ix);
+            const float x = L::one(a.delta, ix) + bias;
+            const float dt = a.softplus ? softplus(x) : x;
+            const f2 dtp = pk(dt, dt), dup = pk(dt * uu, dt * uu);
+            const float* rb = cB + (g + j) * NT;
+            const float* rc = cC + (g + j) * NT;
+            f2 acc = pk(0.f, 0.f);
 #pragma unroll
-          for (int j = 0; j < kGroup; ++j)
-            if (j < nv) a.y[row + t + j] = yo[j];
+            for (int q = 0; q < NP; ++q) {
+              const f2 bq = *reinterpret_cast<const f2*>(rb + 2 * q);
+              const f2 cq = *reinterpret_cast<const f2*>(rc + 2 * q);
+              h[q] = fma2(ex2x2(mul2(dtp, A2[q])), h[q], mul2(dup, bq));
+              acc = fma2(cq, h[q], acc);
+            }
+            float yv = fmaf(Dd, uu, lo(acc) + hi(acc));
+            if (HAS_Z) yv *= silu(L::one(a.z, ix));
+            a.y[ix] = yv;
+          }
         }
       }
     }
     if (more) {
-      st.store(sB[buf ^ 1], sC[buf ^ 1], tid);
+      segB.store(sB[buf ^ 1], sn, tseg);
+      segC.store(sC[buf ^ 1], sn, tseg);
       __syncthreads();
       buf ^= 1;
     }
   }
 
-  if (MODE == kFull && active && a.last_state) {
-    float* out = a.last_state + bd * N;
+  cp_async_wait<0>();
+  if (MODE == kFull && w.active && a.last_state) {
+    float* out = a.last_state + w.bd * N;
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
       if (2 * q < N) out[2 * q] = lo(h[q]);
@@ -241,121 +279,135 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanArgs a) {
 // and the chunk's sum of dt, computed backward from the chunk's end.  With
 // dt >= 0 (softplus on) R only grows, so once A[n] * R * log2(e) < -127 every
 // remaining weight exp2(.) of state n is below 2^-127 and flushes to zero in
-// fp32: such state pairs are skipped (per warp, per tile), and the loop stops
-// once no pair in the block is left.  The sum written is then partial, but
-// every exp(A[n] * sum) that the carry pass forms from it underflows to zero
+// fp32; the block stops at the first tile where that holds for every state
+// of every channel.  The sum written is then partial, but every
+// exp(A[n] * sum) that the carry pass forms from it underflows to zero
 // exactly as the full sum's would.
 template <int NT, bool BF>
-__global__ void __launch_bounds__(kThreads) local_kernel(const ScanArgs a) {
+__global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) local_kernel(const ScanArgs a) {
   using L = In<BF>;
-  using T = TileOf<NT>;
+  using T = Tile<NT>;
   constexpr int NP = NT / 2;
   constexpr float kDead = -127.f;
-  __shared__ __align__(16) float sB[T::kSteps * T::kRow];
+  using RingT = Ring<BF, 2, kCh, kStages>;     // u, delta
+  __shared__ __align__(16) float sB[2][T::kSteps * NT];
+  __shared__ __align__(16) unsigned char sIn[RingT::kBytes];
 
   const int tid = threadIdx.x;
-  const int ct = blockIdx.x % a.ctiles;
-  const int64_t k = blockIdx.x / a.ctiles;
-  const int64_t b = blockIdx.y;
-  const int64_t d = (int64_t)ct * kThreads + tid;
-  const bool active = d < a.dim;
+  const Unit w = unit_of(a);
   const int N = (int)a.dstate;
-  const int64_t t_begin = k * a.chunk_len;
-  const int64_t t_end = min(a.seqlen, t_begin + a.chunk_len);
-  const int64_t bd = b * a.dim + (active ? d : 0);
-  const int64_t row = bd * a.seqlen;
-  const int64_t bc_row = b * (int64_t)N * a.seqlen;
 
   f2 A2[NP], acc[NP];
-  float amax[NP];
-  const float* Arow = a.A + (active ? d : 0) * N;
+  float amax = -1e30f;  // the slowest decay of this channel (padding states never count)
+  const float* Arow = a.A + (w.active ? w.d : 0) * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     const int n0 = 2 * q, n1 = 2 * q + 1;
-    const float a0 = (active && n0 < N) ? Arow[n0] * kLog2e : 0.f;
-    const float a1 = (active && n1 < N) ? Arow[n1] * kLog2e : 0.f;
+    const float a0 = (w.active && n0 < N) ? Arow[n0] * kLog2e : 0.f;
+    const float a1 = (w.active && n1 < N) ? Arow[n1] * kLog2e : 0.f;
     A2[q] = pk(a0, a1);
-    // padding states never keep a pair alive
-    amax[q] = fmaxf(n0 < N ? a0 : -1e30f, n1 < N ? a1 : -1e30f);
+    if (n0 < N) amax = fmaxf(amax, a0);
+    if (n1 < N) amax = fmaxf(amax, a1);
     acc[q] = pk(0.f, 0.f);
   }
-  const float bias = (a.delta_bias && active) ? a.delta_bias[d] : 0.f;
+  const float bias = (a.delta_bias && w.active) ? a.delta_bias[w.d] : 0.f;
   const f2 bias2 = pk(bias, bias);
   const bool may_stop = a.softplus != 0;
   float R = 0.f;
 
-  const int64_t ntiles = (t_end - t_begin + T::kSteps - 1) / T::kSteps;
-  for (int64_t it = ntiles - 1; it >= 0; --it) {
-    const int64_t tt0 = t_begin + it * T::kSteps;
-    const int tn = (int)min((int64_t)T::kSteps, t_end - tt0);
-    // which pairs can still receive a non-zero weight in this tile (R only grows backward)
-    unsigned live = 0;
-#pragma unroll
-    for (int q = 0; q < NP; ++q) {
-      const bool mine = active && !(may_stop && amax[q] * R < kDead);
-      if (__any_sync(0xffffffffu, mine)) live |= 1u << q;
-    }
-    if (!__syncthreads_or(live != 0)) break;
-    Stager<NT, BF, false> st;
-    st.load(a, bc_row, tt0, tn, N, tid);
-    st.store(sB, nullptr, tid);
-    __syncthreads();
+  const int sn = tid % NT, tseg = tid / NT;
+  const bool srow = sn < N;
+  const int64_t soff = w.bc_row + (int64_t)sn * a.seqlen + tseg * kGroup;
+  const int64_t ntiles = (w.t_end - w.t_begin + T::kSteps - 1) / T::kSteps;
+  Segment<NT, BF> segB;
 
-    if (active) {
+  int64_t tt0 = w.t_begin + (ntiles - 1) * T::kSteps;
+  segB.load(a.B, soff + tt0, srow, tt0 + tseg * kGroup, w.t_end, a.vec_bc);
+  segB.store(sB[0], sn, tseg);
+  __syncthreads();
+
+  // Groups are taken from the chunk's end backward; with aligned rows and a
+  // chunk of whole groups every group goes through the ring, else none does.
+  const int ngr = (int)((w.t_end - w.t_begin + kGroup - 1) / kGroup);
+  const bool ring_on = w.active && a.vec && (w.t_end - w.t_begin) % kGroup == 0;
+  RingT ring;  // group j of the ring is the j-th group from the chunk's end
+  ring.base = smem_addr(sIn) + tid * 16;
+  ring.src[0] = static_cast<const char*>(L::addr(a.u, w.row + w.t_end - kGroup));
+  ring.src[1] = static_cast<const char*>(L::addr(a.delta, w.row + w.t_end - kGroup));
+  ring.step = -(int64_t)(kGroup * L::kBytes);
+  if (ring_on)
+    for (int j = 0; j < kAhead; ++j) {
+      if (j < ngr) ring.put(j);
+      cp_async_commit();
+    }
+
+  int buf = 0;
+  for (int64_t it = ntiles - 1; it >= 0; --it, tt0 -= T::kSteps) {
+    const int tn = (int)min((int64_t)T::kSteps, w.t_end - tt0);
+    const bool more = it > 0;
+    if (more) segB.load(a.B, soff + tt0 - T::kSteps, srow, tt0 - T::kSteps + tseg * kGroup, w.t_end, a.vec_bc);
+    if (w.active) {
+      const float* cB = sB[buf];
       const int ng = (tn + kGroup - 1) / kGroup;
       for (int gi = ng - 1; gi >= 0; --gi) {
         const int g = gi * kGroup;
         const int64_t t = tt0 + g;
-        const int nv = min(kGroup, tn - g);
-        f2 u2[4], x2[4];
-        if (a.vec && nv == kGroup) {
-          const typename L::Raw8 ru = L::load8(a.u, row + t), rd = L::load8(a.delta, row + t);
+        if (ring_on) {
+          const int j = ngr - 1 - (int)((t - w.t_begin) / kGroup);
+          if (j + kAhead < ngr) ring.put(j + kAhead);
+          cp_async_commit();
+          cp_async_wait<kAhead>();
+          const typename L::Raw8 ru = ring.get(j, 0);
+          const typename L::Raw8 rd = ring.get(j, 1);
+          f2 dt2[4], du2[4];
+          step_scalars<BF>(ru, rd, bias2, a.softplus, dt2, du2);
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            u2[p] = L::pair(ru, p);
-            x2[p] = L::pair(rd, p);
-          }
-        } else {
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const int j0 = 2 * p, j1 = 2 * p + 1;
-            u2[p] = pk(j0 < nv ? L::one(a.u, row + t + j0) : 0.f, j1 < nv ? L::one(a.u, row + t + j1) : 0.f);
-            x2[p] = pk(j0 < nv ? L::one(a.delta, row + t + j0) : 0.f, j1 < nv ? L::one(a.delta, row + t + j1) : 0.f);
-          }
-        }
-        f2 dt2[4], du2[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const f2 x = add2(x2[p], bias2);
-          dt2[p] = a.softplus ? softplus2(x) : x;
-          du2[p] = mul2(dt2[p], u2[p]);
-        }
-#pragma unroll
-        for (int j = kGroup - 1; j >= 0; --j) {
-          if (j < nv) {
+          for (int j = kGroup - 1; j >= 0; --j) {
             const float dt = (j & 1) ? hi(dt2[j >> 1]) : lo(dt2[j >> 1]);
             const float du = (j & 1) ? hi(du2[j >> 1]) : lo(du2[j >> 1]);
             const f2 Rp = pk(R, R), dup = pk(du, du);
-            const float* rb = sB + (g + j) * T::kRow;
+            const float* rb = cB + (g + j) * NT;
 #pragma unroll
             for (int q = 0; q < NP; q += 2) {
               const float4 bv = *reinterpret_cast<const float4*>(rb + 2 * q);
-              if (live & (1u << q))
-                acc[q] = fma2(ex2x2(mul2(Rp, A2[q])), mul2(dup, pk(bv.x, bv.y)), acc[q]);
-              if (live & (2u << q))
-                acc[q + 1] = fma2(ex2x2(mul2(Rp, A2[q + 1])), mul2(dup, pk(bv.z, bv.w)), acc[q + 1]);
+              acc[q] = fma2(ex2x2(mul2(Rp, A2[q])), mul2(dup, pk(bv.x, bv.y)), acc[q]);
+              acc[q + 1] = fma2(ex2x2(mul2(Rp, A2[q + 1])), mul2(dup, pk(bv.z, bv.w)), acc[q + 1]);
+            }
+            R += dt;
+          }
+        } else {
+          const int nv = min(kGroup, tn - g);
+          for (int j = nv - 1; j >= 0; --j) {
+            const int64_t ix = w.row + t + j;
+            const float x = L::one(a.delta, ix) + bias;
+            const float dt = a.softplus ? softplus(x) : x;
+            const float du = dt * L::one(a.u, ix);
+            const f2 Rp = pk(R, R), dup = pk(du, du);
+            const float* rb = cB + (g + j) * NT;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+              const f2 bq = *reinterpret_cast<const f2*>(rb + 2 * q);
+              acc[q] = fma2(ex2x2(mul2(Rp, A2[q])), mul2(dup, bq), acc[q]);
             }
             R += dt;
           }
         }
       }
     }
-    __syncthreads();
+    // Every weight left in this chunk underflows for every channel of the block: stop.
+    const bool dead = !w.active || (may_stop && amax * R < kDead);
+    if (__syncthreads_and(dead)) break;
+    if (more) {
+      segB.store(sB[buf ^ 1], sn, tseg);
+      __syncthreads();
+      buf ^= 1;
+    }
   }
 
-  if (!active) return;
-  a.ws_S[bd * a.nchunks + k] = R;
-  float* H = a.ws_H + (bd * a.nchunks + k) * N;
+  cp_async_wait<0>();
+  if (!w.active) return;
+  a.ws_S[w.bd * a.nchunks + w.k] = R;
+  float* H = a.ws_H + (w.bd * a.nchunks + w.k) * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     if (2 * q < N) H[2 * q] = lo(acc[q]);

@@ -3,6 +3,7 @@
 #include "ss_dispatch.cuh"
 #include "ss_kernels.cuh"
 #include "ss_launch.h"
+#include "ss_occupancy.cuh"
 
 namespace ssk {
 
@@ -40,10 +41,18 @@ __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
   if (a.last_state) a.last_state[bd * N + n] = c;
 }
 
+template <int NT, bool BF>
+static void go_local(const ScanArgs& a, dim3 grid, cudaStream_t s) {
+  auto k = local_kernel<NT, BF>;
+  size_t dyn = 0;
+  balanced_smem((const void*)k, kCh, (int64_t)grid.x * grid.y, &dyn);
+  k<<<grid, kCh, dyn, s>>>(a);
+}
+
 int launch_scan_local(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s) {
   SSK_DISPATCH_NT(a.dstate, {
-    if (bf16) local_kernel<NT, true><<<grid, kThreads, 0, s>>>(a);
-    else local_kernel<NT, false><<<grid, kThreads, 0, s>>>(a);
+    if (bf16) go_local<NT, true>(a, grid, s);
+    else go_local<NT, false>(a, grid, s);
   });
   return 0;
 }

@@ -5,7 +5,7 @@
 
 namespace ssk {
 
-constexpr int kThreads = 128;  // channels per block
+constexpr int kCh = 64;        // channels (threads) per scan block
 constexpr int kGroup = 8;      // time steps per vector load
 constexpr int kDecodeThreads = 256;
 
@@ -28,6 +28,7 @@ struct ScanArgs {
   int ctiles;        // channel tiles (blocks) per (b, chunk)
   int softplus;
   int vec;           // 1: every row start is 16-byte aligned for u, delta, z and y
+  int vec_bc;        // 1: every 8-step segment of a B or C row is 16-byte aligned
 };
 
 // One decode step, one thread per (b, d).
