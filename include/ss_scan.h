@@ -59,7 +59,7 @@ typedef enum {
     SS_EDTYPE = -3,      /* in_dtype is neither SS_F32 nor SS_BF16 */
     SS_EWORKSPACE = -4,  /* chunked workspace missing, too small or misaligned */
     SS_ECUDA = -5,       /* a CUDA launch or call failed (see ss_last_cuda_error) */
-    SS_ETIMEOUT = -6     /* reserved for bounded device-side waits */
+    SS_ETIMEOUT = -6     /* a bounded device-side wait gave up (see ss_device_status) */
 } ss_status;
 
 /* Largest supported state size N. */
@@ -185,6 +185,17 @@ const char* ss_status_string(int status);
 /* The CUDA error code (cudaError_t value) behind the last SS_ECUDA returned on
  * this host thread, or 0. */
 int ss_last_cuda_error(void);
+
+/*
+ * The status word of the current device.  Kernels that wait on their own
+ * asynchronous bulk copies bound every wait; one that gives up records it in
+ * this word, skips the rest of its work and returns (its outputs are then not
+ * valid) instead of hanging the device.  Returns SS_OK when no wait has given
+ * up since the word was last cleared, SS_ETIMEOUT otherwise, SS_ECUDA if the
+ * device could not be queried.  Synchronous: it first waits for all work on
+ * the current device (cudaDeviceSynchronize).  clear != 0 resets the word.
+ */
+int ss_device_status(int clear);
 
 #ifdef __cplusplus
 }

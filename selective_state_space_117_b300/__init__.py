@@ -20,7 +20,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["scan_fwd", "scan_chunked", "state_update", "chunked_workspace_bytes", "SSError", "library_path",
+__all__ = ["scan_fwd", "scan_chunked", "state_update", "chunked_workspace_bytes", "device_status", "SSError",
+           "library_path",
            "F32", "BF16", "MAX_DSTATE", "LAUNCHES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +78,8 @@ def lib():
         L.ss_status_string.restype = ctypes.c_char_p
         L.ss_last_cuda_error.argtypes = []
         L.ss_last_cuda_error.restype = ctypes.c_int
+        L.ss_device_status.argtypes = [ctypes.c_int]
+        L.ss_device_status.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -223,3 +226,12 @@ def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, soft
                                _stream(u.device, stream))
     _check(st, "ss_state_update")
     return y
+
+
+def device_status(clear: bool = False) -> int:
+    """Status word of the current device (ss_device_status): SS_OK, or SS_ETIMEOUT
+    when a kernel's bounded wait gave up.  Synchronises the device first."""
+    st = lib().ss_device_status(int(bool(clear)))
+    if st not in (SS_OK, SS_ETIMEOUT):
+        _check(st, "ss_device_status")
+    return st

@@ -36,6 +36,26 @@ constexpr size_t kWsAlign = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The device status word: kernels whose bounded waits give up record it here
+// (one word per device, looked up once per device with cudaGetSymbolAddress).
+__device__ int g_dev_status;
+
+constexpr int kMaxStatusDevices = 256;
+std::mutex g_status_mu;
+int* g_status_ptr[kMaxStatusDevices];
+
+int* device_status_word() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxStatusDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
 // Shape, dtype and pointer checks shared by the two full-sequence entry points.
 int check_scan(const ss_dims* dims, const void* u, const void* delta, const float* A, const void* B,
                const void* C, const float* D, const void* z, const float* delta_bias, const float* y,
@@ -76,6 +96,7 @@ ssk::ScanArgs make_scan_args(const ss_dims& d, const void* u, const void* delta,
   // B/C rows are staged in 8-step segments from tile starts that are multiples of 8 steps.
   const bool bc16 = (d.seqlen * (int64_t)es) % 16 == 0 && aligned(B, 16) && aligned(C, 16);
   a.vec_bc = (bc16 && chunk_len % ssk::kGroup == 0) ? 1 : 0;
+  a.err = device_status_word();
   return a;
 }
 
@@ -104,7 +125,10 @@ int ss_scan_fwd(const ss_dims* dims, const void* u, const void* delta, const flo
   const ssk::ScanArgs a = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
                                          d.seqlen);
   const dim3 grid((unsigned)a.ctiles, (unsigned)d.batch);
-  if (ssk::launch_scan_full(a, d.in_dtype == SS_BF16, z != nullptr, grid, s) != 0) return SS_EINVAL;
+  const bool bf = d.in_dtype == SS_BF16;
+  if (ssk::tma_usable(a, bf, ssk::kFull) && ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFull, grid, s) == 0)
+    return launched();
+  if (ssk::launch_scan_full(a, bf, z != nullptr, grid, s) != 0) return SS_EINVAL;
   return launched();
 }
 
@@ -142,7 +166,9 @@ int ss_scan_chunked_phase(int phase, const ss_dims* dims, const void* u, const v
   int rc = 0;
   if (phase == SS_PHASE_LOCAL) rc = ssk::launch_scan_local(a, bf, grid, s);
   else if (phase == SS_PHASE_CARRY) rc = ssk::launch_carry(a, s);
-  else rc = ssk::launch_scan_fixup(a, bf, z != nullptr, grid, s);
+  else if (!(ssk::tma_usable(a, bf, ssk::kFixup) &&
+             ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFixup, grid, s) == 0))
+    rc = ssk::launch_scan_fixup(a, bf, z != nullptr, grid, s);
   if (rc != 0) return SS_EINVAL;
   return launched();
 }
@@ -205,6 +231,21 @@ const char* ss_status_string(int status) {
 }
 
 int ss_last_cuda_error(void) { return g_last_cuda; }
+
+int ss_device_status(int clear) {
+  int* word = device_status_word();
+  if (!word) return cuda_fail(cudaGetLastError());
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  int v = 0;
+  e = cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (clear && v != 0) {
+    e = cudaMemset(word, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return v == 0 ? SS_OK : SS_ETIMEOUT;
+}
 
 }  // extern "C"
 

@@ -41,15 +41,14 @@ constexpr int kStages = 4;
 constexpr int kAhead = kStages - 1;
 
 // Register ceiling: the state count decides how many blocks of kCh threads
-// must fit on an SM.  NT <= 16: 8 blocks (16 warps, 4 per scheduler) leave
-// 128 registers per thread; the launcher may run fewer blocks per SM to even
-// out the last wave (ss_occupancy.cuh).
-#ifndef SSK_MINB16
-#define SSK_MINB16 8
-#endif
+// must fit on an SM.  NT <= 16: 6 blocks (12 warps, 3 per scheduler) leave
+// 168 registers per thread, which measured faster than 8 blocks at 128
+// registers (the compiler keeps more of each 8-step group in flight); the
+// launcher may run fewer blocks per SM to even out the last wave
+// (ss_occupancy.cuh).
 template <int NT, bool BF>
 struct MinBlocks {
-  static constexpr int value = NT <= 16 ? SSK_MINB16 : (NT == 32 ? 5 : 3);
+  static constexpr int value = NT <= 16 ? 6 : (NT == 32 ? 5 : 3);
 };
 
 // One 8-step segment of a B or C state row, fetched raw into registers and
@@ -111,6 +110,46 @@ __device__ __forceinline__ void step_scalars(const typename In<BF>::Raw8& ru, co
     const f2 x = add2(L::pair(rd, p), bias2);
     dt2[p] = softplus ? softplus2(x) : x;
     du2[p] = mul2(dt2[p], L::pair(ru, p));
+  }
+}
+
+// One full 8-step group of the forward recurrence for this thread's channel:
+// inputs as raw 8-element rows (u, delta, z), B and C of the 8 steps as fp32
+// rows of NT values at cB and cC, the state h updated in place, and the 8
+// outputs (skip term and gate applied) returned as pairs in y2.
+template <int NT, bool BF, bool HAS_Z>
+__device__ __forceinline__ void scan_group(const typename In<BF>::Raw8& cu, const typename In<BF>::Raw8& rd,
+                                           const typename In<BF>::Raw8& cz, f2 bias2, f2 D2, int softplus,
+                                           const f2 (&A2)[NT / 2], f2 (&h)[NT / 2], const float* cB,
+                                           const float* cC, f2 (&y2)[4]) {
+  using L = In<BF>;
+  constexpr int NP = NT / 2;
+  f2 dt2[4], du2[4];
+  step_scalars<BF>(cu, rd, bias2, softplus, dt2, du2);
+  float yo[kGroup];
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j) {
+    const float dt = (j & 1) ? hi(dt2[j >> 1]) : lo(dt2[j >> 1]);
+    const float du = (j & 1) ? hi(du2[j >> 1]) : lo(du2[j >> 1]);
+    const f2 dtp = pk(dt, dt), dup = pk(du, du);
+    const float* rb = cB + j * NT;
+    const float* rc = cC + j * NT;
+    f2 acc;
+#pragma unroll
+    for (int q = 0; q < NP; q += 2) {
+      const float4 bv = *reinterpret_cast<const float4*>(rb + 2 * q);
+      const float4 cv = *reinterpret_cast<const float4*>(rc + 2 * q);
+      h[q] = fma2(ex2x2(mul2(dtp, A2[q])), h[q], mul2(dup, pk(bv.x, bv.y)));
+      acc = q == 0 ? mul2(pk(cv.x, cv.y), h[q]) : fma2(pk(cv.x, cv.y), h[q], acc);
+      h[q + 1] = fma2(ex2x2(mul2(dtp, A2[q + 1])), h[q + 1], mul2(dup, pk(bv.z, bv.w)));
+      acc = fma2(pk(cv.z, cv.w), h[q + 1], acc);
+    }
+    yo[j] = lo(acc) + hi(acc);
+  }
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    y2[p] = fma2(D2, L::pair(cu, p), pk(yo[2 * p], yo[2 * p + 1]));
+    if (HAS_Z) y2[p] = mul2(y2[p], silu2(L::pair(cz, p)));
   }
 }
 
@@ -196,36 +235,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(c
           const typename L::Raw8 rd = ring.get(gi, 1);
           typename L::Raw8 cz{};
           if (HAS_Z) cz = ring.get(gi, NA - 1);
-          f2 dt2[4], du2[4];
-          step_scalars<BF>(cu, rd, bias2, a.softplus, dt2, du2);
-          // ---- the recurrence over 8 steps, no bounds checks
-          float yo[kGroup];
-#pragma unroll
-          for (int j = 0; j < kGroup; ++j) {
-            const float dt = (j & 1) ? hi(dt2[j >> 1]) : lo(dt2[j >> 1]);
-            const float du = (j & 1) ? hi(du2[j >> 1]) : lo(du2[j >> 1]);
-            const f2 dtp = pk(dt, dt), dup = pk(du, du);
-            const float* rb = cB + (g + j) * NT;
-            const float* rc = cC + (g + j) * NT;
-            f2 acc;
-#pragma unroll
-            for (int q = 0; q < NP; q += 2) {
-              const float4 bv = *reinterpret_cast<const float4*>(rb + 2 * q);
-              const float4 cv = *reinterpret_cast<const float4*>(rc + 2 * q);
-              h[q] = fma2(ex2x2(mul2(dtp, A2[q])), h[q], mul2(dup, pk(bv.x, bv.y)));
-              acc = q == 0 ? mul2(pk(cv.x, cv.y), h[q]) : fma2(pk(cv.x, cv.y), h[q], acc);
-              h[q + 1] = fma2(ex2x2(mul2(dtp, A2[q + 1])), h[q + 1], mul2(dup, pk(bv.z, bv.w)));
-              acc = fma2(pk(cv.z, cv.w), h[q + 1], acc);
-            }
-            yo[j] = lo(acc) + hi(acc);
-          }
-          // ---- skip term, gate, store
           f2 y2[4];
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            y2[p] = fma2(D2, L::pair(cu, p), pk(yo[2 * p], yo[2 * p + 1]));
-            if (HAS_Z) y2[p] = mul2(y2[p], silu2(L::pair(cz, p)));
-          }
+          scan_group<NT, BF, HAS_Z>(cu, rd, cz, bias2, D2, a.softplus, A2, h, cB + g * NT, cC + g * NT, y2);
           float4* qy = reinterpret_cast<float4*>(a.y + w.row + t);
           qy[0] = make_float4(lo(y2[0]), hi(y2[0]), lo(y2[1]), hi(y2[1]));
           qy[1] = make_float4(lo(y2[2]), hi(y2[2]), lo(y2[3]), hi(y2[3]));

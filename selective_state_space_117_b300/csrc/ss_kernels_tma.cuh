@@ -1,0 +1,192 @@
+// Forward scan with TMA-staged inputs and outputs (sm_103a).
+//
+// Same work decomposition and arithmetic as scan_kernel (one thread per
+// (batch row, channel, chunk), states in registers, scan_group for every 8
+// steps), but every operand moves as a bulk tensor copy: per 16-step tile one
+// thread issues 3-D TMA loads of the block's u, delta and z rows (swizzled, so
+// each thread's row reads are bank-conflict free) and of B_t and C_t, into a
+// ring of kTmaSlots tiles completed by mbarriers, and one bulk tensor store
+// writes the block's 64 x 16 tile of y.  The threads do no per-element global
+// address arithmetic and issue no scattered loads or stores.
+#pragma once
+
+#include "ss_kernels.cuh"
+#include "ss_tma.cuh"
+
+namespace ssk {
+
+constexpr int kTmaSteps = 16;  // steps per tile
+constexpr int kTmaSlots = 3;   // input tiles in flight
+
+struct alignas(64) TmaMaps {
+  CUtensorMap u, delta, z, B, C, y;
+};
+
+constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
+
+// Shared-memory layout (byte offsets from a 1024-byte aligned base).
+template <int NT, bool BF, bool HAS_Z>
+struct TmaLayout {
+  static constexpr int ES = In<BF>::kBytes;
+  static constexpr int RB = kTmaSteps * ES;   // input row bytes: 32 (bf16) or 64 (fp32) = swizzle span
+  static constexpr int YB = kTmaSteps * 4;    // y row bytes: 64 = swizzle span
+  static constexpr int NA = HAS_Z ? 3 : 2;
+  static constexpr int kIn = kCh * RB;        // one input array's tile
+  static constexpr int kBC = NT * RB;         // one raw B or C tile (N <= NT rows)
+  static constexpr int kSlot = align1k(NA * kIn + 2 * kBC);
+  static constexpr int kY = kCh * YB;
+  static constexpr int kBCf = kTmaSteps * NT * 4;  // one fp32 B or C tile, [t][n]
+  static constexpr int oY = kTmaSlots * kSlot;
+  static constexpr int oBCf = oY + 2 * kY;
+  static constexpr int oBar = oBCf + 4 * kBCf;
+  static constexpr int kBytes = oBar + kTmaSlots * 8;
+  static constexpr int kAlloc = kBytes + 1024;   // slack to align the base
+};
+
+// Thread 0: load tile k (inputs and B/C) into its slot and arm the slot's barrier.
+template <int NT, bool BF, bool HAS_Z>
+__device__ __forceinline__ void tma_issue(const TmaMaps& m, unsigned char* sm, uint64_t* bar, int k, int64_t t_begin,
+                                          int y0, int zb, int N) {
+  using Lay = TmaLayout<NT, BF, HAS_Z>;
+  const int s = k % kTmaSlots;
+  unsigned char* slot = sm + s * Lay::kSlot;
+  mbar_expect_tx(&bar[s], Lay::NA * Lay::kIn + 2 * N * Lay::RB);
+  const int x = (int)(t_begin + (int64_t)k * kTmaSteps);
+  tma_load_3d(slot, &m.u, &bar[s], x, y0, zb);
+  tma_load_3d(slot + Lay::kIn, &m.delta, &bar[s], x, y0, zb);
+  if (HAS_Z) tma_load_3d(slot + 2 * Lay::kIn, &m.z, &bar[s], x, y0, zb);
+  tma_load_3d(slot + Lay::NA * Lay::kIn, &m.B, &bar[s], x, 0, zb);
+  tma_load_3d(slot + Lay::NA * Lay::kIn + Lay::kBC, &m.C, &bar[s], x, 0, zb);
+}
+
+// All threads: the raw [n][t] B and C tiles of a slot (N rows) into fp32 [t][n]
+// tiles of NT columns (zero for n >= N).
+template <int NT, bool BF, bool HAS_Z>
+__device__ __forceinline__ void tma_convert_bc(const unsigned char* slot, int N, float* dB, float* dC, int tid) {
+  using L = In<BF>;
+  using Lay = TmaLayout<NT, BF, HAS_Z>;
+  constexpr int SEGS = kTmaSteps / kGroup;
+  const unsigned raw = smem_addr(slot + Lay::NA * Lay::kIn);
+  for (int e = tid; e < 2 * NT * SEGS; e += kCh) {
+    const int arr = e / (NT * SEGS), rem = e % (NT * SEGS), n = rem % NT, q = rem / NT;
+    float* dst = arr ? dC : dB;
+    float v[kGroup];
+    if (n < N) {
+      const typename L::Raw8 r = L::from_smem(raw + arr * Lay::kBC + n * Lay::RB + q * kGroup * Lay::ES, 16);
+#pragma unroll
+      for (int p = 0; p < kGroup / 2; ++p) {
+        const f2 x = L::pair(r, p);
+        v[2 * p] = lo(x);
+        v[2 * p + 1] = hi(x);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j) v[j] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) dst[(q * kGroup + j) * NT + n] = v[j];
+  }
+}
+
+template <int NT, bool BF, bool HAS_Z, int MODE>
+__global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
+    scan_tma_kernel(const ScanArgs a, const __grid_constant__ TmaMaps m) {
+  using L = In<BF>;
+  using Lay = TmaLayout<NT, BF, HAS_Z>;
+  constexpr int NP = NT / 2;
+  constexpr int TS = kTmaSteps;
+  constexpr int S = kTmaSlots;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+
+  const int tid = threadIdx.x;
+  const Unit w = unit_of(a);
+  const int N = (int)a.dstate;
+  const int ct = blockIdx.x % a.ctiles;
+  const int ntiles = (int)((w.t_end - w.t_begin + TS - 1) / TS);
+  const int y0 = ct * kCh, zb = (int)w.b;
+
+  f2 A2[NP], h[NP];
+  const float* Arow = a.A + (w.active ? w.d : 0) * N;
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    const int n0 = 2 * q, n1 = 2 * q + 1;
+    A2[q] = pk((w.active && n0 < N) ? Arow[n0] * kLog2e : 0.f, (w.active && n1 < N) ? Arow[n1] * kLog2e : 0.f);
+    float h0 = 0.f, h1 = 0.f;
+    if (MODE == kFixup && w.active) {
+      const float* H = a.ws_H + (w.bd * a.nchunks + w.k) * N;
+      if (n0 < N) h0 = H[n0];
+      if (n1 < N) h1 = H[n1];
+    }
+    h[q] = pk(h0, h1);
+  }
+  const float bias = (a.delta_bias && w.active) ? a.delta_bias[w.d] : 0.f;
+  const float Dd = (a.D && w.active) ? a.D[w.d] : 0.f;
+  const f2 bias2 = pk(bias, bias), D2 = pk(Dd, Dd);
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int k = 0; k < S && k < ntiles; ++k) tma_issue<NT, BF, HAS_Z>(m, sm, bar, k, w.t_begin, y0, zb, N);
+
+  float* bcf = reinterpret_cast<float*>(sm + Lay::oBCf);  // [buffer][B, C][TS * NT]
+  constexpr int BCF = Lay::kBCf / 4;
+  bool ok = mbar_wait(&bar[0], 0, a.err);
+  tma_convert_bc<NT, BF, HAS_Z>(sm, N, bcf, bcf + BCF, tid);
+  __syncthreads();
+
+  for (int k = 0; k < ntiles; ++k) {
+    const int s = k % S;
+    const unsigned slot = smem_addr(sm + s * Lay::kSlot);
+    unsigned char* yt = sm + Lay::oY + (k & 1) * Lay::kY;
+    const float* cB = bcf + (k & 1) * 2 * BCF;
+    const float* cC = cB + BCF;
+    const int64_t t0 = w.t_begin + (int64_t)k * TS;
+    if (w.active && ok) {
+      const unsigned ybase = smem_addr(yt);
+#pragma unroll
+      for (int g = 0; g < TS / kGroup; ++g) {
+        if (t0 + g * kGroup >= w.t_end) break;
+        const typename L::Raw8 cu = tile_row8<BF, Lay::RB>(slot, tid, g);
+        const typename L::Raw8 rd = tile_row8<BF, Lay::RB>(slot + Lay::kIn, tid, g);
+        typename L::Raw8 cz{};
+        if (HAS_Z) cz = tile_row8<BF, Lay::RB>(slot + 2 * Lay::kIn, tid, g);
+        f2 y2[4];
+        scan_group<NT, BF, HAS_Z>(cu, rd, cz, bias2, D2, a.softplus, A2, h, cB + g * kGroup * NT,
+                                  cC + g * kGroup * NT, y2);
+        sts16(ybase + swz<Lay::YB>(tid, 2 * g), make_float4(lo(y2[0]), hi(y2[0]), lo(y2[1]), hi(y2[1])));
+        sts16(ybase + swz<Lay::YB>(tid, 2 * g + 1), make_float4(lo(y2[2]), hi(y2[2]), lo(y2[3]), hi(y2[3])));
+      }
+    }
+    fence_async_smem();
+    if (k + 1 < ntiles) {
+      const int s1 = (k + 1) % S;
+      if (ok) ok = mbar_wait(&bar[s1], ((k + 1) / S) & 1, a.err);
+      float* nb = bcf + ((k + 1) & 1) * 2 * BCF;
+      tma_convert_bc<NT, BF, HAS_Z>(sm + s1 * Lay::kSlot, N, nb, nb + BCF, tid);
+    }
+    if (tid == 0) bulk_wait_read<0>();  // the previous tile's y store has left the other buffer
+    __syncthreads();
+    if (tid == 0) {
+      tma_store_3d(&m.y, yt, (int)t0, y0, zb);
+      bulk_commit();
+      if (k + S < ntiles) tma_issue<NT, BF, HAS_Z>(m, sm, bar, k + S, w.t_begin, y0, zb, N);
+    }
+  }
+  if (tid == 0) bulk_wait<0>();
+
+  if (MODE == kFull && w.active && a.last_state) {
+    float* out = a.last_state + w.bd * N;
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+      if (2 * q < N) out[2 * q] = lo(h[q]);
+      if (2 * q + 1 < N) out[2 * q + 1] = hi(h[q]);
+    }
+  }
+}
+
+}  // namespace ssk

@@ -15,4 +15,10 @@ int launch_scan_fixup(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaS
 int launch_carry(const ScanArgs& a, cudaStream_t s);
 int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
 
+// TMA forward scan (mode kFull or kFixup).  tma_usable says whether the
+// shapes, alignments and driver allow it; launch_scan_tma returns 0 when it
+// launched, nonzero when a tensor map could not be built (nothing launched).
+bool tma_usable(const ScanArgs& a, bool bf16, int mode);
+int launch_scan_tma(const ScanArgs& a, bool bf16, bool has_z, int mode, dim3 grid, cudaStream_t s);
+
 }  // namespace ssk

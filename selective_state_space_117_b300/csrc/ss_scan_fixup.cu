@@ -11,7 +11,7 @@ template <int NT, bool BF, bool Z>
 static void go_fixup(const ScanArgs& a, dim3 grid, cudaStream_t s) {
   auto k = scan_kernel<NT, BF, Z, kFixup>;
   size_t dyn = 0;
-  balanced_smem((const void*)k, kCh, (int64_t)grid.x * grid.y, &dyn);
+  balanced_smem((const void*)k, kCh, (int64_t)grid.x * grid.y, 0, &dyn);
   k<<<grid, kCh, dyn, s>>>(a);
 }
 

@@ -45,7 +45,7 @@ template <int NT, bool BF>
 static void go_local(const ScanArgs& a, dim3 grid, cudaStream_t s) {
   auto k = local_kernel<NT, BF>;
   size_t dyn = 0;
-  balanced_smem((const void*)k, kCh, (int64_t)grid.x * grid.y, &dyn);
+  balanced_smem((const void*)k, kCh, (int64_t)grid.x * grid.y, 0, &dyn);
   k<<<grid, kCh, dyn, s>>>(a);
 }
 

@@ -29,6 +29,7 @@ struct ScanArgs {
   int softplus;
   int vec;           // 1: every row start is 16-byte aligned for u, delta, z and y
   int vec_bc;        // 1: every 8-step segment of a B or C row is 16-byte aligned
+  int* err;          // device status word (bounded waits record a timeout here), may be null
 };
 
 // One decode step, one thread per (b, d).

@@ -364,3 +364,11 @@ def test_chunked_local_pass_cutoff(dtype):
     for chunk in (256, 64):
         y, hl = run(p, "chunked", chunk)
         compare(p, y, hl, f"cutoff/chunked{chunk}")
+
+
+def test_device_status_clean_after_runs():
+    """No bounded wait gave up during any of the launches above (or in this test)."""
+    p = custom(101, 2, 130, 16, 4096, torch.bfloat16)
+    run(p, "fwd")
+    run(p, "chunked", 1024)
+    assert ss.device_status(clear=True) == ss.SS_OK
