@@ -164,7 +164,10 @@ int ss_scan_chunked_phase(int phase, const ss_dims* dims, const void* u, const v
   const dim3 grid((unsigned)(a.ctiles * a.nchunks), (unsigned)d.batch);
   const bool bf = d.in_dtype == SS_BF16;
   int rc = 0;
-  if (phase == SS_PHASE_LOCAL) rc = ssk::launch_scan_local(a, bf, grid, s);
+  if (phase == SS_PHASE_LOCAL) {
+    if (!(ssk::tma_usable(a, bf, ssk::kLocal) && ssk::launch_local_tma(a, bf, grid, s) == 0))
+      rc = ssk::launch_scan_local(a, bf, grid, s);
+  }
   else if (phase == SS_PHASE_CARRY) rc = ssk::launch_carry(a, s);
   else if (!(ssk::tma_usable(a, bf, ssk::kFixup) &&
              ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFixup, grid, s) == 0))
@@ -210,7 +213,7 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
   const uintptr_t bc_align = d.in_dtype == SS_BF16 ? 8 : 16;
   a.vec = (d.dstate % 4 == 0 && aligned(state, 16) && aligned(A, 16) && aligned(B, bc_align) && aligned(C, bc_align))
               ? 1 : 0;
-  if (ceil_div(d.batch * d.dim * 16, ssk::kDecodeThreads) > kMaxGridX) return SS_EINVAL;
+  if (d.dim > (int64_t)INT32_MAX / 16) return SS_EINVAL;   // (channel, lane) index of a batch row fits int
   const dim3 grid(1);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (ssk::launch_decode(a, d.in_dtype == SS_BF16, z != nullptr, grid, s) != 0) return SS_EINVAL;

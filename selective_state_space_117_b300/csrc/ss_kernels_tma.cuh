@@ -59,20 +59,21 @@ __device__ __forceinline__ void tma_issue(const TmaMaps& m, unsigned char* sm, u
   tma_load_3d(slot + Lay::NA * Lay::kIn + Lay::kBC, &m.C, &bar[s], x, 0, zb);
 }
 
-// All threads: the raw [n][t] B and C tiles of a slot (N rows) into fp32 [t][n]
-// tiles of NT columns (zero for n >= N).
-template <int NT, bool BF, bool HAS_Z>
-__device__ __forceinline__ void tma_convert_bc(const unsigned char* slot, int N, float* dB, float* dC, int tid) {
+// All threads: NARR raw [n][t] tiles (B, then C; N rows of RB bytes, NT rows
+// apart) starting at `raw` into fp32 [t][n] tiles of NT columns at dst[0..]
+// (zero for n >= N).
+template <int NT, bool BF, int NARR>
+__device__ __forceinline__ void tma_convert_rows(const unsigned char* raw, int N, float* const (&dst)[NARR], int tid) {
   using L = In<BF>;
-  using Lay = TmaLayout<NT, BF, HAS_Z>;
+  constexpr int ES = L::kBytes;
+  constexpr int RB = kTmaSteps * ES;
   constexpr int SEGS = kTmaSteps / kGroup;
-  const unsigned raw = smem_addr(slot + Lay::NA * Lay::kIn);
-  for (int e = tid; e < 2 * NT * SEGS; e += kCh) {
+  const unsigned base = smem_addr(raw);
+  for (int e = tid; e < NARR * NT * SEGS; e += kCh) {
     const int arr = e / (NT * SEGS), rem = e % (NT * SEGS), n = rem % NT, q = rem / NT;
-    float* dst = arr ? dC : dB;
     float v[kGroup];
     if (n < N) {
-      const typename L::Raw8 r = L::from_smem(raw + arr * Lay::kBC + n * Lay::RB + q * kGroup * Lay::ES, 16);
+      const typename L::Raw8 r = L::from_smem(base + (arr * NT + n) * RB + q * kGroup * ES, 16);
 #pragma unroll
       for (int p = 0; p < kGroup / 2; ++p) {
         const f2 x = L::pair(r, p);
@@ -83,9 +84,17 @@ __device__ __forceinline__ void tma_convert_bc(const unsigned char* slot, int N,
 #pragma unroll
       for (int j = 0; j < kGroup; ++j) v[j] = 0.f;
     }
+    float* d = dst[arr];
 #pragma unroll
-    for (int j = 0; j < kGroup; ++j) dst[(q * kGroup + j) * NT + n] = v[j];
+    for (int j = 0; j < kGroup; ++j) d[(q * kGroup + j) * NT + n] = v[j];
   }
+}
+
+template <int NT, bool BF, bool HAS_Z>
+__device__ __forceinline__ void tma_convert_bc(const unsigned char* slot, int N, float* dB, float* dC, int tid) {
+  using Lay = TmaLayout<NT, BF, HAS_Z>;
+  float* const dst[2] = {dB, dC};
+  tma_convert_rows<NT, BF, 2>(slot + Lay::NA * Lay::kIn, N, dst, tid);
 }
 
 template <int NT, bool BF, bool HAS_Z, int MODE>
@@ -186,6 +195,147 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
       if (2 * q < N) out[2 * q] = lo(h[q]);
       if (2 * q + 1 < N) out[2 * q + 1] = hi(h[q]);
     }
+  }
+}
+
+// Shared-memory layout of local_tma_kernel: slots of (u, delta, raw B).
+template <int NT, bool BF>
+struct LocalTmaLayout {
+  static constexpr int ES = In<BF>::kBytes;
+  static constexpr int RB = kTmaSteps * ES;
+  static constexpr int kIn = kCh * RB;
+  static constexpr int kBC = NT * RB;
+  static constexpr int kSlot = align1k(2 * kIn + kBC);
+  static constexpr int kBf = kTmaSteps * NT * 4;
+  static constexpr int oBf = kTmaSlots * kSlot;
+  static constexpr int oBar = oBf + 2 * kBf;
+  static constexpr int kBytes = oBar + kTmaSlots * 8;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+// The chunked scan's local pass (see local_kernel for the computation and its
+// early stop) with TMA-staged inputs: tiles are loaded and consumed from the
+// chunk's end backward.  A block that stops early first waits for the loads
+// it has already issued, so no bulk copy lands in shared memory after exit.
+template <int NT, bool BF>
+__global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
+    local_tma_kernel(const ScanArgs a, const __grid_constant__ TmaMaps m) {
+  using L = In<BF>;
+  using Lay = LocalTmaLayout<NT, BF>;
+  constexpr int NP = NT / 2;
+  constexpr int TS = kTmaSteps;
+  constexpr int S = kTmaSlots;
+  constexpr float kDead = -127.f;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+
+  const int tid = threadIdx.x;
+  const Unit w = unit_of(a);
+  const int N = (int)a.dstate;
+  const int ct = blockIdx.x % a.ctiles;
+  const int ntiles = (int)((w.t_end - w.t_begin + TS - 1) / TS);
+  const int y0 = ct * kCh, zb = (int)w.b;
+
+  f2 A2[NP], acc[NP];
+  float amax = -1e30f;
+  const float* Arow = a.A + (w.active ? w.d : 0) * N;
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    const int n0 = 2 * q, n1 = 2 * q + 1;
+    const float a0 = (w.active && n0 < N) ? Arow[n0] * kLog2e : 0.f;
+    const float a1 = (w.active && n1 < N) ? Arow[n1] * kLog2e : 0.f;
+    A2[q] = pk(a0, a1);
+    if (n0 < N) amax = fmaxf(amax, a0);
+    if (n1 < N) amax = fmaxf(amax, a1);
+    acc[q] = pk(0.f, 0.f);
+  }
+  const float bias = (a.delta_bias && w.active) ? a.delta_bias[w.d] : 0.f;
+  const f2 bias2 = pk(bias, bias);
+  const bool may_stop = a.softplus != 0;
+  float R = 0.f;
+
+  // Tile k of the loop is time tile ntiles - 1 - k of the chunk.
+  auto issue = [&](int k) {
+    const int s = k % S;
+    unsigned char* slot = sm + s * Lay::kSlot;
+    mbar_expect_tx(&bar[s], 2 * Lay::kIn + N * Lay::RB);
+    const int x = (int)(w.t_begin + (int64_t)(ntiles - 1 - k) * TS);
+    tma_load_3d(slot, &m.u, &bar[s], x, y0, zb);
+    tma_load_3d(slot + Lay::kIn, &m.delta, &bar[s], x, y0, zb);
+    tma_load_3d(slot + 2 * Lay::kIn, &m.B, &bar[s], x, 0, zb);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int k = 0; k < S && k < ntiles; ++k) issue(k);
+
+  float* bf = reinterpret_cast<float*>(sm + Lay::oBf);
+  constexpr int BF_ = Lay::kBf / 4;
+  bool ok = mbar_wait(&bar[0], 0, a.err);
+  {
+    float* const d0[1] = {bf};
+    tma_convert_rows<NT, BF, 1>(sm + 2 * Lay::kIn, N, d0, tid);
+  }
+  __syncthreads();
+
+  for (int k = 0; k < ntiles; ++k) {
+    const int s = k % S;
+    const unsigned slot = smem_addr(sm + s * Lay::kSlot);
+    const float* cB = bf + (k & 1) * BF_;
+    const int64_t t0 = w.t_begin + (int64_t)(ntiles - 1 - k) * TS;
+    if (w.active && ok) {
+#pragma unroll
+      for (int g = TS / kGroup - 1; g >= 0; --g) {
+        if (t0 + g * kGroup >= w.t_end) continue;
+        const typename L::Raw8 ru = tile_row8<BF, Lay::RB>(slot, tid, g);
+        const typename L::Raw8 rd = tile_row8<BF, Lay::RB>(slot + Lay::kIn, tid, g);
+        f2 dt2[4], du2[4];
+        step_scalars<BF>(ru, rd, bias2, a.softplus, dt2, du2);
+#pragma unroll
+        for (int j = kGroup - 1; j >= 0; --j) {
+          const float dt = (j & 1) ? hi(dt2[j >> 1]) : lo(dt2[j >> 1]);
+          const float du = (j & 1) ? hi(du2[j >> 1]) : lo(du2[j >> 1]);
+          const f2 Rp = pk(R, R), dup = pk(du, du);
+          const float* rb = cB + (g * kGroup + j) * NT;
+#pragma unroll
+          for (int q = 0; q < NP; q += 2) {
+            const float4 bv = *reinterpret_cast<const float4*>(rb + 2 * q);
+            acc[q] = fma2(ex2x2(mul2(Rp, A2[q])), mul2(dup, pk(bv.x, bv.y)), acc[q]);
+            acc[q + 1] = fma2(ex2x2(mul2(Rp, A2[q + 1])), mul2(dup, pk(bv.z, bv.w)), acc[q + 1]);
+          }
+          R += dt;
+        }
+      }
+    }
+    if (k + 1 < ntiles) {
+      const int s1 = (k + 1) % S;
+      if (ok) ok = mbar_wait(&bar[s1], ((k + 1) / S) & 1, a.err);
+      float* const d1[1] = {bf + ((k + 1) & 1) * BF_};
+      tma_convert_rows<NT, BF, 1>(sm + s1 * Lay::kSlot + 2 * Lay::kIn, N, d1, tid);
+    }
+    // Every weight left in this chunk underflows for every channel of the block: stop,
+    // after the loads already issued (tiles k + 2 .. k + S - 1) have landed.
+    const bool dead = !w.active || (may_stop && amax * R < kDead);
+    if (__syncthreads_and(dead)) {
+      if (tid == 0)
+        for (int j = k + 2; j < k + S && j < ntiles; ++j)
+          if (ok) ok = mbar_wait(&bar[j % S], (j / S) & 1, a.err);
+      break;
+    }
+    if (tid == 0 && k + S < ntiles) issue(k + S);
+  }
+
+  if (!w.active) return;
+  a.ws_S[w.bd * a.nchunks + w.k] = R;
+  float* H = a.ws_H + (w.bd * a.nchunks + w.k) * N;
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    if (2 * q < N) H[2 * q] = lo(acc[q]);
+    if (2 * q + 1 < N) H[2 * q + 1] = hi(acc[q]);
   }
 }
 

@@ -20,5 +20,7 @@ int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStr
 // launched, nonzero when a tensor map could not be built (nothing launched).
 bool tma_usable(const ScanArgs& a, bool bf16, int mode);
 int launch_scan_tma(const ScanArgs& a, bool bf16, bool has_z, int mode, dim3 grid, cudaStream_t s);
+// TMA local pass of the chunked scan (tma_usable with mode kLocal); same return convention.
+int launch_local_tma(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s);
 
 }  // namespace ssk

@@ -76,6 +76,25 @@ int go_tma(const ScanArgs& a, dim3 grid, cudaStream_t s) {
   return 0;
 }
 
+template <int NT, bool BF>
+int go_local_tma(const ScanArgs& a, dim3 grid, cudaStream_t s) {
+  using Lay = LocalTmaLayout<NT, BF>;
+  TmaMaps m;
+  constexpr int RB = kTmaSteps * In<BF>::kBytes;
+  const CUtensorMapSwizzle sin = swizzle_for(RB);
+  if (!encode3d(&m.u, BF, false, a.u, a.seqlen, a.dim, a.batch, kTmaSteps, kCh, sin) ||
+      !encode3d(&m.delta, BF, false, a.delta, a.seqlen, a.dim, a.batch, kTmaSteps, kCh, sin) ||
+      !encode3d(&m.B, BF, false, a.B, a.seqlen, a.dstate, a.batch, kTmaSteps, (unsigned)a.dstate,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    return 1;
+  m.z = m.C = m.y = m.u;  // unused by the local pass
+  auto k = local_tma_kernel<NT, BF>;
+  size_t dyn = Lay::kAlloc;
+  if (!balanced_smem((const void*)k, kCh, (int64_t)grid.x * grid.y, Lay::kAlloc, &dyn)) return 1;
+  k<<<grid, kCh, dyn, s>>>(a, m);
+  return 0;
+}
+
 template <int MODE>
 int dispatch_tma(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s) {
   SSK_DISPATCH_NT(a.dstate, {
@@ -87,11 +106,18 @@ int dispatch_tma(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream
 
 }  // namespace
 
+int launch_local_tma(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s) {
+  SSK_DISPATCH_NT(a.dstate, {
+    return bf16 ? go_local_tma<NT, true>(a, grid, s) : go_local_tma<NT, false>(a, grid, s);
+  });
+  return 1;
+}
+
 bool tma_usable(const ScanArgs& a, bool bf16, int mode) {
   auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) % 16) == 0; };
   if (!encode_fn()) return false;
   if (a.dstate < 1 || a.dstate > 64 || a.seqlen % kGroup != 0) return false;
-  if (mode == kFixup && a.chunk_len % kTmaSteps != 0) return false;
+  if (mode != kFull && a.chunk_len % kTmaSteps != 0) return false;
   if (!al(a.u) || !al(a.delta) || !al(a.z) || !al(a.B) || !al(a.C) || !al(a.y)) return false;
   if (a.seqlen > (int64_t)INT32_MAX || a.dim > (int64_t)INT32_MAX) return false;
   (void)bf16;

@@ -9,7 +9,7 @@ constexpr int kCh = 64;        // channels (threads) per scan block
 constexpr int kGroup = 8;      // time steps per vector load
 constexpr int kDecodeThreads = 256;
 
-enum Mode { kFull = 0, kFixup = 2 };
+enum Mode { kFull = 0, kLocal = 1, kFixup = 2 };
 
 struct ScanArgs {
   const void* u;
