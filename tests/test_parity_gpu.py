@@ -235,6 +235,44 @@ def test_ragged(case, impl, chunk):
     compare(p, y, hl, f"ragged/{impl}{chunk or ''}")
 
 
+# Shapes for the TMA paths (L a multiple of 8, chunk a multiple of 16): partial
+# last tiles (L = 16 k + 8), channel tiles cut short (dim % 64 != 0), several
+# batch rows, every padded state width, and both input dtypes.
+TMA_SHAPES = [
+    # seed, batch, dim, N, L, dtype, chunk
+    (41, 3, 100, 16, 328, torch.bfloat16, 64),
+    (42, 2, 70, 16, 200, torch.float32, 48),
+    (43, 1, 64, 64, 96, torch.bfloat16, 32),
+    (44, 2, 200, 32, 136, torch.bfloat16, 16),
+    (45, 1, 33, 8, 1032, torch.float32, 512),
+    (46, 4, 128, 4, 72, torch.bfloat16, 16),
+]
+
+
+@pytest.mark.parametrize("case", TMA_SHAPES, ids=[f"b{c[1]}d{c[2]}n{c[3]}L{c[4]}c{c[6]}" for c in TMA_SHAPES])
+@pytest.mark.parametrize("impl", ["fwd", "chunked"])
+def test_tma_shapes(case, impl):
+    seed, batch, dim, N, L, dt, chunk = case
+    p = custom(seed, batch, dim, N, L, dt)
+    y, hl = run(p, impl, chunk)
+    compare(p, y, hl, f"tma/{impl}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_local_pass_wide_decay_spread(dtype):
+    """A spread of decay rates (A from -0.05 to -40) and of step sizes across
+    channels: going back from a chunk's end, the fast states' weights underflow long
+    before the slow ones' (the early stop of the local pass then depends on the
+    slowest channel of each block).  The result must still match the oracle."""
+    p = custom(47, 2, 192, 16, 4096, dtype)
+    n = torch.arange(16, dtype=torch.float32)
+    p.A = (-0.05 * torch.exp(n * (math.log(800.0) / 15.0))).unsqueeze(0).expand(192, 16).contiguous().to(DEV)
+    p.delta_bias = torch.linspace(-1.0, 1.5, 192, device=DEV)
+    for chunk in (1024, 256):
+        y, hl = run(p, "chunked", chunk)
+        compare(p, y, hl, f"decay-spread/chunked{chunk}")
+
+
 @pytest.mark.parametrize("impl", ["fwd", "chunked"])
 def test_unaligned_rows_and_pointers(impl):
     """Tensors that start 1 element past an allocation (not 16-byte aligned) take the scalar path."""
