@@ -133,6 +133,26 @@ int ss_scan_chunked_phase(int phase, const ss_dims* dims, const void* u, const v
                           ss_stream_t stream);
 
 /*
+ * The same scans started from a given state instead of zeros: h0 is a
+ * (batch, dim, dstate) fp32 device array (NULL = zeros) read before the first
+ * step.  Running L1 steps, then L2 more steps from the first call's
+ * last_state, gives the same y and final state as one call over L1 + L2 steps
+ * (up to rounding order): a prompt's state can be computed once and reused,
+ * as the recurrence face of the layer allows ("What it costs", multigrid.ai:
+ * a shared system prompt replayed into a state).  With L = 0, last_state = h0.
+ * Other arguments, results and errors as ss_scan_fwd / ss_scan_chunked;
+ * SS_EALIGN if h0 is not 4-byte aligned.
+ */
+int ss_scan_fwd_h0(const ss_dims* dims, const float* h0, const void* u, const void* delta, const float* A,
+                   const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                   int softplus_flag, float* y, float* last_state, ss_stream_t stream);
+
+int ss_scan_chunked_h0(const ss_dims* dims, const float* h0, const void* u, const void* delta, const float* A,
+                       const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                       int softplus_flag, float* y, float* last_state, int64_t chunk_len, void* workspace,
+                       size_t workspace_bytes, ss_stream_t stream);
+
+/*
  * One decode step on a persistent state (the recurrence face: "each new token
  * only updates a fixed-size state", mernstackdev.com, FAQ; the state of
  * shape (batch, dim, N) is the fixed-size memory of "The state, in bytes",

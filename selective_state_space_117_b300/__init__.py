@@ -69,6 +69,11 @@ def lib():
         L.ss_scan_chunked.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, i64, vp,
                                       ctypes.c_size_t, vp]
         L.ss_scan_chunked.restype = ctypes.c_int
+        L.ss_scan_fwd_h0.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp]
+        L.ss_scan_fwd_h0.restype = ctypes.c_int
+        L.ss_scan_chunked_h0.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, i64, vp,
+                                         ctypes.c_size_t, vp]
+        L.ss_scan_chunked_h0.restype = ctypes.c_int
         L.ss_scan_chunked_phase.argtypes = [ctypes.c_int, dp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp,
                                             i64, vp, ctypes.c_size_t, vp]
         L.ss_scan_chunked_phase.restype = ctypes.c_int
@@ -151,16 +156,20 @@ def _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state):
 
 
 def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, y=None, last_state=None,
-             return_last_state=False, stream=None):
+             return_last_state=False, h0=None, stream=None):
     """Full-sequence selective scan.  Returns y (fp32, (batch, dim, L)), or
-    (y, last_state) when ``return_last_state`` or ``last_state`` is given."""
+    (y, last_state) when ``return_last_state`` or ``last_state`` is given.
+    ``h0`` (fp32, (batch, dim, N)) starts the scan from that state (ss_scan_fwd_h0)."""
     dims, y = _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state)
+    _need(h0, "h0", (dims.batch, dims.dim, dims.dstate), torch.float32, u.device)
     if return_last_state and last_state is None:
         last_state = torch.empty((dims.batch, dims.dim, dims.dstate), dtype=torch.float32, device=u.device)
-    st = lib().ss_scan_fwd(ctypes.byref(dims), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                           _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(last_state),
-                           _stream(u.device, stream))
-    _check(st, "ss_scan_fwd")
+    args = (_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)),
+            _ptr(y), _ptr(last_state), _stream(u.device, stream))
+    if h0 is None:
+        _check(lib().ss_scan_fwd(ctypes.byref(dims), *args), "ss_scan_fwd")
+    else:
+        _check(lib().ss_scan_fwd_h0(ctypes.byref(dims), _ptr(h0), *args), "ss_scan_fwd_h0")
     return (y, last_state) if last_state is not None else y
 
 
@@ -173,7 +182,7 @@ PHASE_LOCAL, PHASE_CARRY, PHASE_FIXUP = 1, 2, 3
 
 
 def scan_chunked(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, chunk_len=2048, y=None,
-                 last_state=None, return_last_state=False, workspace=None, stream=None, phase=None):
+                 last_state=None, return_last_state=False, workspace=None, stream=None, phase=None, h0=None):
     """Chunked selective scan (local scan, carry across chunks, fix-up).  Same
     result and return convention as ``scan_fwd``.  ``workspace`` is an optional
     uint8 CUDA tensor of at least ``chunked_workspace_bytes`` bytes.  With
@@ -187,13 +196,18 @@ def scan_chunked(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=Tr
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=u.device)
     if workspace.device != u.device or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
-    args = (ctypes.byref(dims), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+    _need(h0, "h0", (dims.batch, dims.dim, dims.dstate), torch.float32, u.device)
+    if h0 is not None and phase is not None:
+        raise ValueError("h0 is only supported for the whole chunked call (phase=None)")
+    tail = (_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
             int(bool(softplus)), _ptr(y), _ptr(last_state), int(chunk_len), _ptr(workspace), workspace.numel(),
             _stream(u.device, stream))
-    if phase is None:
-        _check(lib().ss_scan_chunked(*args), "ss_scan_chunked")
+    if h0 is not None:
+        _check(lib().ss_scan_chunked_h0(ctypes.byref(dims), _ptr(h0), *tail), "ss_scan_chunked_h0")
+    elif phase is None:
+        _check(lib().ss_scan_chunked(ctypes.byref(dims), *tail), "ss_scan_chunked")
     else:
-        _check(lib().ss_scan_chunked_phase(int(phase), *args), f"ss_scan_chunked_phase({phase})")
+        _check(lib().ss_scan_chunked_phase(int(phase), ctypes.byref(dims), *tail), f"ss_scan_chunked_phase({phase})")
     return (y, last_state) if last_state is not None else y
 
 

@@ -100,13 +100,35 @@ ssk::ScanArgs make_scan_args(const ss_dims& d, const void* u, const void* delta,
   return a;
 }
 
-// Zero the final state when there is nothing to scan (L = 0: h stays at its zero start).
-int zero_state(const ss_dims& d, float* last_state, cudaStream_t s) {
+// The final state when there is nothing to scan (L = 0): the initial state, i.e.
+// zeros or a copy of h0.
+int initial_state(const ss_dims& d, const float* h0, float* last_state, cudaStream_t s) {
   if (!last_state) return SS_OK;
   const size_t n = (size_t)(d.batch * d.dim * d.dstate);
   if (n == 0) return SS_OK;
-  const cudaError_t e = cudaMemsetAsync(last_state, 0, n * sizeof(float), s);
+  const cudaError_t e = h0 ? cudaMemcpyAsync(last_state, h0, n * sizeof(float), cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(last_state, 0, n * sizeof(float), s);
   return e == cudaSuccess ? SS_OK : cuda_fail(e);
+}
+
+int scan_fwd_impl(const ss_dims* dims, const float* h0, const void* u, const void* delta, const float* A,
+                  const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                  int softplus_flag, float* y, float* last_state, cudaStream_t s) {
+  const int st = check_scan(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
+  if (st != SS_OK) return st;
+  if (!aligned(h0, 4)) return SS_EALIGN;
+  const ss_dims& d = *dims;
+  if (d.batch == 0 || d.dim == 0) return SS_OK;
+  if (d.seqlen == 0) return initial_state(d, h0, last_state, s);
+  ssk::ScanArgs a = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
+                                   d.seqlen);
+  a.h0 = h0;
+  const dim3 grid((unsigned)a.ctiles, (unsigned)d.batch);
+  const bool bf = d.in_dtype == SS_BF16;
+  if (ssk::tma_usable(a, bf, ssk::kFull) && ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFull, grid, s) == 0)
+    return launched();
+  if (ssk::launch_scan_full(a, bf, z != nullptr, grid, s) != 0) return SS_EINVAL;
+  return launched();
 }
 
 }  // namespace
@@ -116,20 +138,15 @@ extern "C" {
 int ss_scan_fwd(const ss_dims* dims, const void* u, const void* delta, const float* A, const void* B,
                 const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
                 float* y, float* last_state, ss_stream_t stream) {
-  const int st = check_scan(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
-  if (st != SS_OK) return st;
-  const ss_dims& d = *dims;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (d.batch == 0 || d.dim == 0) return SS_OK;
-  if (d.seqlen == 0) return zero_state(d, last_state, s);
-  const ssk::ScanArgs a = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
-                                         d.seqlen);
-  const dim3 grid((unsigned)a.ctiles, (unsigned)d.batch);
-  const bool bf = d.in_dtype == SS_BF16;
-  if (ssk::tma_usable(a, bf, ssk::kFull) && ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFull, grid, s) == 0)
-    return launched();
-  if (ssk::launch_scan_full(a, bf, z != nullptr, grid, s) != 0) return SS_EINVAL;
-  return launched();
+  return scan_fwd_impl(dims, nullptr, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ss_scan_fwd_h0(const ss_dims* dims, const float* h0, const void* u, const void* delta, const float* A,
+                   const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                   int softplus_flag, float* y, float* last_state, ss_stream_t stream) {
+  return scan_fwd_impl(dims, h0, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t ss_scan_chunked_workspace_bytes(const ss_dims* dims, int64_t chunk_len) {
@@ -141,22 +158,27 @@ size_t ss_scan_chunked_workspace_bytes(const ss_dims* dims, int64_t chunk_len) {
   return align_up(s_bytes, kWsAlign) + h_bytes;
 }
 
-int ss_scan_chunked_phase(int phase, const ss_dims* dims, const void* u, const void* delta, const float* A,
-                          const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
-                          int softplus_flag, float* y, float* last_state, int64_t chunk_len, void* workspace,
-                          size_t workspace_bytes, ss_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int chunked_phase_impl(int phase, const ss_dims* dims, const float* h0, const void* u, const void* delta,
+                       const float* A, const void* B, const void* C, const float* D, const void* z,
+                       const float* delta_bias, int softplus_flag, float* y, float* last_state, int64_t chunk_len,
+                       void* workspace, size_t workspace_bytes, cudaStream_t s) {
   if (phase < SS_PHASE_LOCAL || phase > SS_PHASE_FIXUP) return SS_EINVAL;
   const int st = check_scan(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
   if (st != SS_OK) return st;
+  if (!aligned(h0, 4)) return SS_EALIGN;
   if (chunk_len < 1) return SS_EINVAL;
   const ss_dims& d = *dims;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (d.batch == 0 || d.dim == 0) return SS_OK;
-  if (d.seqlen == 0) return phase == SS_PHASE_CARRY ? zero_state(d, last_state, s) : SS_OK;
+  if (d.seqlen == 0) return phase == SS_PHASE_CARRY ? initial_state(d, h0, last_state, s) : SS_OK;
   const size_t need = ss_scan_chunked_workspace_bytes(dims, chunk_len);
   if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes < need) return SS_EWORKSPACE;
   ssk::ScanArgs a = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
                                    chunk_len);
+  a.h0 = h0;
   if ((int64_t)a.ctiles * a.nchunks > kMaxGridX) return SS_EINVAL;
   a.ws_S = static_cast<float*>(workspace);
   a.ws_H = reinterpret_cast<float*>(static_cast<char*>(workspace) +
@@ -167,25 +189,54 @@ int ss_scan_chunked_phase(int phase, const ss_dims* dims, const void* u, const v
   if (phase == SS_PHASE_LOCAL) {
     if (!(ssk::tma_usable(a, bf, ssk::kLocal) && ssk::launch_local_tma(a, bf, grid, s) == 0))
       rc = ssk::launch_scan_local(a, bf, grid, s);
-  }
-  else if (phase == SS_PHASE_CARRY) rc = ssk::launch_carry(a, s);
-  else if (!(ssk::tma_usable(a, bf, ssk::kFixup) &&
-             ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFixup, grid, s) == 0))
+  } else if (phase == SS_PHASE_CARRY) {
+    rc = ssk::launch_carry(a, s);
+  } else if (!(ssk::tma_usable(a, bf, ssk::kFixup) &&
+               ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFixup, grid, s) == 0)) {
     rc = ssk::launch_scan_fixup(a, bf, z != nullptr, grid, s);
+  }
   if (rc != 0) return SS_EINVAL;
   return launched();
+}
+
+int chunked_impl(const ss_dims* dims, const float* h0, const void* u, const void* delta, const float* A,
+                 const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                 int softplus_flag, float* y, float* last_state, int64_t chunk_len, void* workspace,
+                 size_t workspace_bytes, cudaStream_t s) {
+  for (int phase = SS_PHASE_LOCAL; phase <= SS_PHASE_FIXUP; ++phase) {
+    const int st = chunked_phase_impl(phase, dims, h0, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y,
+                                      last_state, chunk_len, workspace, workspace_bytes, s);
+    if (st != SS_OK) return st;
+  }
+  return SS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ss_scan_chunked_phase(int phase, const ss_dims* dims, const void* u, const void* delta, const float* A,
+                          const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                          int softplus_flag, float* y, float* last_state, int64_t chunk_len, void* workspace,
+                          size_t workspace_bytes, ss_stream_t stream) {
+  return chunked_phase_impl(phase, dims, nullptr, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y,
+                            last_state, chunk_len, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ss_scan_chunked(const ss_dims* dims, const void* u, const void* delta, const float* A, const void* B,
                     const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
                     float* y, float* last_state, int64_t chunk_len, void* workspace, size_t workspace_bytes,
                     ss_stream_t stream) {
-  for (int phase = SS_PHASE_LOCAL; phase <= SS_PHASE_FIXUP; ++phase) {
-    const int st = ss_scan_chunked_phase(phase, dims, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y,
-                                         last_state, chunk_len, workspace, workspace_bytes, stream);
-    if (st != SS_OK) return st;
-  }
-  return SS_OK;
+  return chunked_impl(dims, nullptr, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, chunk_len,
+                      workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ss_scan_chunked_h0(const ss_dims* dims, const float* h0, const void* u, const void* delta, const float* A,
+                       const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                       int softplus_flag, float* y, float* last_state, int64_t chunk_len, void* workspace,
+                       size_t workspace_bytes, ss_stream_t stream) {
+  return chunked_impl(dims, h0, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, chunk_len,
+                      workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ss_state_update(const ss_dims* dims, float* state, const void* u, const void* delta, const float* A,

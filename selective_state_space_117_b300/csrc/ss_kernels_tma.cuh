@@ -123,8 +123,10 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
     const int n0 = 2 * q, n1 = 2 * q + 1;
     A2[q] = pk((w.active && n0 < N) ? Arow[n0] * kLog2e : 0.f, (w.active && n1 < N) ? Arow[n1] * kLog2e : 0.f);
     float h0 = 0.f, h1 = 0.f;
-    if (MODE == kFixup && w.active) {
-      const float* H = a.ws_H + (w.bd * a.nchunks + w.k) * N;
+    const float* H = nullptr;
+    if (MODE == kFixup) H = a.ws_H + (w.bd * a.nchunks + w.k) * N;  // carry-in of this chunk
+    else if (a.h0) H = a.h0 + w.bd * N;                             // caller's initial state
+    if (H && w.active) {
       if (n0 < N) h0 = H[n0];
       if (n1 < N) h1 = H[n1];
     }

@@ -9,7 +9,7 @@ namespace ssk {
 
 // Exclusive scan over chunks of the pairs (P_k, H_k) = (exp(A * S_k), chunk end state) under
 // (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2), one thread per (b, d, n):
-//   carry_0 = 0,   carry_{k+1} = P_k * carry_k + H_k.
+//   carry_0 = h0 (zeros without one),   carry_{k+1} = P_k * carry_k + H_k.
 // Overwrites the workspace's H_k with carry_k (the true state entering chunk k) and writes the
 // final state after the last chunk.  Loads are issued 8 chunks ahead of the dependent chain.
 __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
   const int64_t K = a.nchunks;
   float* H = a.ws_H + bd * K * N + n;
   const float* S = a.ws_S + bd * K;
-  float c = 0.f;
+  float c = a.h0 ? a.h0[bd * N + n] : 0.f;  // the state entering chunk 0
   for (int64_t k0 = 0; k0 < K; k0 += 8) {
     float he[8], sk[8];
 #pragma unroll

@@ -22,6 +22,7 @@ struct ScanArgs {
   const float* delta_bias;
   float* y;
   float* last_state;
+  const float* h0;   // (batch, dim, N) initial state, or null for zeros
   float* ws_S;       // (batch, dim, nchunks): sum of dt over each chunk
   float* ws_H;       // (batch, dim, nchunks, N): chunk end state, then carry-in
   int64_t batch, dim, dstate, seqlen, chunk_len, nchunks;

@@ -410,3 +410,50 @@ def test_device_status_clean_after_runs():
     run(p, "fwd")
     run(p, "chunked", 1024)
     assert ss.device_status(clear=True) == ss.SS_OK
+
+
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("chunked", 64), ("chunked", 7)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_initial_state(impl, chunk, dtype):
+    """Scans started from a given state h0 against the oracle started from the same state."""
+    p = custom(111, 2, 90, 16, 296, dtype)
+    g = torch.Generator().manual_seed(112)
+    h0 = torch.randn((2, 90, 16), generator=g)
+    kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, softplus=p.softplus, return_last_state=True, h0=h0.to(DEV))
+    if impl == "fwd":
+        y, hl = ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, **kw)
+    else:
+        y, hl = ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, chunk_len=chunk, **kw)
+    yr, hr = oracle_scan(p.to("cpu"), h0=h0.double().numpy().reshape(180, 16))
+    bf = dtype == torch.bfloat16
+    check(host(y).reshape(180, 296), yr, bf, f"h0/{impl} y")
+    check(host(hl).reshape(180, 16), hr, bf, f"h0/{impl} last_state")
+
+
+@pytest.mark.parametrize("impl", ["fwd", "chunked"])
+def test_prompt_state_handoff(impl):
+    """A prompt's state, computed once and handed to the next call through h0, gives
+    the same outputs as one scan over prompt + continuation; the state then continues
+    in decode steps."""
+    p = custom(113, 1, 130, 16, 512, torch.bfloat16)
+    kw = dict(D=p.D, delta_bias=p.delta_bias, return_last_state=True)
+    split = 320
+
+    def part(t, a, b):
+        return t[:, :, a:b].contiguous()
+
+    def call(lo, hi, h0=None):
+        args = [part(t, lo, hi) for t in (p.u, p.delta)] + [p.A] + [part(t, lo, hi) for t in (p.B, p.C)]
+        extra = dict(z=part(p.z, lo, hi), h0=h0, **kw)
+        if impl == "fwd":
+            return ss.scan_fwd(*args, **extra)
+        return ss.scan_chunked(*args, chunk_len=64, **extra)
+
+    y_all, h_all = call(0, 512)
+    y1, h1 = call(0, split)
+    y2, h2 = call(split, 512, h0=h1)
+    check(host(torch.cat([y1, y2], dim=2)), host(y_all), True, "handoff y")
+    check(host(h2), host(h_all), True, "handoff state")
+    # L = 0 returns the initial state
+    _, h_empty = call(512, 512, h0=h2)
+    assert torch.equal(h_empty, h2)
