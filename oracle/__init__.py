@@ -48,6 +48,8 @@ def _bind(path):
     lib.sso_state_update.restype = ctypes.c_int
     lib.sso_delta.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_int]
     lib.sso_delta.restype = ctypes.c_double
+    lib.sso_conv1d.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int, dp, ctypes.c_int]
+    lib.sso_conv1d.restype = ctypes.c_int
     return lib
 
 
@@ -139,6 +141,23 @@ def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, soft
     return y
 
 
+def conv1d(x, w, bias=None, silu=True, *, dtype="f32", nthreads=0, lib=None):
+    """Causal depthwise convolution of width 4 (w[:, 3] on the current step), plus
+    bias, then SiLU when ``silu``.  x (batch, dim, L) in the wire format of
+    ``dtype``; w (dim, 4); bias (dim,).  Returns float64 (batch, dim, L)."""
+    code = _dtype_code(dtype)
+    x = _in(x, code)
+    w, bias = _f32(w), _f32(bias)
+    batch, dim, L = x.shape
+    assert w.shape == (dim, 4) and (bias is None or bias.shape == (dim,))
+    out = np.empty((batch, dim, L), dtype=np.float64)
+    rc = (lib or _load()).sso_conv1d(batch, dim, L, code, _ptr(x), _ptr(w), _ptr(bias), int(bool(silu)), _ptr(out),
+                                     _threads(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out
+
+
 def step_size(draw: float, bias: float = 0.0, softplus: bool = True, lib=None) -> float:
     """dt for one raw value: softplus(draw + bias), or draw + bias when softplus is off."""
     return (lib or _load()).sso_delta(float(draw), float(bias), int(bool(softplus)))
@@ -160,11 +179,15 @@ class Variant:
     def step_size(self, *a, **k):
         return step_size(*a, lib=self.lib, **k)
 
+    def conv1d(self, *a, **k):
+        return conv1d(*a, lib=self.lib, **k)
+
 
 class _Default:
     scan = staticmethod(scan)
     state_update = staticmethod(state_update)
     step_size = staticmethod(step_size)
+    conv1d = staticmethod(conv1d)
 
 
 default = _Default()

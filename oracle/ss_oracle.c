@@ -175,3 +175,40 @@ double sso_delta(double draw, double bias, int softplus_flag) {
     double x = draw + bias;
     return softplus_flag ? sso_softplus(x) : x;
 }
+
+/*
+ * Causal depthwise convolution of width 4 with an optional SiLU, the short
+ * convolution in front of the SSM ("What a Mamba block actually contains",
+ * multigrid.ai: a four-wide depthwise conv1d before the selective SSM;
+ * "Mamba: Linear-Time Sequence Modeling with Selective State Spaces",
+ * azimuth.plus: branch 1 is projection -> 1D convolution of kernel size 4 ->
+ * SiLU -> SSM).  Per batch row b, channel d and step t:
+ *
+ *     s      = bias[d] + sum_{k=0..3} w[d,k] * x[b,d,t-3+k]     (x = 0 before t = 0)
+ *     out    = silu(s) if silu_flag, else s
+ *
+ * so w[d,3] weighs the current step and w[d,0] the step three back.
+ *   x   : (batch, dim, seqlen), fp32 or bf16 bit patterns
+ *   w   : (dim, 4) fp32;   bias : (dim) fp32 or NULL
+ *   out : (batch, dim, seqlen) double
+ */
+int sso_conv1d(int64_t batch, int64_t dim, int64_t seqlen, int dtype, const void* x, const float* w,
+               const float* bias, int silu_flag, double* out, int nthreads) {
+    if (batch < 0 || dim < 0 || seqlen < 0) return -1;
+    if (dtype != SSO_F32 && dtype != SSO_BF16) return -1;
+    if (nthreads < 1) nthreads = 1;
+    int64_t rows = batch * dim;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+    for (int64_t c = 0; c < rows; ++c) {
+        int64_t d = c % dim;
+        for (int64_t t = 0; t < seqlen; ++t) {
+            double s = bias ? (double)bias[d] : 0.0;
+            for (int64_t k = 0; k < 4; ++k) {
+                int64_t src = t - 3 + k;
+                if (src >= 0) s += (double)w[d * 4 + k] * sso_widen(x, c * seqlen + src, dtype);
+            }
+            out[c * seqlen + t] = silu_flag ? sso_silu(s) : s;
+        }
+    }
+    return 0;
+}

@@ -321,6 +321,60 @@ def pin_degenerate_sizes(orc):
     assert rel_err(y, want.reshape(6, 6)) < 1e-14 and hl.shape == (6, 0)
 
 
+# ---------------------------------------------------------------- the short convolution
+
+def pin_conv_impulse_response(orc):
+    """A unit impulse at t0 returns the taps in causal order: out[t0 + j] = w[3 - j]
+    for j = 0..3 and zero everywhere else (no bias, no SiLU)."""
+    L, t0 = 12, 5
+    x = np.zeros((1, 3, L), dtype=np.float32)
+    x[0, :, t0] = 1.0
+    w = f32([[1.0, 10.0, 100.0, 1000.0], [-2.0, 0.5, 3.0, -7.0], [4.0, -1.0, 0.25, 2.0]])
+    out = orc.conv1d(x, w, silu=False)
+    for d in range(3):
+        want = np.zeros(L)
+        for j in range(4):
+            want[t0 + j] = w[d, 3 - j]
+        assert np.array_equal(out[0, d], want), (d, out[0, d], want)
+
+
+def pin_conv_worked_sum(orc):
+    """x = 1..5 with taps (1, 10, 100, 1000): each output reads the last four
+    inputs as decimal digits, 1000, 2100, 3210, 4321, 5432 (the sum written out)."""
+    x = f32([1, 2, 3, 4, 5]).reshape(1, 1, 5)
+    out = orc.conv1d(x, f32([[1.0, 10.0, 100.0, 1000.0]]), silu=False)
+    assert np.array_equal(out[0, 0], [1000.0, 2100.0, 3210.0, 4321.0, 5432.0]), out
+
+
+def pin_conv_identity_silu(orc):
+    """Taps (0, 0, 0, 1) with a bias pass x + b through: the output is
+    silu(x + b) = (x + b) / (1 + exp(-(x + b)))."""
+    r = np.random.default_rng(31)
+    x = f32(r.normal(size=(2, 3, 20)))
+    b = f32(r.normal(size=(3,)))
+    w = f32(np.tile([0.0, 0.0, 0.0, 1.0], (3, 1)))
+    out = orc.conv1d(x, w, bias=b, silu=True)
+    s = x.astype(np.float64) + b[None, :, None].astype(np.float64)
+    assert rel_err(out, silu64(s)) < 1e-15
+
+
+def pin_conv_linear_causal(orc):
+    """Without the SiLU the convolution is linear in x, and a change at t0 leaves every
+    output before t0 bitwise unchanged."""
+    r = np.random.default_rng(32)
+    x1 = f32(r.normal(size=(1, 4, 30)))
+    x2 = f32(r.normal(size=(1, 4, 30)))
+    w = f32(r.normal(size=(4, 4)))
+    o1, o2 = orc.conv1d(x1, w, silu=False), orc.conv1d(x2, w, silu=False)
+    o12 = orc.conv1d(f32(x1.astype(np.float64) + x2.astype(np.float64)), w, silu=False)
+    assert rel_err(o12, o1 + o2) < 1e-6          # x1 + x2 rounded to fp32
+    x3 = x1.copy()
+    x3[0, :, 17] += 1.0
+    o3 = orc.conv1d(x3, w, silu=False)
+    assert np.array_equal(o3[:, :, :17], o1[:, :, :17]) and not np.array_equal(o3[:, :, 17:21], o1[:, :, 17:21])
+
+
 PINS = [pin_tiny_example, pin_selective_toy, pin_lti_convolution, pin_unrolled_sum, pin_zero_step_keeps_state,
         pin_large_step_resets, pin_recurrence_equals_scan, pin_linear_and_causal, pin_gated_rnn_decay,
-        pin_inverse_softplus_bias, pin_bf16_widening, pin_channel_subset, pin_degenerate_sizes]
+        pin_inverse_softplus_bias, pin_bf16_widening, pin_channel_subset, pin_degenerate_sizes,
+        pin_conv_impulse_response, pin_conv_worked_sum, pin_conv_identity_silu, pin_conv_linear_causal]

@@ -43,6 +43,11 @@ MUTANTS = [
     ("u_batch_channel_transposed", [("int64_t ix = c * seqlen + t;", "int64_t ix = (d * batch + b) * seqlen + t;")]),
     ("decode_BC_ignores_batch", [("B, C, b * dstate, 1,", "B, C, 0, 1,")]),
     ("decode_u_index", [("double uu = sso_widen(u, c, dtype);", "double uu = sso_widen(u, d, dtype);")]),
+    ("conv_taps_reversed", [("(double)w[d * 4 + k] * sso_widen(x", "(double)w[d * 4 + 3 - k] * sso_widen(x")]),
+    ("conv_not_causal", [("int64_t src = t - 3 + k;", "int64_t src = t - 2 + k;")]),
+    ("conv_bias_dropped", [("double s = bias ? (double)bias[d] : 0.0;", "double s = 0.0;")]),
+    ("conv_silu_ignored", [("out[c * seqlen + t] = silu_flag ? sso_silu(s) : s;", "out[c * seqlen + t] = s;")]),
+    ("conv_wrong_channel_taps", [("(double)w[d * 4 + k]", "(double)w[(d % 2) * 4 + k]")]),
 ]
 
 
