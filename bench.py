@@ -347,6 +347,7 @@ def run_ours(args):
 
     e2e = None if args.no_e2e else bench_e2e(ss, torch, p, y, hl, ws, world, elems, min(5, args.steps))
     dec = None if args.no_decode else bench_decode(ss, I, torch, pk)
+    conv = None if args.no_decode else bench_conv(ss, torch, pk)
 
     line = {
         "metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": world, "steps": args.steps,
@@ -369,6 +370,8 @@ def run_ours(args):
     }
     if dec is not None:
         line["decode"] = dec
+    if conv is not None:
+        line["conv1d"] = conv
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
     if rank == 0:
@@ -412,6 +415,32 @@ def bench_e2e(ss, torch, p, y, hl, ws, world, elems, e2e_steps):
     del dp, hp, hy, hh
     return {"value": elems * world / (e2e_ms * 1e-3), "unit": "elem/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
+
+
+def bench_conv(ss, torch, pk, batch=1, dim=5120, seqlen=65536, reps=20):
+    """The short convolution in front of the scan (ss_causal_conv1d with SiLU) on the
+    long-sequence shape, bf16 in and out: 2 x 2 B of traffic per element."""
+    g = torch.Generator(device="cuda").manual_seed(5)
+    x = torch.randn((batch, dim, seqlen), generator=g, device="cuda").to(torch.bfloat16)
+    w = torch.randn((dim, 4), generator=g, device="cuda") * 0.5
+    b = torch.randn((dim,), generator=g, device="cuda") * 0.1
+    out = torch.empty_like(x)
+    for _ in range(3):
+        ss.causal_conv1d(x, w, b, out=out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ss.causal_conv1d(x, w, b, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    byts = batch * dim * seqlen * 4 + dim * 5 * 4
+    gbs = byts / (ms * 1e-3) / 1e9
+    del x, out
+    return {"workload": f"conv1d_silu: batch={batch}, D={dim}, L={seqlen}, width 4, bf16 in and out",
+            "entry_point": "ss_causal_conv1d", "ms": round(ms, 4), "algorithmic_bytes": byts, "gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / pk["hbm_gbs"], 4), "gpu_launches": reps}
 
 
 def bench_decode(ss, I, torch, pk, steps=1024, batch=256, dim=5120, dstate=16):
@@ -461,7 +490,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode and conv1d side measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dim", type=int, default=5120, help="channels (5120 = the workload; smaller only for profiling)")

@@ -199,6 +199,25 @@ int ss_scan_chunked_static(const ss_dims* dims, const void* u, const void* delta
                            const float* delta_bias, int softplus_flag, float* y, float* last_state,
                            int64_t chunk_len, ss_stream_t stream);
 
+/*
+ * Causal depthwise convolution of width 4, optionally followed by SiLU: the
+ * short convolution in front of the selective SSM ("What a Mamba block
+ * actually contains", multigrid.ai; the block description of "Mamba:
+ * Linear-Time Sequence Modeling with Selective State Spaces", azimuth.plus:
+ * linear projection -> 1D convolution of kernel size 4 -> SiLU -> SSM).
+ *
+ *   out[b,d,t] = silu(bias[d] + sum_{k=0..3} weight[d,k] * x[b,d,t-3+k])   (x = 0 before t = 0)
+ *
+ * weight[d,3] weighs the current step.  Its output is the scan's input u.
+ *   dims         batch, dim, seqlen and in_dtype (dstate is ignored)
+ *   x, out       (batch, dim, seqlen) of in_dtype (bf16 output is rounded to nearest even)
+ *   weight       (dim, 4) fp32, 16-byte aligned;  bias (dim) fp32 or NULL
+ *   silu_flag    nonzero: apply SiLU;  zero: the plain convolution
+ * out must not overlap x.  Errors as ss_scan_fwd.  One kernel on `stream`.
+ */
+int ss_causal_conv1d(const ss_dims* dims, const void* x, const float* weight, const float* bias, int silu_flag,
+                     void* out, ss_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* ss_status_string(int status);
 

@@ -20,7 +20,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["scan_fwd", "scan_chunked", "state_update", "chunked_workspace_bytes", "device_status", "SSError",
+__all__ = ["scan_fwd", "scan_chunked", "state_update", "causal_conv1d", "chunked_workspace_bytes", "device_status",
+           "SSError",
            "library_path",
            "F32", "BF16", "MAX_DSTATE", "LAUNCHES"]
 
@@ -83,6 +84,8 @@ def lib():
         L.ss_status_string.restype = ctypes.c_char_p
         L.ss_last_cuda_error.argtypes = []
         L.ss_last_cuda_error.restype = ctypes.c_int
+        L.ss_causal_conv1d.argtypes = [dp, vp, vp, vp, ctypes.c_int, vp, vp]
+        L.ss_causal_conv1d.restype = ctypes.c_int
         L.ss_device_status.argtypes = [ctypes.c_int]
         L.ss_device_status.restype = ctypes.c_int
         _lib = L
@@ -249,3 +252,26 @@ def device_status(clear: bool = False) -> int:
     if st not in (SS_OK, SS_ETIMEOUT):
         _check(st, "ss_device_status")
     return st
+
+
+def causal_conv1d(x, weight, bias=None, silu=True, *, out=None, stream=None):
+    """Causal depthwise convolution of width 4 (weight[:, 3] on the current step),
+    plus bias, then SiLU when ``silu`` (ss_causal_conv1d).  x (batch, dim, L) fp32
+    or bf16; weight (dim, 4) fp32; bias (dim,) fp32.  Returns out, x's dtype."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 3:
+        raise ValueError("x must be a (batch, dim, seqlen) tensor")
+    if x.device.type != "cuda":
+        raise ValueError("the convolution runs on a CUDA device only; x is on " + str(x.device))
+    batch, dim, L = x.shape
+    code = _dtype_code(x)
+    _need(x, "x", (batch, dim, L), x.dtype, x.device)
+    _need(weight, "weight", (dim, 4), torch.float32, x.device)
+    _need(bias, "bias", (dim,), torch.float32, x.device)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", (batch, dim, L), x.dtype, x.device)
+    dims = Dims(batch, dim, 0, L, code)
+    st = lib().ss_causal_conv1d(ctypes.byref(dims), _ptr(x), _ptr(weight), _ptr(bias), int(bool(silu)), _ptr(out),
+                                _stream(x.device, stream))
+    _check(st, "ss_causal_conv1d")
+    return out

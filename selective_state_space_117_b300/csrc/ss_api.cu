@@ -271,6 +271,26 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
   return launched();
 }
 
+int ss_causal_conv1d(const ss_dims* dims, const void* x, const float* weight, const float* bias, int silu_flag,
+                     void* out, ss_stream_t stream) {
+  if (!dims) return SS_EINVAL;
+  const ss_dims& d = *dims;
+  if (d.in_dtype != SS_F32 && d.in_dtype != SS_BF16) return SS_EDTYPE;
+  if (d.batch < 0 || d.dim < 0 || d.seqlen < 0) return SS_EINVAL;
+  if (d.batch == 0 || d.dim == 0 || d.seqlen == 0) return SS_OK;
+  if (!x || !weight || !out) return SS_EINVAL;
+  const size_t es = in_size(d.in_dtype);
+  if (!aligned(x, es) || !aligned(out, es) || !aligned(weight, 16) || !aligned(bias, 4)) return SS_EALIGN;
+  ssk::ConvArgs a{};
+  a.x = x; a.w = weight; a.bias = bias; a.out = out;
+  a.rows = d.batch * d.dim; a.dim = d.dim; a.seqlen = d.seqlen;
+  a.nseg = ssk::conv1d_segments(d.seqlen);
+  a.vec = ((d.seqlen * (int64_t)es) % 16 == 0 && aligned(x, 16) && aligned(out, 16)) ? 1 : 0;
+  if (ssk::launch_conv1d(a, d.in_dtype == SS_BF16, silu_flag != 0, reinterpret_cast<cudaStream_t>(stream)) != 0)
+    return SS_EINVAL;
+  return launched();
+}
+
 const char* ss_status_string(int status) {
   switch (status) {
     case SS_OK: return "SS_OK";

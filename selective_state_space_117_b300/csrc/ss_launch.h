@@ -15,6 +15,10 @@ int launch_scan_fixup(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaS
 int launch_carry(const ScanArgs& a, cudaStream_t s);
 int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
 
+// Causal depthwise conv1d (width 4) with optional SiLU; segments of a row per warp.
+int launch_conv1d(const ConvArgs& a, bool bf16, bool silu_on, cudaStream_t s);
+int64_t conv1d_segments(int64_t seqlen);
+
 // TMA forward scan (mode kFull or kFixup).  tma_usable says whether the
 // shapes, alignments and driver allow it; launch_scan_tma returns 0 when it
 // launched, nonzero when a tensor map could not be built (nothing launched).

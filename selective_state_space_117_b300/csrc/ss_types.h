@@ -33,6 +33,16 @@ struct ScanArgs {
   int* err;          // device status word (bounded waits record a timeout here), may be null
 };
 
+// Causal depthwise conv1d of width 4 over (rows = batch * dim, seqlen).
+struct ConvArgs {
+  const void* x;
+  const float* w;      // (dim, 4), 16-byte aligned
+  const float* bias;   // (dim) or null
+  void* out;
+  int64_t rows, dim, seqlen, nseg;
+  int vec;             // 1: rows are 16-byte aligned for 8-element vectors
+};
+
 // One decode step, one thread per (b, d).
 struct DecodeArgs {
   float* state;
