@@ -41,10 +41,10 @@ def _bind(path):
     lib = ctypes.CDLL(path)
     i64, vp, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
     lib.sso_scan.argtypes = [i64, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp,
-                             ctypes.c_int, vp, i64, dp, dp, dp, ctypes.c_int]
+                             ctypes.c_int, vp, i64, dp, dp, dp, ctypes.c_int, ctypes.c_int]
     lib.sso_scan.restype = ctypes.c_int
     lib.sso_state_update.argtypes = [i64, i64, i64, ctypes.c_int, dp, vp, vp, vp, vp, vp, vp, vp,
-                                     vp, ctypes.c_int, vp, i64, dp, ctypes.c_int]
+                                     vp, ctypes.c_int, vp, i64, dp, ctypes.c_int, ctypes.c_int]
     lib.sso_state_update.restype = ctypes.c_int
     lib.sso_delta.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_int]
     lib.sso_delta.restype = ctypes.c_double
@@ -92,10 +92,11 @@ def _threads(nthreads):
 
 
 def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *,
-         dtype="f32", h0=None, chans=None, nthreads=0, lib=None):
+         dtype="f32", h0=None, chans=None, nthreads=0, zoh=False, lib=None):
     """Full-sequence scan.  Shapes: u/delta/z (batch, dim, L); B/C (batch, N, L);
     A (dim, N); D/delta_bias (dim,).  Returns (y, h_last) as float64 arrays of
-    shape (nchan, L) and (nchan, N), where nchan = batch*dim or len(chans)."""
+    shape (nchan, L) and (nchan, N), where nchan = batch*dim or len(chans).
+    ``zoh`` uses the zero-order-hold input weight (exp(dt A) - 1)/A instead of dt."""
     code = _dtype_code(dtype)
     u, delta, B, C, z = (_in(x, code) for x in (u, delta, B, C, z))
     A, D, delta_bias = _f32(A), _f32(D), _f32(delta_bias)
@@ -111,14 +112,14 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *,
     hl = np.empty((nch, N), dtype=np.float64)
     rc = (lib or _load()).sso_scan(batch, dim, N, L, code, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
                           _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(ch), nch,
-                          _ptr(hh0), _ptr(y), _ptr(hl), _threads(nthreads))
+                          _ptr(hh0), _ptr(y), _ptr(hl), _threads(nthreads), int(bool(zoh)))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return y, hl
 
 
 def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *,
-                 dtype="f32", chans=None, nthreads=0, lib=None):
+                 dtype="f32", chans=None, nthreads=0, zoh=False, lib=None):
     """One decode step.  Shapes: u/delta/z (batch, dim); B/C (batch, N);
     state (nchan, N) float64, updated in place.  Returns y (nchan,) float64."""
     code = _dtype_code(dtype)
@@ -135,7 +136,8 @@ def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, soft
     y = np.empty((nch,), dtype=np.float64)
     rc = (lib or _load()).sso_state_update(batch, dim, N, code, _ptr(state), _ptr(u), _ptr(delta), _ptr(A),
                                   _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-                                  int(bool(softplus)), _ptr(ch), nch, _ptr(y), _threads(nthreads))
+                                  int(bool(softplus)), _ptr(ch), nch, _ptr(y), _threads(nthreads),
+                                  int(bool(zoh)))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return y

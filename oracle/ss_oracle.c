@@ -18,6 +18,7 @@
  *     dt     = softplus(x)            if softplus_flag, else x
  *     Abar_n = exp(dt * A[d,n])
  *     h_n    = Abar_n * h_n + dt * B[b,n,t] * u[b,d,t]   for n < N
+ *              (zero-order hold: (exp(dt A) - 1)/A in place of dt)
  *     y      = sum_n C[b,n,t] * h_n + D[d] * u[b,d,t]     (D optional)
  *     y      = y * silu(z[b,d,t])                          (z optional)
  *
@@ -72,13 +73,23 @@ static double sso_silu(double z) {
     return z / (1.0 + exp(-z));
 }
 
+/* Input weight of the zero-order-hold discretisation: (exp(dt A) - 1) / A, which
+ * tends to dt as A -> 0.  With it the update is the exact solution of
+ * dh/dt = A h + B x over a step of length dt with x held constant (the
+ * "principled discretization" behind Theorem 1 of "Mamba: Linear-Time Sequence
+ * Modeling with Selective State Spaces", azimuth.plus). */
+static double sso_zoh_weight(double dt, double A) {
+    return A != 0.0 ? expm1(dt * A) / A : dt;
+}
+
 /* One time step of one channel.  h has dstate entries and is updated in place.
- * Returns y.  Index arithmetic is done by the callers. */
+ * Returns y.  Index arithmetic is done by the callers.  zoh selects the input
+ * weight: dt (Euler, the equations as printed) or sso_zoh_weight. */
 static double sso_step(double* h, int64_t dstate,
                        double u, double draw, double bias, int softplus_flag,
                        const float* A_row, double Dd,
                        const void* B, const void* C, int64_t bc_base, int64_t bc_stride,
-                       int has_z, double z, int dtype) {
+                       int has_z, double z, int dtype, int zoh) {
     double x = draw + bias;
     double dt = softplus_flag ? sso_softplus(x) : x;
     double y = 0.0;
@@ -86,7 +97,8 @@ static double sso_step(double* h, int64_t dstate,
         double Bn = sso_widen(B, bc_base + n * bc_stride, dtype);
         double Cn = sso_widen(C, bc_base + n * bc_stride, dtype);
         double Abar = exp(dt * (double)A_row[n]);
-        h[n] = Abar * h[n] + dt * Bn * u;
+        double wdt = zoh ? sso_zoh_weight(dt, (double)A_row[n]) : dt;
+        h[n] = Abar * h[n] + wdt * Bn * u;
         y += Cn * h[n];
     }
     y += Dd * u;
@@ -106,7 +118,7 @@ int sso_scan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int dty
              const void* u, const void* delta, const float* A, const void* B, const void* C,
              const float* D, const void* z, const float* delta_bias, int softplus_flag,
              const int64_t* chans, int64_t nchans, const double* h0,
-             double* y, double* h_last, int nthreads) {
+             double* y, double* h_last, int nthreads, int zoh) {
     if (batch < 0 || dim < 0 || dstate < 0 || seqlen < 0) return -1;
     if (dtype != SSO_F32 && dtype != SSO_BF16) return -1;
     int64_t total = batch * dim;
@@ -129,7 +141,7 @@ int sso_scan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int dty
             double zz = z ? sso_widen(z, ix, dtype) : 0.0;
             y[i * seqlen + t] = sso_step(h, dstate, uu, dr, bias, softplus_flag, A + d * dstate, Dd,
                                          B, C, b * dstate * seqlen + t, seqlen,
-                                         z != NULL, zz, dtype);
+                                         z != NULL, zz, dtype, zoh);
         }
         if (h_last)
             for (int64_t n = 0; n < dstate; ++n) h_last[i * dstate + n] = h[n];
@@ -148,7 +160,7 @@ int sso_state_update(int64_t batch, int64_t dim, int64_t dstate, int dtype,
                      double* state, const void* u, const void* delta, const float* A,
                      const void* B, const void* C, const float* D, const void* z,
                      const float* delta_bias, int softplus_flag,
-                     const int64_t* chans, int64_t nchans, double* y, int nthreads) {
+                     const int64_t* chans, int64_t nchans, double* y, int nthreads, int zoh) {
     if (batch < 0 || dim < 0 || dstate < 0) return -1;
     if (dtype != SSO_F32 && dtype != SSO_BF16) return -1;
     int64_t total = batch * dim;
@@ -165,7 +177,7 @@ int sso_state_update(int64_t batch, int64_t dim, int64_t dstate, int dtype,
         double zz = z ? sso_widen(z, c, dtype) : 0.0;
         y[i] = sso_step(state + i * dstate, dstate, uu, dr, delta_bias ? (double)delta_bias[d] : 0.0,
                         softplus_flag, A + d * dstate, D ? (double)D[d] : 0.0,
-                        B, C, b * dstate, 1, z != NULL, zz, dtype);
+                        B, C, b * dstate, 1, z != NULL, zz, dtype, zoh);
     }
     return bad ? -1 : 0;
 }

@@ -321,6 +321,71 @@ def pin_degenerate_sizes(orc):
     assert rel_err(y, want.reshape(6, 6)) < 1e-14 and hl.shape == (6, 0)
 
 
+# ---------------------------------------------------------------- zero-order hold
+
+def pin_zoh_theorem1(orc):
+    """Theorem 1 ("Mamba: Linear-Time Sequence Modeling with Selective State
+    Spaces", azimuth.plus): with N = 1, A = -1, B = C = 1 and dt = softplus(g_t),
+    the zero-order-hold scan is the gated RNN h_t = (1 - s_t) h_{t-1} + s_t x_t
+    with s_t = sigmoid(g_t), exactly (1 - exp(-softplus(g)) = sigmoid(g))."""
+    r = np.random.default_rng(41)
+    L = 50
+    x = f32(r.normal(size=(1, 2, L)))
+    g = f32(r.normal(scale=2.0, size=(1, 2, L)))
+    one = f32(np.ones((1, 1, L)))
+    y, hl = orc.scan(x, g, f32(-np.ones((2, 1))), one, one, softplus=True, zoh=True)
+    for d in range(2):
+        s = 1.0 / (1.0 + np.exp(-g[0, d].astype(np.float64)))
+        h, want = 0.0, []
+        for t in range(L):
+            h = (1.0 - s[t]) * h + s[t] * float(x[0, d, t])
+            want.append(h)
+        assert rel_err(y[d], want) < 1e-12, (d, rel_err(y[d], want))
+        assert abs(hl[d, 0] - want[-1]) < 1e-12
+
+
+def pin_zoh_limits(orc):
+    """A = 0 exactly: the hold weight is its limit dt, so ZOH and the printed
+    (Euler) update agree bitwise; |A dt| ~ 1e-9: they agree to 1e-8 relative.
+    Large |A dt|: the weight tends to -1/A, the steady state of the held input."""
+    p = rand_problem(42, batch=1, dim=3, N=4, L=16, gate=False, with_D=False)
+    A0 = f32(np.zeros((3, 4)))
+    ye, he = orc.scan(p["u"], p["delta"], A0, p["B"], p["C"], delta_bias=p["delta_bias"])
+    yz, hz = orc.scan(p["u"], p["delta"], A0, p["B"], p["C"], delta_bias=p["delta_bias"], zoh=True)
+    assert np.array_equal(ye, yz) and np.array_equal(he, hz)
+    At = f32(np.full((3, 4), -1e-9))
+    ye, _ = orc.scan(p["u"], p["delta"], At, p["B"], p["C"], delta_bias=p["delta_bias"])
+    yz, _ = orc.scan(p["u"], p["delta"], At, p["B"], p["C"], delta_bias=p["delta_bias"], zoh=True)
+    assert rel_err(yz, ye) < 1e-8
+    # one step with dt = 40, A = -2 from h = 0: h = (exp(-80) - 1)/(-2) * B u ~ B u / 2
+    y, h = orc.scan(f32([[[3.0]]]), f32([[[40.0]]]), f32([[-2.0]]), f32([[[5.0]]]), f32([[[1.0]]]),
+                    softplus=False, zoh=True)
+    assert abs(h[0, 0] - 7.5) < 1e-12 and abs(y[0, 0] - 7.5) < 1e-12
+
+
+def pin_zoh_lti_convolution(orc):
+    """Time-invariant zero-order hold: y_t = sum_k C Abar^k Bbar u_{t-k} with
+    Abar = exp(dt A) and Bbar = (exp(dt A) - 1)/A B, as an O(L^2) convolution."""
+    r = np.random.default_rng(43)
+    dim, N, L = 2, 3, 30
+    u = f32(r.normal(size=(1, dim, L)))
+    draw = f32(r.normal(size=(1, dim, 1)))
+    A = f32(-np.exp(r.uniform(-1.0, 1.0, size=(dim, N))))
+    B0 = f32(r.normal(size=(1, N, 1)))
+    C0 = f32(r.normal(size=(1, N, 1)))
+    y, _ = orc.scan(u, np.repeat(draw, L, axis=2), A, np.repeat(B0, L, axis=2), np.repeat(C0, L, axis=2),
+                    softplus=True, zoh=True)
+    k = np.arange(L)
+    for d in range(dim):
+        dt = softplus64(float(draw[0, d, 0]))
+        K = np.zeros(L)
+        for n in range(N):
+            a = float(A[d, n])
+            K += float(C0[0, n, 0]) * np.exp(k * dt * a) * (np.expm1(dt * a) / a) * float(B0[0, n, 0])
+        want = np.convolve(u[0, d].astype(np.float64), K)[:L]
+        assert rel_err(y[d], want) < 1e-11
+
+
 # ---------------------------------------------------------------- the short convolution
 
 def pin_conv_impulse_response(orc):
@@ -377,4 +442,5 @@ def pin_conv_linear_causal(orc):
 PINS = [pin_tiny_example, pin_selective_toy, pin_lti_convolution, pin_unrolled_sum, pin_zero_step_keeps_state,
         pin_large_step_resets, pin_recurrence_equals_scan, pin_linear_and_causal, pin_gated_rnn_decay,
         pin_inverse_softplus_bias, pin_bf16_widening, pin_channel_subset, pin_degenerate_sizes,
-        pin_conv_impulse_response, pin_conv_worked_sum, pin_conv_identity_silu, pin_conv_linear_causal]
+        pin_conv_impulse_response, pin_conv_worked_sum, pin_conv_identity_silu, pin_conv_linear_causal,
+        pin_zoh_theorem1, pin_zoh_limits, pin_zoh_lti_convolution]

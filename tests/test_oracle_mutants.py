@@ -24,14 +24,14 @@ MUTANTS = [
     ("softplus_wrong_negative_branch", [("log1p(exp(-fabs(x)))", "log1p(exp(-x))")]),
     ("exp_sign_flipped", [("exp(dt * (double)A_row[n])", "exp(-dt * (double)A_row[n])")]),
     ("exp_missing_dt", [("exp(dt * (double)A_row[n])", "exp((double)A_row[n])")]),
-    ("input_term_missing_dt", [("h[n] = Abar * h[n] + dt * Bn * u;", "h[n] = Abar * h[n] + Bn * u;")]),
+    ("input_term_missing_dt", [("h[n] = Abar * h[n] + wdt * Bn * u;", "h[n] = Abar * h[n] + Bn * u;")]),
     ("B_C_swapped", [("double Bn = sso_widen(B, ", "double Bn = sso_widen(C, "),
                      ("double Cn = sso_widen(C, ", "double Cn = sso_widen(B, ")]),
     ("D_term_dropped", [("y += Dd * u;", "")]),
     ("gate_before_D", [("y += Dd * u;\n    if (has_z) y *= sso_silu(z);", "if (has_z) y *= sso_silu(z);\n    y += Dd * u;")]),
     ("sigmoid_not_silu", [("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));")]),
     ("silu_sign", [("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));")]),
-    ("readout_before_update", [("h[n] = Abar * h[n] + dt * Bn * u;\n        y += Cn * h[n];",
+    ("readout_before_update", [("h[n] = Abar * h[n] + wdt * Bn * u;\n        y += Cn * h[n];",
                                 "y += Cn * h[n];\n        h[n] = Abar * h[n] + dt * Bn * u;")]),
     ("BC_time_off_by_one", [("B, C, b * dstate * seqlen + t, seqlen,", "B, C, b * dstate * seqlen + (t > 0 ? t - 1 : 0), seqlen,")]),
     ("A_row_wrong_channel", [("A + d * dstate, Dd,", "A + (d % 2) * dstate, Dd,")]),
@@ -43,6 +43,10 @@ MUTANTS = [
     ("u_batch_channel_transposed", [("int64_t ix = c * seqlen + t;", "int64_t ix = (d * batch + b) * seqlen + t;")]),
     ("decode_BC_ignores_batch", [("B, C, b * dstate, 1,", "B, C, 0, 1,")]),
     ("decode_u_index", [("double uu = sso_widen(u, c, dtype);", "double uu = sso_widen(u, d, dtype);")]),
+    ("zoh_times_A", [("return A != 0.0 ? expm1(dt * A) / A : dt;", "return A != 0.0 ? expm1(dt * A) * A : dt;")]),
+    ("zoh_exp_not_expm1", [("return A != 0.0 ? expm1(dt * A) / A : dt;", "return A != 0.0 ? exp(dt * A) / A : dt;")]),
+    ("zoh_limit_zero", [("return A != 0.0 ? expm1(dt * A) / A : dt;", "return A != 0.0 ? expm1(dt * A) / A : 0.0;")]),
+    ("zoh_flag_ignored", [("double wdt = zoh ? sso_zoh_weight(dt, (double)A_row[n]) : dt;", "double wdt = dt;")]),
     ("conv_taps_reversed", [("(double)w[d * 4 + k] * sso_widen(x", "(double)w[d * 4 + 3 - k] * sso_widen(x")]),
     ("conv_not_causal", [("int64_t src = t - 3 + k;", "int64_t src = t - 2 + k;")]),
     ("conv_bias_dropped", [("double s = bias ? (double)bias[d] : 0.0;", "double s = 0.0;")]),
