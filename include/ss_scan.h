@@ -65,12 +65,24 @@ typedef enum {
 /* Largest supported state size N. */
 #define SS_MAX_DSTATE 64
 
+/*
+ * Discretisation flag (ss_dims.flags).  Without it the input enters as the
+ * equations print it, dt * B * u ("Selective state", multigrid.ai).  With
+ * SS_FLAG_ZOH it enters with the zero-order-hold weight (exp(dt A) - 1) / A
+ * (dt in the limit A -> 0): the exact solution over a step with the input held
+ * constant, under which Theorem 1 of "Mamba: Linear-Time Sequence Modeling with
+ * Selective State Spaces" (azimuth.plus) holds exactly (N = 1, A = -1 gives the
+ * gated RNN h = (1 - sigmoid(g)) h + sigmoid(g) x).  Abar = exp(dt A) either way.
+ */
+#define SS_FLAG_ZOH 1
+
 typedef struct {
     int64_t batch;     /* >= 0; at most 65535 */
     int64_t dim;       /* channels D, >= 0 */
     int64_t dstate;    /* state size N, 0 .. SS_MAX_DSTATE */
     int64_t seqlen;    /* sequence length L, >= 0 (ignored by ss_state_update) */
     int32_t in_dtype;  /* ss_dtype of u, delta, B, C, z */
+    int32_t flags;     /* 0 or SS_FLAG_ZOH; other bits are rejected with SS_EINVAL */
 } ss_dims;
 
 /*

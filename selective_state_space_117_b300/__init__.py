@@ -45,9 +45,12 @@ class SSError(RuntimeError):
         self.status = status
 
 
+FLAG_ZOH = 1
+
+
 class Dims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("dim", ctypes.c_int64), ("dstate", ctypes.c_int64),
-                ("seqlen", ctypes.c_int64), ("in_dtype", ctypes.c_int32)]
+                ("seqlen", ctypes.c_int64), ("in_dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -159,11 +162,13 @@ def _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state):
 
 
 def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, y=None, last_state=None,
-             return_last_state=False, h0=None, stream=None):
+             return_last_state=False, h0=None, zoh=False, stream=None):
     """Full-sequence selective scan.  Returns y (fp32, (batch, dim, L)), or
     (y, last_state) when ``return_last_state`` or ``last_state`` is given.
-    ``h0`` (fp32, (batch, dim, N)) starts the scan from that state (ss_scan_fwd_h0)."""
+    ``h0`` (fp32, (batch, dim, N)) starts the scan from that state (ss_scan_fwd_h0).
+    ``zoh`` uses the zero-order-hold input weight (SS_FLAG_ZOH)."""
     dims, y = _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state)
+    dims.flags = FLAG_ZOH if zoh else 0
     _need(h0, "h0", (dims.batch, dims.dim, dims.dstate), torch.float32, u.device)
     if return_last_state and last_state is None:
         last_state = torch.empty((dims.batch, dims.dim, dims.dstate), dtype=torch.float32, device=u.device)
@@ -185,13 +190,15 @@ PHASE_LOCAL, PHASE_CARRY, PHASE_FIXUP = 1, 2, 3
 
 
 def scan_chunked(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, chunk_len=2048, y=None,
-                 last_state=None, return_last_state=False, workspace=None, stream=None, phase=None, h0=None):
+                 last_state=None, return_last_state=False, workspace=None, stream=None, phase=None, h0=None,
+                 zoh=False):
     """Chunked selective scan (local scan, carry across chunks, fix-up).  Same
     result and return convention as ``scan_fwd``.  ``workspace`` is an optional
     uint8 CUDA tensor of at least ``chunked_workspace_bytes`` bytes.  With
     ``phase`` in (1, 2, 3) only that phase runs (ss_scan_chunked_phase); the
     three phases in order on one stream, sharing a workspace, are the full call."""
     dims, y = _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state)
+    dims.flags = FLAG_ZOH if zoh else 0
     if return_last_state and last_state is None:
         last_state = torch.empty((dims.batch, dims.dim, dims.dstate), dtype=torch.float32, device=u.device)
     need = int(lib().ss_scan_chunked_workspace_bytes(ctypes.byref(dims), int(chunk_len)))
@@ -215,7 +222,7 @@ def scan_chunked(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=Tr
 
 
 def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, y=None,
-                 stream=None):
+                 zoh=False, stream=None):
     """One decode step.  state (batch, dim, N) fp32 is updated in place;
     u, delta, z are (batch, dim); B, C are (batch, N).  Returns y (batch, dim) fp32."""
     if not isinstance(u, torch.Tensor) or u.dim() != 2:
@@ -237,7 +244,7 @@ def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, soft
     if y is None:
         y = torch.empty((batch, dim), dtype=torch.float32, device=dev)
     _need(y, "y", (batch, dim), torch.float32, dev)
-    dims = Dims(batch, dim, N, 1, code)
+    dims = Dims(batch, dim, N, 1, code, FLAG_ZOH if zoh else 0)
     st = lib().ss_state_update(ctypes.byref(dims), _ptr(state), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
                                _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(y),
                                _stream(u.device, stream))

@@ -64,6 +64,7 @@ int check_scan(const ss_dims* dims, const void* u, const void* delta, const floa
   const ss_dims& d = *dims;
   if (d.in_dtype != SS_F32 && d.in_dtype != SS_BF16) return SS_EDTYPE;
   if (d.batch < 0 || d.dim < 0 || d.dstate < 0 || d.seqlen < 0) return SS_EINVAL;
+  if ((d.flags & ~SS_FLAG_ZOH) != 0) return SS_EINVAL;
   if (d.dstate > SS_MAX_DSTATE || d.batch > kMaxGridY) return SS_EINVAL;
   if (ceil_div(d.dim, ssk::kCh) > kMaxGridX) return SS_EINVAL;
   const size_t es = in_size(d.in_dtype);
@@ -97,6 +98,7 @@ ssk::ScanArgs make_scan_args(const ss_dims& d, const void* u, const void* delta,
   const bool bc16 = (d.seqlen * (int64_t)es) % 16 == 0 && aligned(B, 16) && aligned(C, 16);
   a.vec_bc = (bc16 && chunk_len % ssk::kGroup == 0) ? 1 : 0;
   a.err = device_status_word();
+  a.zoh = (d.flags & SS_FLAG_ZOH) ? 1 : 0;
   return a;
 }
 
@@ -125,7 +127,7 @@ int scan_fwd_impl(const ss_dims* dims, const float* h0, const void* u, const voi
   a.h0 = h0;
   const dim3 grid((unsigned)a.ctiles, (unsigned)d.batch);
   const bool bf = d.in_dtype == SS_BF16;
-  if (ssk::tma_usable(a, bf, ssk::kFull) && ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFull, grid, s) == 0)
+  if (ssk::tma_available(a, bf, ssk::kFull) && ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFull, grid, s) == 0)
     return launched();
   if (ssk::launch_scan_full(a, bf, z != nullptr, grid, s) != 0) return SS_EINVAL;
   return launched();
@@ -187,11 +189,11 @@ int chunked_phase_impl(int phase, const ss_dims* dims, const float* h0, const vo
   const bool bf = d.in_dtype == SS_BF16;
   int rc = 0;
   if (phase == SS_PHASE_LOCAL) {
-    if (!(ssk::tma_usable(a, bf, ssk::kLocal) && ssk::launch_local_tma(a, bf, grid, s) == 0))
+    if (!(ssk::tma_available(a, bf, ssk::kLocal) && ssk::launch_local_tma(a, bf, grid, s) == 0))
       rc = ssk::launch_scan_local(a, bf, grid, s);
   } else if (phase == SS_PHASE_CARRY) {
     rc = ssk::launch_carry(a, s);
-  } else if (!(ssk::tma_usable(a, bf, ssk::kFixup) &&
+  } else if (!(ssk::tma_available(a, bf, ssk::kFixup) &&
                ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFixup, grid, s) == 0)) {
     rc = ssk::launch_scan_fixup(a, bf, z != nullptr, grid, s);
   }
@@ -247,6 +249,7 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
   if (d.in_dtype != SS_F32 && d.in_dtype != SS_BF16) return SS_EDTYPE;
   if (d.batch < 0 || d.dim < 0 || d.dstate < 0 || d.dstate > SS_MAX_DSTATE || d.batch > kMaxGridY)
     return SS_EINVAL;
+  if ((d.flags & ~SS_FLAG_ZOH) != 0) return SS_EINVAL;
   if (ceil_div(d.dim, ssk::kCh) > kMaxGridX) return SS_EINVAL;
   if (d.batch == 0 || d.dim == 0) return SS_OK;
   if (!u || !delta || !y) return SS_EINVAL;
@@ -261,6 +264,7 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
   a.delta_bias = delta_bias; a.y = y;
   a.batch = d.batch; a.dim = d.dim; a.dstate = d.dstate;
   a.softplus = softplus_flag ? 1 : 0;
+  a.zoh = (d.flags & SS_FLAG_ZOH) ? 1 : 0;
   const uintptr_t bc_align = d.in_dtype == SS_BF16 ? 8 : 16;
   a.vec = (d.dstate % 4 == 0 && aligned(state, 16) && aligned(A, 16) && aligned(B, bc_align) && aligned(C, bc_align))
               ? 1 : 0;

@@ -39,7 +39,7 @@ __device__ __forceinline__ void st_keep4(float* p, float4 v, uint64_t pol) {
 // Every load is issued before any arithmetic; with several lanes per channel
 // each lane computes dt itself (no cross-lane wait) and the readout sum crosses
 // the lanes with xor shuffles.
-template <int NT, bool BF, bool HAS_Z>
+template <int NT, bool BF, bool HAS_Z, bool ZOH>
 __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeArgs a) {
   using L = In<BF>;
   constexpr int SPL = NT < kDecodeSpl ? NT : kDecodeSpl;
@@ -104,13 +104,21 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeArgs
   // ---- the step: dt, then every state pair, then the readout
   const float dt = a.softplus ? softplus(x) : x;
   const float du = dt * uu;
-  const f2 dtp = pk(dt, dt), dup = pk(du, du), l2e = pk(kLog2e, kLog2e);
+  const f2 dtp = pk(dt, dt), dup = pk(du, du), upp = pk(uu, uu), l2e = pk(kLog2e, kLog2e);
   f2 acc = pk(0.f, 0.f);
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     const f2 hq = pk(hv[2 * q], hv[2 * q + 1]);
-    const f2 e = ex2x2(mul2(dtp, mul2(l2e, pk(Av[2 * q], Av[2 * q + 1]))));
-    const f2 hn = fma2(e, hq, mul2(dup, pk(Bv[2 * q], Bv[2 * q + 1])));
+    const f2 Aq = pk(Av[2 * q], Av[2 * q + 1]);
+    const f2 arg = mul2(dtp, mul2(l2e, Aq));
+    const f2 e = ex2x2(arg);
+    f2 hn;
+    if constexpr (ZOH) {
+      const f2 iA = pk(Av[2 * q] != 0.f ? 1.f / Av[2 * q] : 0.f, Av[2 * q + 1] != 0.f ? 1.f / Av[2 * q + 1] : 0.f);
+      hn = fma2(e, hq, mul2(hold2(arg, e, dtp, iA), mul2(upp, pk(Bv[2 * q], Bv[2 * q + 1]))));
+    } else {
+      hn = fma2(e, hq, mul2(dup, pk(Bv[2 * q], Bv[2 * q + 1])));
+    }
     hv[2 * q] = lo(hn);
     hv[2 * q + 1] = hi(hn);
     acc = fma2(pk(Cv[2 * q], Cv[2 * q + 1]), hn, acc);
@@ -140,18 +148,24 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeArgs
   }
 }
 
+template <int NT, bool BF, bool Z>
+static void go_decode(const DecodeArgs& a, cudaStream_t s) {
+  constexpr int G = NT < kDecodeSpl ? 1 : NT / kDecodeSpl;
+  const int64_t threads = a.dim * G;
+  const dim3 g2((unsigned)((threads + kDecodeThreads - 1) / kDecodeThreads), (unsigned)a.batch);
+  if (a.zoh) decode_kernel<NT, BF, Z, true><<<g2, kDecodeThreads, 0, s>>>(a);
+  else decode_kernel<NT, BF, Z, false><<<g2, kDecodeThreads, 0, s>>>(a);
+}
+
 int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s) {
   (void)grid;
   SSK_DISPATCH_NT(a.dstate, {
-    constexpr int G = NT < kDecodeSpl ? 1 : NT / kDecodeSpl;
-    const int64_t threads = a.dim * G;
-    const dim3 g2((unsigned)((threads + kDecodeThreads - 1) / kDecodeThreads), (unsigned)a.batch);
     if (bf16) {
-      if (has_z) decode_kernel<NT, true, true><<<g2, kDecodeThreads, 0, s>>>(a);
-      else decode_kernel<NT, true, false><<<g2, kDecodeThreads, 0, s>>>(a);
+      if (has_z) go_decode<NT, true, true>(a, s);
+      else go_decode<NT, true, false>(a, s);
     } else {
-      if (has_z) decode_kernel<NT, false, true><<<g2, kDecodeThreads, 0, s>>>(a);
-      else decode_kernel<NT, false, false><<<g2, kDecodeThreads, 0, s>>>(a);
+      if (has_z) go_decode<NT, false, true>(a, s);
+      else go_decode<NT, false, false>(a, s);
     }
   });
   return 0;

@@ -117,11 +117,21 @@ __device__ __forceinline__ void step_scalars(const typename In<BF>::Raw8& ru, co
 // inputs as raw 8-element rows (u, delta, z), B and C of the 8 steps as fp32
 // rows of NT values at cB and cC, the state h updated in place, and the 8
 // outputs (skip term and gate applied) returned as pairs in y2.
-template <int NT, bool BF, bool HAS_Z>
+// One state pair's update h = Abar h + (input weight) B u for one step:
+// Euler weight dt (du = dt u), or the zero-order-hold weight (hold2).
+template <bool ZOH>
+__device__ __forceinline__ f2 step_pair(f2 h, f2 A2, f2 iA2, f2 dtp, f2 dup, f2 upp, f2 Bp) {
+  const f2 arg = mul2(dtp, A2);
+  const f2 e = ex2x2(arg);
+  if constexpr (ZOH) return fma2(e, h, mul2(hold2(arg, e, dtp, iA2), mul2(upp, Bp)));
+  return fma2(e, h, mul2(dup, Bp));
+}
+
+template <int NT, bool BF, bool HAS_Z, bool ZOH>
 __device__ __forceinline__ void scan_group(const typename In<BF>::Raw8& cu, const typename In<BF>::Raw8& rd,
                                            const typename In<BF>::Raw8& cz, f2 bias2, f2 D2, int softplus,
-                                           const f2 (&A2)[NT / 2], f2 (&h)[NT / 2], const float* cB,
-                                           const float* cC, f2 (&y2)[4]) {
+                                           const f2 (&A2)[NT / 2], const f2 (&iA2)[NT / 2], f2 (&h)[NT / 2],
+                                           const float* cB, const float* cC, f2 (&y2)[4]) {
   using L = In<BF>;
   constexpr int NP = NT / 2;
   f2 dt2[4], du2[4];
@@ -131,6 +141,12 @@ __device__ __forceinline__ void scan_group(const typename In<BF>::Raw8& cu, cons
   for (int j = 0; j < kGroup; ++j) {
     const float dt = (j & 1) ? hi(dt2[j >> 1]) : lo(dt2[j >> 1]);
     const float du = (j & 1) ? hi(du2[j >> 1]) : lo(du2[j >> 1]);
+    f2 upp = pk(0.f, 0.f);
+    if (ZOH) {
+      const f2 u2 = L::pair(cu, j >> 1);
+      const float uu = (j & 1) ? hi(u2) : lo(u2);
+      upp = pk(uu, uu);
+    }
     const f2 dtp = pk(dt, dt), dup = pk(du, du);
     const float* rb = cB + j * NT;
     const float* rc = cC + j * NT;
@@ -139,9 +155,9 @@ __device__ __forceinline__ void scan_group(const typename In<BF>::Raw8& cu, cons
     for (int q = 0; q < NP; q += 2) {
       const float4 bv = *reinterpret_cast<const float4*>(rb + 2 * q);
       const float4 cv = *reinterpret_cast<const float4*>(rc + 2 * q);
-      h[q] = fma2(ex2x2(mul2(dtp, A2[q])), h[q], mul2(dup, pk(bv.x, bv.y)));
+      h[q] = step_pair<ZOH>(h[q], A2[q], iA2[q], dtp, dup, upp, pk(bv.x, bv.y));
       acc = q == 0 ? mul2(pk(cv.x, cv.y), h[q]) : fma2(pk(cv.x, cv.y), h[q], acc);
-      h[q + 1] = fma2(ex2x2(mul2(dtp, A2[q + 1])), h[q + 1], mul2(dup, pk(bv.z, bv.w)));
+      h[q + 1] = step_pair<ZOH>(h[q + 1], A2[q + 1], iA2[q + 1], dtp, dup, upp, pk(bv.z, bv.w));
       acc = fma2(pk(cv.z, cv.w), h[q + 1], acc);
     }
     yo[j] = lo(acc) + hi(acc);
@@ -153,7 +169,7 @@ __device__ __forceinline__ void scan_group(const typename In<BF>::Raw8& cu, cons
   }
 }
 
-template <int NT, bool BF, bool HAS_Z, int MODE>
+template <int NT, bool BF, bool HAS_Z, int MODE, bool ZOH>
 __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(const ScanArgs a) {
   using L = In<BF>;
   using T = Tile<NT>;
@@ -169,12 +185,14 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(c
   const int N = (int)a.dstate;
 
   // Padding states n >= N keep B = C = 0 (their staged values are zero), A = 0 and h = 0.
-  f2 A2[NP], h[NP];
+  f2 A2[NP], iA2[NP], h[NP];
   const float* Arow = a.A + (w.active ? w.d : 0) * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     const int n0 = 2 * q, n1 = 2 * q + 1;
-    A2[q] = pk((w.active && n0 < N) ? Arow[n0] * kLog2e : 0.f, (w.active && n1 < N) ? Arow[n1] * kLog2e : 0.f);
+    const float a0 = (w.active && n0 < N) ? Arow[n0] : 0.f, a1 = (w.active && n1 < N) ? Arow[n1] : 0.f;
+    A2[q] = pk(a0 * kLog2e, a1 * kLog2e);
+    iA2[q] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
     float h0 = 0.f, h1 = 0.f;
     const float* H = nullptr;
     if (MODE == kFixup) H = a.ws_H + (w.bd * a.nchunks + w.k) * N;  // carry-in of this chunk
@@ -238,7 +256,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(c
           typename L::Raw8 cz{};
           if (HAS_Z) cz = ring.get(gi, NA - 1);
           f2 y2[4];
-          scan_group<NT, BF, HAS_Z>(cu, rd, cz, bias2, D2, a.softplus, A2, h, cB + g * NT, cC + g * NT, y2);
+          scan_group<NT, BF, HAS_Z, ZOH>(cu, rd, cz, bias2, D2, a.softplus, A2, iA2, h, cB + g * NT, cC + g * NT,
+                                         y2);
           float4* qy = reinterpret_cast<float4*>(a.y + w.row + t);
           qy[0] = make_float4(lo(y2[0]), hi(y2[0]), lo(y2[1]), hi(y2[1]));
           qy[1] = make_float4(lo(y2[2]), hi(y2[2]), lo(y2[3]), hi(y2[3]));
@@ -250,7 +269,7 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(c
             const float uu = L::one(a.u, ix);
             const float x = L::one(a.delta, ix) + bias;
             const float dt = a.softplus ? softplus(x) : x;
-            const f2 dtp = pk(dt, dt), dup = pk(dt * uu, dt * uu);
+            const f2 dtp = pk(dt, dt), dup = pk(dt * uu, dt * uu), upp = pk(uu, uu);
             const float* rb = cB + (g + j) * NT;
             const float* rc = cC + (g + j) * NT;
             f2 acc = pk(0.f, 0.f);
@@ -258,7 +277,7 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(c
             for (int q = 0; q < NP; ++q) {
               const f2 bq = *reinterpret_cast<const f2*>(rb + 2 * q);
               const f2 cq = *reinterpret_cast<const f2*>(rc + 2 * q);
-              h[q] = fma2(ex2x2(mul2(dtp, A2[q])), h[q], mul2(dup, bq));
+              h[q] = step_pair<ZOH>(h[q], A2[q], iA2[q], dtp, dup, upp, bq);
               acc = fma2(cq, h[q], acc);
             }
             float yv = fmaf(Dd, uu, lo(acc) + hi(acc));
@@ -287,6 +306,23 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(c
   }
 }
 
+// One state pair's term of the backward local pass at one step, with R the sum
+// of dt after the step: Euler adds exp(A R) dt B u; the zero-order hold adds
+// (exp(A (R + dt)) - exp(A R)) / A * B u, the first exponential being the one the
+// next (earlier) step needs, so wc carries it and the hold costs no extra exp.
+template <bool ZOH>
+__device__ __forceinline__ void local_pair(f2& acc, f2& wc, f2 A2, f2 iA2, float R, float dt, float du, float uu,
+                                           f2 Bp) {
+  if constexpr (ZOH) {
+    const f2 dtp = pk(dt, dt), Rn = pk(R + dt, R + dt);
+    const f2 wn = ex2x2(mul2(Rn, A2));
+    acc = fma2(hold_between2(wn, wc, mul2(dtp, A2), dtp, iA2), mul2(pk(uu, uu), Bp), acc);
+    wc = wn;
+  } else {
+    acc = fma2(ex2x2(mul2(pk(R, R), A2)), mul2(pk(du, du), Bp), acc);
+  }
+}
+
 // First phase of the chunked scan: for every chunk, its zero-start end state
 //   Hend[n] = sum_s exp(A[n] * R_s) * dt_s * B_s[n] * u_s,   R_s = sum_{r > s in chunk} dt_r
 // and the chunk's sum of dt, computed backward from the chunk's end.  With
@@ -296,7 +332,7 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(c
 // of every channel.  The sum written is then partial, but every
 // exp(A[n] * sum) that the carry pass forms from it underflows to zero
 // exactly as the full sum's would.
-template <int NT, bool BF>
+template <int NT, bool BF, bool ZOH>
 __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) local_kernel(const ScanArgs a) {
   using L = In<BF>;
   using T = Tile<NT>;
@@ -310,15 +346,17 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) local_kernel(
   const Unit w = unit_of(a);
   const int N = (int)a.dstate;
 
-  f2 A2[NP], acc[NP];
+  f2 A2[NP], iA2[NP], wc[NP], acc[NP];
   float amax = -1e30f;  // the slowest decay of this channel (padding states never count)
   const float* Arow = a.A + (w.active ? w.d : 0) * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     const int n0 = 2 * q, n1 = 2 * q + 1;
-    const float a0 = (w.active && n0 < N) ? Arow[n0] * kLog2e : 0.f;
-    const float a1 = (w.active && n1 < N) ? Arow[n1] * kLog2e : 0.f;
+    const float an0 = (w.active && n0 < N) ? Arow[n0] : 0.f, an1 = (w.active && n1 < N) ? Arow[n1] : 0.f;
+    const float a0 = an0 * kLog2e, a1 = an1 * kLog2e;
     A2[q] = pk(a0, a1);
+    iA2[q] = pk(an0 != 0.f ? 1.f / an0 : 0.f, an1 != 0.f ? 1.f / an1 : 0.f);
+    wc[q] = pk(1.f, 1.f);  // exp(A R) at R = 0 (zero-order hold only)
     if (n0 < N) amax = fmaxf(amax, a0);
     if (n1 < N) amax = fmaxf(amax, a1);
     acc[q] = pk(0.f, 0.f);
@@ -378,13 +416,13 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) local_kernel(
           for (int j = kGroup - 1; j >= 0; --j) {
             const float dt = (j & 1) ? hi(dt2[j >> 1]) : lo(dt2[j >> 1]);
             const float du = (j & 1) ? hi(du2[j >> 1]) : lo(du2[j >> 1]);
-            const f2 Rp = pk(R, R), dup = pk(du, du);
+            const float uu = (j & 1) ? hi(L::pair(ru, j >> 1)) : lo(L::pair(ru, j >> 1));
             const float* rb = cB + (g + j) * NT;
 #pragma unroll
             for (int q = 0; q < NP; q += 2) {
               const float4 bv = *reinterpret_cast<const float4*>(rb + 2 * q);
-              acc[q] = fma2(ex2x2(mul2(Rp, A2[q])), mul2(dup, pk(bv.x, bv.y)), acc[q]);
-              acc[q + 1] = fma2(ex2x2(mul2(Rp, A2[q + 1])), mul2(dup, pk(bv.z, bv.w)), acc[q + 1]);
+              local_pair<ZOH>(acc[q], wc[q], A2[q], iA2[q], R, dt, du, uu, pk(bv.x, bv.y));
+              local_pair<ZOH>(acc[q + 1], wc[q + 1], A2[q + 1], iA2[q + 1], R, dt, du, uu, pk(bv.z, bv.w));
             }
             R += dt;
           }
@@ -395,12 +433,12 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) local_kernel(
             const float x = L::one(a.delta, ix) + bias;
             const float dt = a.softplus ? softplus(x) : x;
             const float du = dt * L::one(a.u, ix);
-            const f2 Rp = pk(R, R), dup = pk(du, du);
+            const float uu = L::one(a.u, ix);
             const float* rb = cB + (g + j) * NT;
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
               const f2 bq = *reinterpret_cast<const f2*>(rb + 2 * q);
-              acc[q] = fma2(ex2x2(mul2(Rp, A2[q])), mul2(dup, bq), acc[q]);
+              local_pair<ZOH>(acc[q], wc[q], A2[q], iA2[q], R, dt, du, uu, bq);
             }
             R += dt;
           }

@@ -97,7 +97,7 @@ __device__ __forceinline__ void tma_convert_bc(const unsigned char* slot, int N,
   tma_convert_rows<NT, BF, 2>(slot + Lay::NA * Lay::kIn, N, dst, tid);
 }
 
-template <int NT, bool BF, bool HAS_Z, int MODE>
+template <int NT, bool BF, bool HAS_Z, int MODE, bool ZOH>
 __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
     scan_tma_kernel(const ScanArgs a, const __grid_constant__ TmaMaps m) {
   using L = In<BF>;
@@ -116,12 +116,14 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
   const int ntiles = (int)((w.t_end - w.t_begin + TS - 1) / TS);
   const int y0 = ct * kCh, zb = (int)w.b;
 
-  f2 A2[NP], h[NP];
+  f2 A2[NP], iA2[NP], h[NP];
   const float* Arow = a.A + (w.active ? w.d : 0) * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     const int n0 = 2 * q, n1 = 2 * q + 1;
-    A2[q] = pk((w.active && n0 < N) ? Arow[n0] * kLog2e : 0.f, (w.active && n1 < N) ? Arow[n1] * kLog2e : 0.f);
+    const float a0 = (w.active && n0 < N) ? Arow[n0] : 0.f, a1 = (w.active && n1 < N) ? Arow[n1] : 0.f;
+    A2[q] = pk(a0 * kLog2e, a1 * kLog2e);
+    iA2[q] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
     float h0 = 0.f, h1 = 0.f;
     const float* H = nullptr;
     if (MODE == kFixup) H = a.ws_H + (w.bd * a.nchunks + w.k) * N;  // carry-in of this chunk
@@ -167,8 +169,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
         typename L::Raw8 cz{};
         if (HAS_Z) cz = tile_row8<BF, Lay::RB>(slot + 2 * Lay::kIn, tid, g);
         f2 y2[4];
-        scan_group<NT, BF, HAS_Z>(cu, rd, cz, bias2, D2, a.softplus, A2, h, cB + g * kGroup * NT,
-                                  cC + g * kGroup * NT, y2);
+        scan_group<NT, BF, HAS_Z, ZOH>(cu, rd, cz, bias2, D2, a.softplus, A2, iA2, h, cB + g * kGroup * NT,
+                                       cC + g * kGroup * NT, y2);
         sts16(ybase + swz<Lay::YB>(tid, 2 * g), make_float4(lo(y2[0]), hi(y2[0]), lo(y2[1]), hi(y2[1])));
         sts16(ybase + swz<Lay::YB>(tid, 2 * g + 1), make_float4(lo(y2[2]), hi(y2[2]), lo(y2[3]), hi(y2[3])));
       }
@@ -219,7 +221,7 @@ struct LocalTmaLayout {
 // early stop) with TMA-staged inputs: tiles are loaded and consumed from the
 // chunk's end backward.  A block that stops early first waits for the loads
 // it has already issued, so no bulk copy lands in shared memory after exit.
-template <int NT, bool BF>
+template <int NT, bool BF, bool ZOH>
 __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
     local_tma_kernel(const ScanArgs a, const __grid_constant__ TmaMaps m) {
   using L = In<BF>;
@@ -239,15 +241,17 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
   const int ntiles = (int)((w.t_end - w.t_begin + TS - 1) / TS);
   const int y0 = ct * kCh, zb = (int)w.b;
 
-  f2 A2[NP], acc[NP];
+  f2 A2[NP], iA2[NP], wc[NP], acc[NP];
   float amax = -1e30f;
   const float* Arow = a.A + (w.active ? w.d : 0) * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     const int n0 = 2 * q, n1 = 2 * q + 1;
-    const float a0 = (w.active && n0 < N) ? Arow[n0] * kLog2e : 0.f;
-    const float a1 = (w.active && n1 < N) ? Arow[n1] * kLog2e : 0.f;
+    const float an0 = (w.active && n0 < N) ? Arow[n0] : 0.f, an1 = (w.active && n1 < N) ? Arow[n1] : 0.f;
+    const float a0 = an0 * kLog2e, a1 = an1 * kLog2e;
     A2[q] = pk(a0, a1);
+    iA2[q] = pk(an0 != 0.f ? 1.f / an0 : 0.f, an1 != 0.f ? 1.f / an1 : 0.f);
+    wc[q] = pk(1.f, 1.f);  // exp(A R) at R = 0 (zero-order hold only)
     if (n0 < N) amax = fmaxf(amax, a0);
     if (n1 < N) amax = fmaxf(amax, a1);
     acc[q] = pk(0.f, 0.f);
@@ -301,13 +305,13 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
         for (int j = kGroup - 1; j >= 0; --j) {
           const float dt = (j & 1) ? hi(dt2[j >> 1]) : lo(dt2[j >> 1]);
           const float du = (j & 1) ? hi(du2[j >> 1]) : lo(du2[j >> 1]);
-          const f2 Rp = pk(R, R), dup = pk(du, du);
+          const float uu = (j & 1) ? hi(L::pair(ru, j >> 1)) : lo(L::pair(ru, j >> 1));
           const float* rb = cB + (g * kGroup + j) * NT;
 #pragma unroll
           for (int q = 0; q < NP; q += 2) {
             const float4 bv = *reinterpret_cast<const float4*>(rb + 2 * q);
-            acc[q] = fma2(ex2x2(mul2(Rp, A2[q])), mul2(dup, pk(bv.x, bv.y)), acc[q]);
-            acc[q + 1] = fma2(ex2x2(mul2(Rp, A2[q + 1])), mul2(dup, pk(bv.z, bv.w)), acc[q + 1]);
+            local_pair<ZOH>(acc[q], wc[q], A2[q], iA2[q], R, dt, du, uu, pk(bv.x, bv.y));
+            local_pair<ZOH>(acc[q + 1], wc[q + 1], A2[q + 1], iA2[q + 1], R, dt, du, uu, pk(bv.z, bv.w));
           }
           R += dt;
         }

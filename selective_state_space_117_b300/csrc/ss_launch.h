@@ -9,9 +9,21 @@
 namespace ssk {
 
 // Each returns 0 when a kernel was launched, -1 when dstate is unsupported.
-int launch_scan_full(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
-int launch_scan_local(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s);
-int launch_scan_fixup(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
+// The _t templates take the discretisation (ZOH: zero-order hold) and are
+// instantiated in separate files; the plain names pick one from a.zoh.
+template <bool ZOH> int launch_scan_full_t(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
+template <bool ZOH> int launch_scan_fixup_t(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
+template <bool ZOH> int launch_scan_local_t(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s);
+inline int launch_scan_full(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s) {
+  return a.zoh ? launch_scan_full_t<true>(a, bf16, has_z, grid, s) : launch_scan_full_t<false>(a, bf16, has_z, grid, s);
+}
+inline int launch_scan_fixup(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s) {
+  return a.zoh ? launch_scan_fixup_t<true>(a, bf16, has_z, grid, s)
+               : launch_scan_fixup_t<false>(a, bf16, has_z, grid, s);
+}
+inline int launch_scan_local(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s) {
+  return a.zoh ? launch_scan_local_t<true>(a, bf16, grid, s) : launch_scan_local_t<false>(a, bf16, grid, s);
+}
 int launch_carry(const ScanArgs& a, cudaStream_t s);
 int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
 
@@ -19,12 +31,19 @@ int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStr
 int launch_conv1d(const ConvArgs& a, bool bf16, bool silu_on, cudaStream_t s);
 int64_t conv1d_segments(int64_t seqlen);
 
-// TMA forward scan (mode kFull or kFixup).  tma_usable says whether the
-// shapes, alignments and driver allow it; launch_scan_tma returns 0 when it
+// TMA kernels.  tma_available says whether the shapes, alignments and driver
+// allow them (mode kFull, kLocal or kFixup); the launchers return 0 when they
 // launched, nonzero when a tensor map could not be built (nothing launched).
-bool tma_usable(const ScanArgs& a, bool bf16, int mode);
-int launch_scan_tma(const ScanArgs& a, bool bf16, bool has_z, int mode, dim3 grid, cudaStream_t s);
-// TMA local pass of the chunked scan (tma_usable with mode kLocal); same return convention.
-int launch_local_tma(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s);
+bool tma_available(const ScanArgs& a, bool bf16, int mode);
+template <bool ZOH>
+int launch_scan_tma_t(const ScanArgs& a, bool bf16, bool has_z, int mode, dim3 grid, cudaStream_t s);
+template <bool ZOH> int launch_local_tma_t(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s);
+inline int launch_scan_tma(const ScanArgs& a, bool bf16, bool has_z, int mode, dim3 grid, cudaStream_t s) {
+  return a.zoh ? launch_scan_tma_t<true>(a, bf16, has_z, mode, grid, s)
+               : launch_scan_tma_t<false>(a, bf16, has_z, mode, grid, s);
+}
+inline int launch_local_tma(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s) {
+  return a.zoh ? launch_local_tma_t<true>(a, bf16, grid, s) : launch_local_tma_t<false>(a, bf16, grid, s);
+}
 
 }  // namespace ssk

@@ -1,31 +1,6 @@
-// Launcher of the chunked scan's fix-up phase (mode kFixup): every chunk runs
-// again from its carried-in state and writes y.
-#include "ss_dispatch.cuh"
-#include "ss_kernels.cuh"
-#include "ss_launch.h"
-#include "ss_occupancy.cuh"
+// Ring-staged fix-up pass of the chunked scan (mode kFixup), Euler input weight.
+#include "ss_ring_launch.cuh"
 
 namespace ssk {
-
-template <int NT, bool BF, bool Z>
-static void go_fixup(const ScanArgs& a, dim3 grid, cudaStream_t s) {
-  auto k = scan_kernel<NT, BF, Z, kFixup>;
-  size_t dyn = 0;
-  balanced_smem((const void*)k, kCh, (int64_t)grid.x * grid.y, 0, &dyn);
-  k<<<grid, kCh, dyn, s>>>(a);
-}
-
-int launch_scan_fixup(const ScanArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s) {
-  SSK_DISPATCH_NT(a.dstate, {
-    if (bf16) {
-      if (has_z) go_fixup<NT, true, true>(a, grid, s);
-      else go_fixup<NT, true, false>(a, grid, s);
-    } else {
-      if (has_z) go_fixup<NT, false, true>(a, grid, s);
-      else go_fixup<NT, false, false>(a, grid, s);
-    }
-  });
-  return 0;
-}
-
+template int launch_scan_fixup_t<false>(const ScanArgs&, bool, bool, dim3, cudaStream_t);
 }  // namespace ssk

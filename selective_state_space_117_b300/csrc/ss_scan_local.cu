@@ -1,9 +1,6 @@
-// Launchers of the chunked scan's first two phases: the zero-start end state
-// of every chunk (local_kernel) and the carry pass across chunks.
-#include "ss_dispatch.cuh"
-#include "ss_kernels.cuh"
-#include "ss_launch.h"
-#include "ss_occupancy.cuh"
+// The carry pass across chunks, and the ring-staged local pass (local_kernel)
+// with the Euler input weight.
+#include "ss_ring_launch.cuh"
 
 namespace ssk {
 
@@ -41,22 +38,6 @@ __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
   if (a.last_state) a.last_state[bd * N + n] = c;
 }
 
-template <int NT, bool BF>
-static void go_local(const ScanArgs& a, dim3 grid, cudaStream_t s) {
-  auto k = local_kernel<NT, BF>;
-  size_t dyn = 0;
-  balanced_smem((const void*)k, kCh, (int64_t)grid.x * grid.y, 0, &dyn);
-  k<<<grid, kCh, dyn, s>>>(a);
-}
-
-int launch_scan_local(const ScanArgs& a, bool bf16, dim3 grid, cudaStream_t s) {
-  SSK_DISPATCH_NT(a.dstate, {
-    if (bf16) go_local<NT, true>(a, grid, s);
-    else go_local<NT, false>(a, grid, s);
-  });
-  return 0;
-}
-
 int launch_carry(const ScanArgs& a, cudaStream_t s) {
   const int64_t total = a.batch * a.dim * a.dstate;
   if (total == 0) return 0;
@@ -64,5 +45,7 @@ int launch_carry(const ScanArgs& a, cudaStream_t s) {
   carry_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
   return 0;
 }
+
+template int launch_scan_local_t<false>(const ScanArgs&, bool, dim3, cudaStream_t);
 
 }  // namespace ssk

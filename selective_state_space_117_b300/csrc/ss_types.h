@@ -31,6 +31,7 @@ struct ScanArgs {
   int vec;           // 1: every row start is 16-byte aligned for u, delta, z and y
   int vec_bc;        // 1: every 8-step segment of a B or C row is 16-byte aligned
   int* err;          // device status word (bounded waits record a timeout here), may be null
+  int zoh;           // 1: zero-order-hold input weight (exp(dt A) - 1) / A instead of dt
 };
 
 // Causal depthwise conv1d of width 4 over (rows = batch * dim, seqlen).
@@ -58,6 +59,7 @@ struct DecodeArgs {
   int64_t batch, dim, dstate;
   int softplus;
   int vec;           // 1: N % 4 == 0 and state, A, B, C rows allow 16/8-byte vector access
+  int zoh;           // 1: zero-order-hold input weight
 };
 
 }  // namespace ssk

@@ -63,6 +63,9 @@ def _chunked(dims, chunk=8, ws=P, ws_bytes=1 << 30, **over):
 
 def test_validation_status_codes():
     assert _fwd(_dims(dt=7)) == ss.SS_EDTYPE
+    bad = _dims()
+    bad.flags = 2                                           # unknown discretisation bit
+    assert _fwd(bad) == ss.SS_EINVAL
     assert _fwd(_dims(L=-1)) == ss.SS_EINVAL
     assert _fwd(_dims(n=65)) == ss.SS_EINVAL
     assert _fwd(_dims(b=70000)) == ss.SS_EINVAL
