@@ -58,18 +58,20 @@ TRAFFIC = {
 }
 
 
+# The files that define the chunked step's three kernels and how they are launched.
+STEP_SOURCES = ("ss_device.cuh", "ss_kernels.cuh", "ss_kernels_tma.cuh", "ss_tma.cuh", "ss_tma_launch.cuh",
+                "ss_scan_tma.cu", "ss_scan_local.cu", "ss_occupancy.cuh", "ss_types.h", "ss_dispatch.cuh")
+
+
 def kernel_sources_hash():
-    """sha256 (first 16 hex digits) over the CUDA sources and the C ABI header."""
+    """sha256 (first 16 hex digits) over the sources of the chunked step's kernels."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(HERE, "selective_state_space_117_b300", "csrc")
-    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
-    for f in files:
+    for f in STEP_SOURCES:
         h.update(f.encode())
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
-    with open(os.path.join(HERE, "include", "ss_scan.h"), "rb") as fh:
-        h.update(fh.read())
     return h.hexdigest()[:16]
 
 
