@@ -350,6 +350,10 @@ def run_ours(args):
     e2e = None if args.no_e2e else bench_e2e(ss, torch, p, y, hl, ws, world, elems, min(5, args.steps))
     dec = None if args.no_decode else bench_decode(ss, I, torch, pk)
     conv = None if args.no_decode else bench_conv(ss, torch, pk)
+    side = {}
+    if not args.no_decode:
+        side["zoh"] = bench_zoh_step(ss, torch, p, kw, elems)
+        side["fwd_layer"] = bench_fwd_layer(ss, I, torch, pk)
 
     line = {
         "metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": world, "steps": args.steps,
@@ -374,6 +378,7 @@ def run_ours(args):
         line["decode"] = dec
     if conv is not None:
         line["conv1d"] = conv
+    line.update(side)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p)
     if rank == 0:
@@ -417,6 +422,47 @@ def bench_e2e(ss, torch, p, y, hl, ws, world, elems, e2e_steps):
     del dp, hp, hy, hh
     return {"value": elems * world / (e2e_ms * 1e-3), "unit": "elem/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
+
+
+def bench_fwd_layer(ss, I, torch, pk, reps=20):
+    """ss_scan_fwd on the Mamba-130M-shaped layer (batch 8, D 1536, N 16, L 2048, bf16
+    inputs, gate), the single-pass entry point's own workload."""
+    p = I.workload("mamba130m_layer_bf16", device="cuda", gen_device="cuda")
+    elems, byts, exps = workload_counts(p.batch, p.dim, p.dstate, p.seqlen)
+    y = torch.empty((p.batch, p.dim, p.seqlen), device="cuda")
+    hl = torch.empty((p.batch, p.dim, p.dstate), device="cuda")
+    kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, y=y, last_state=hl)
+    for _ in range(3):
+        ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, **kw)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, **kw)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    roof = roofline_terms(byts, exps, ms, pk)
+    return {"workload": "mamba130m_layer_bf16: batch=8, D=1536, N=16, L=2048, bf16 inputs, gate",
+            "entry_point": "ss_scan_fwd", "ms": round(ms, 4), "elem_per_s": elems / (ms * 1e-3),
+            "roofline": roof, "note": "inputs 0.25 GB, about twice the L2: no flush between repetitions",
+            "gpu_launches": reps}
+
+
+def bench_zoh_step(ss, torch, p, kw, elems, reps=5):
+    """The long-sequence chunked step with the zero-order-hold input weight."""
+    for _ in range(2):
+        ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, zoh=True, **kw)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, zoh=True, **kw)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    return {"entry_point": "ss_scan_chunked with SS_FLAG_ZOH, same workload", "ms_per_step": round(ms, 4),
+            "elem_per_s": elems / (ms * 1e-3), "gpu_launches": 3 * reps}
 
 
 def bench_conv(ss, torch, pk, batch=1, dim=5120, seqlen=65536, reps=20):
@@ -492,7 +538,8 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode and conv1d side measurements")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the side measurements (decode, conv1d, ZOH step, single-pass layer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dim", type=int, default=5120, help="channels (5120 = the workload; smaller only for profiling)")

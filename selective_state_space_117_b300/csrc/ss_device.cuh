@@ -128,22 +128,26 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // Input weight of the zero-order hold, (exp(dt A) - 1) / A, for a pair of states,
 // given arg = dt * A * log2(e), e = exp2(arg), dt as a pair and inv_a = 1/A (0
-// where A = 0).  Where |dt A| >= 1/2 it is (e - 1) / A; below, where e - 1 would
-// cancel, it is dt * E(dt A) with E(y) = (exp(y) - 1) / y = sum_k y^k / (k + 1)!
-// cut after y^6 (truncation below 2e-7 relative for |y| < 1/2; the series also
-// gives the limit dt at A = 0).
-__device__ __forceinline__ f2 hold2(f2 arg, f2 e, f2 dtp, f2 inv_a) {
-  const f2 y = mul2(arg, splat(kLn2));
-  f2 p = splat(1.f / 5040.f);
-  p = fma2(p, y, splat(1.f / 720.f));
-  p = fma2(p, y, splat(1.f / 120.f));
-  p = fma2(p, y, splat(1.f / 24.f));
+// where A = 0).  Where |dt A| >= 1/10 it is (e - 1) / A: e carries a relative
+// error of about 2^-22, so e - 1 is good to about 2.4e-7 / 0.1 = 2.4e-6 relative.
+// Below, where e - 1 would cancel, it is dt * E(dt A) with E(y) = (exp(y) - 1) / y
+// = 1 + y/2 + y^2/6 + y^3/24 + ..., cut after y^3 (truncation below 1e-6
+// relative for |y| < 1/10; the series also gives the limit dt at A = 0).
+constexpr float kHoldSeriesBelow = 0.1f;
+
+__device__ __forceinline__ f2 hold_series2(f2 y) {
+  f2 p = splat(1.f / 24.f);
   p = fma2(p, y, splat(1.f / 6.f));
   p = fma2(p, y, splat(0.5f));
-  p = fma2(p, y, splat(1.f));
-  const f2 small = mul2(p, dtp);
+  return fma2(p, y, splat(1.f));
+}
+
+__device__ __forceinline__ f2 hold2(f2 arg, f2 e, f2 dtp, f2 inv_a) {
+  const f2 y = mul2(arg, splat(kLn2));
+  const f2 small = mul2(hold_series2(y), dtp);
   const f2 large = mul2(add2(e, splat(-1.f)), inv_a);
-  return pk(fabsf(lo(y)) < 0.5f ? lo(small) : lo(large), fabsf(hi(y)) < 0.5f ? hi(small) : hi(large));
+  return pk(fabsf(lo(y)) < kHoldSeriesBelow ? lo(small) : lo(large),
+            fabsf(hi(y)) < kHoldSeriesBelow ? hi(small) : hi(large));
 }
 
 // The same weight when the two exponentials at the ends of the step are known:
@@ -151,16 +155,10 @@ __device__ __forceinline__ f2 hold2(f2 arg, f2 e, f2 dtp, f2 inv_a) {
 // w_cur * (exp(dt A) - 1) / A, used by the backward local pass.
 __device__ __forceinline__ f2 hold_between2(f2 w_next, f2 w_cur, f2 arg_dt, f2 dtp, f2 inv_a) {
   const f2 y = mul2(arg_dt, splat(kLn2));
-  f2 p = splat(1.f / 5040.f);
-  p = fma2(p, y, splat(1.f / 720.f));
-  p = fma2(p, y, splat(1.f / 120.f));
-  p = fma2(p, y, splat(1.f / 24.f));
-  p = fma2(p, y, splat(1.f / 6.f));
-  p = fma2(p, y, splat(0.5f));
-  p = fma2(p, y, splat(1.f));
-  const f2 small = mul2(mul2(p, dtp), w_cur);
+  const f2 small = mul2(mul2(hold_series2(y), dtp), w_cur);
   const f2 large = mul2(add2(w_next, mul2(w_cur, splat(-1.f))), inv_a);
-  return pk(fabsf(lo(y)) < 0.5f ? lo(small) : lo(large), fabsf(hi(y)) < 0.5f ? hi(small) : hi(large));
+  return pk(fabsf(lo(y)) < kHoldSeriesBelow ? lo(small) : lo(large),
+            fabsf(hi(y)) < kHoldSeriesBelow ? hi(small) : hi(large));
 }
 
 // ---------------------------------------------------------------- bf16
