@@ -50,6 +50,10 @@ def _bind(path):
     lib.sso_delta.restype = ctypes.c_double
     lib.sso_conv1d.argtypes = [i64, i64, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int, dp, ctypes.c_int]
     lib.sso_conv1d.restype = ctypes.c_int
+    lib.sso_scan_bwd.argtypes = [i64, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp,
+                                 ctypes.c_int, vp, i64, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                                 ctypes.c_int, ctypes.c_int]
+    lib.sso_scan_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -118,6 +122,54 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *,
     return y, hl
 
 
+def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, dy, dlast=None,
+             dtype="f32", h0=None, chans=None, want_BC=True, nthreads=0, zoh=False, lib=None):
+    """Gradients of  sum(dy * y) + sum(dlast * h_last)  for the scan of ``scan``.
+
+    ``dy`` is (batch, dim, L) (or (nchan, L) with ``chans``), ``dlast`` and ``h0``
+    (nchan, N); all three are taken as float64.  Returns a dict of float64 arrays:
+    du, ddelta, dz (None without z) shaped like u; dh0 (nchan, N) (None without
+    h0); dB, dC (batch, N, L) over the listed channels (None unless ``want_BC``).
+    Without ``chans``: dA (dim, N), dD, ddelta_bias (dim,) summed over the batch
+    rows (None when D / delta_bias are absent).  With ``chans``: dA_part
+    (nchan, N), dD_part, dbias_part (nchan,) are each channel's own terms."""
+    code = _dtype_code(dtype)
+    u, delta, B, C, z = (_in(x, code) for x in (u, delta, B, C, z))
+    A, D, delta_bias = _f32(A), _f32(D), _f32(delta_bias)
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    assert delta.shape == u.shape and B.shape == (batch, N, L) and C.shape == (batch, N, L)
+    assert A.shape == (dim, N) and (z is None or z.shape == u.shape)
+    ch = None if chans is None else np.ascontiguousarray(chans, dtype=np.int64)
+    nch = batch * dim if ch is None else ch.shape[0]
+    f64 = lambda a, shape: None if a is None else np.ascontiguousarray(a, dtype=np.float64).reshape(shape)
+    dyy, dl, hh0 = f64(dy, (nch, L)), f64(dlast, (nch, N)), f64(h0, (nch, N))
+    du = np.zeros((nch, L)); ddelta = np.zeros((nch, L))
+    dz = np.zeros((nch, L)) if z is not None else None
+    dA_part = np.zeros((nch, N)); dD_part = np.zeros(nch); db_part = np.zeros(nch)
+    dh0 = np.zeros((nch, N)) if h0 is not None else None
+    dB = np.zeros((batch, N, L)) if want_BC else None
+    dC = np.zeros((batch, N, L)) if want_BC else None
+    rc = (lib or _load()).sso_scan_bwd(batch, dim, N, L, code, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                       _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(ch), nch,
+                                       _ptr(hh0), _ptr(dyy), _ptr(dl), _ptr(du), _ptr(ddelta), _ptr(dz),
+                                       _ptr(dA_part), _ptr(dD_part), _ptr(db_part), _ptr(dh0), _ptr(dB), _ptr(dC),
+                                       _threads(nthreads), int(bool(zoh)))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    out = dict(du=du, ddelta=ddelta, dz=dz, dh0=dh0, dB=dB, dC=dC)
+    if ch is None:
+        out["du"], out["ddelta"] = du.reshape(batch, dim, L), ddelta.reshape(batch, dim, L)
+        if dz is not None:
+            out["dz"] = dz.reshape(batch, dim, L)
+        out["dA"] = dA_part.reshape(batch, dim, N).sum(axis=0)
+        out["dD"] = dD_part.reshape(batch, dim).sum(axis=0) if D is not None else None
+        out["ddelta_bias"] = db_part.reshape(batch, dim).sum(axis=0) if delta_bias is not None else None
+    else:
+        out.update(dA_part=dA_part, dD_part=dD_part, dbias_part=db_part)
+    return out
+
+
 def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *,
                  dtype="f32", chans=None, nthreads=0, zoh=False, lib=None):
     """One decode step.  Shapes: u/delta/z (batch, dim); B/C (batch, N);
@@ -181,12 +233,16 @@ class Variant:
     def step_size(self, *a, **k):
         return step_size(*a, lib=self.lib, **k)
 
+    def scan_bwd(self, *a, **k):
+        return scan_bwd(*a, lib=self.lib, **k)
+
     def conv1d(self, *a, **k):
         return conv1d(*a, lib=self.lib, **k)
 
 
 class _Default:
     scan = staticmethod(scan)
+    scan_bwd = staticmethod(scan_bwd)
     state_update = staticmethod(state_update)
     step_size = staticmethod(step_size)
     conv1d = staticmethod(conv1d)

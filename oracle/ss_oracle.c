@@ -224,3 +224,157 @@ int sso_conv1d(int64_t batch, int64_t dim, int64_t seqlen, int dtype, const void
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ backward */
+
+static double sso_sigmoid(double x) {
+    return 1.0 / (1.0 + exp(-x));
+}
+
+/* d/dA of the zero-order-hold weight (exp(dt A) - 1)/A, i.e. (dt exp(dt A) - w)/A.
+ * That form cancels for small dt*A; there it is dt^2 times the series
+ * 1/2 + y/3 + y^2/8 + y^3/30 (y = dt*A), the derivative of (e^y - 1)/y. */
+static double sso_zoh_weight_dA(double dt, double A) {
+    double y = dt * A;
+    if (fabs(y) < 1e-3) return dt * dt * (0.5 + y * (1.0 / 3.0 + y * (1.0 / 8.0 + y / 30.0)));
+    return (dt * exp(y) - expm1(y) / A) / A;
+}
+
+/*
+ * Backward pass of sso_scan: the gradient of
+ *
+ *     Loss = sum_{b,d,t} dy[b,d,t] * y[b,d,t]  +  sum_{b,d,n} dlast[b,d,n] * h_last[b,d,n]
+ *
+ * with respect to every input, i.e. the vector-Jacobian product of the forward
+ * map above with the cotangents (dy, dlast).  The pages fix only the principle
+ * ("Mamba: Linear-Time Sequence Modeling with Selective State Spaces",
+ * azimuth.plus, the "Recomputation" technique; "Mamba State Space Models:
+ * Fixed State, Linear Time", deepnoodle.ai, "Fixed state instead of a growing
+ * cache"): the states are not stored by the forward pass but recomputed.  Here
+ * each channel's states are recomputed by a forward sweep, then the chain
+ * rule is applied step by step in reverse time.  With
+ *     e = exp(dt A[n]),  w = dt (Euler) or (e - 1)/A[n] (zero-order hold),
+ *     h_t = e h_{t-1} + w B_t u_t,  s_t = sum_n C_t h_t + D u_t,  y_t = s_t silu(z_t),
+ * and mu[n] the gradient reaching h_t from later steps (dlast at t = L-1):
+ *     ds     = dy silu(z),           dz = dy s silu'(z)
+ *     lam[n] = mu[n] + C_t[n] ds     (total gradient of h_t[n])
+ *     dC_t  += ds h_t,  dD += ds u,  du = D ds + sum_n lam w B_t
+ *     dB_t  += lam w u
+ *     ddt    = sum_n lam (h_{t-1} e A + B_t u dw/ddt)     dw/ddt = 1 or e
+ *     dA    += lam (h_{t-1} e dt + B_t u dw/dA)             dw/dA  = 0 or sso_zoh_weight_dA
+ *     ddelta = ddt softplus'(x) = ddt sigmoid(x)   (ddt when the flag is off),  dbias += ddelta
+ *     mu[n]  = e lam                 (carried to step t-1; dh0 = mu after t = 0)
+ *
+ * Arguments follow sso_scan.  Cotangents: dy (nchans, seqlen) and dlast
+ * (nchans, dstate, nullable = 0), both double.  Per-channel outputs, packed by
+ * list position: du, ddelta (nchans, seqlen); dz (nchans, seqlen, nullable,
+ * only with z); dA_part (nchans, dstate), dD_part, dbias_part (nchans) are this
+ * channel's terms of dA[d,:], dD[d], ddelta_bias[d] (the caller sums over
+ * batch rows); dh0 (nchans, dstate, nullable).  dB, dC (batch, dstate, seqlen),
+ * nullable: zeroed, then the listed channels' terms are added.
+ */
+int sso_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int dtype,
+                 const void* u, const void* delta, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                 const int64_t* chans, int64_t nchans, const double* h0,
+                 const double* dy, const double* dlast,
+                 double* du, double* ddelta, double* dz, double* dA_part, double* dD_part,
+                 double* dbias_part, double* dh0, double* dB, double* dC, int nthreads, int zoh) {
+    if (batch < 0 || dim < 0 || dstate < 0 || seqlen < 0) return -1;
+    if (dtype != SSO_F32 && dtype != SSO_BF16) return -1;
+    int64_t total = batch * dim;
+    if (chans == NULL) nchans = total;
+    if (nthreads < 1) nthreads = 1;
+    const int64_t N = dstate, L = seqlen;
+    if (dB) memset(dB, 0, sizeof(double) * (size_t)(batch * N * L));
+    if (dC) memset(dC, 0, sizeof(double) * (size_t)(batch * N * L));
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(|:bad)
+    for (int64_t i = 0; i < nchans; ++i) {
+        int64_t c = chans ? chans[i] : i;
+        if (c < 0 || c >= total) { bad = 1; continue; }
+        int64_t b = c / dim, d = c % dim;
+        const float* Ad = A + d * N;
+        double bias = delta_bias ? (double)delta_bias[d] : 0.0;
+        double Dd = D ? (double)D[d] : 0.0;
+        /* hist[t * N + n] = h_{t-1}[n] for t = 0..L (hist row 0 = h0, row L = h_last) */
+        double* hist = (double*)calloc((size_t)((L + 1) * N + 1), sizeof(double));
+        double* dts = (double*)malloc(sizeof(double) * (size_t)(L + 1));
+        double* mu = (double*)calloc((size_t)(N + 1), sizeof(double));
+        double* dBc = (double*)calloc((size_t)(N * L + 1), sizeof(double));
+        double* dCc = (double*)calloc((size_t)(N * L + 1), sizeof(double));
+        double* dAc = (double*)calloc((size_t)(N + 1), sizeof(double));
+        for (int64_t n = 0; n < N; ++n) hist[n] = h0 ? h0[i * N + n] : 0.0;
+
+        /* forward sweep: recompute dt_t and every state */
+        for (int64_t t = 0; t < L; ++t) {
+            int64_t ix = c * L + t;
+            double x = sso_widen(delta, ix, dtype) + bias;
+            double dt = softplus_flag ? sso_softplus(x) : x;
+            double uu = sso_widen(u, ix, dtype);
+            dts[t] = dt;
+            for (int64_t n = 0; n < N; ++n) {
+                double Bn = sso_widen(B, b * N * L + n * L + t, dtype);
+                double e = exp(dt * (double)Ad[n]);
+                double w = zoh ? sso_zoh_weight(dt, (double)Ad[n]) : dt;
+                hist[(t + 1) * N + n] = e * hist[t * N + n] + w * Bn * uu;
+            }
+        }
+
+        /* reverse sweep */
+        for (int64_t n = 0; n < N; ++n) mu[n] = dlast ? dlast[i * N + n] : 0.0;
+        double dDc = 0.0, dbc = 0.0;
+        for (int64_t t = L - 1; t >= 0; --t) {
+            int64_t ix = c * L + t;
+            double x = sso_widen(delta, ix, dtype) + bias;
+            double dt = dts[t];
+            double uu = sso_widen(u, ix, dtype);
+            const double* hp = hist + t * N;          /* h_{t-1} */
+            const double* hc = hist + (t + 1) * N;    /* h_t */
+            double s = Dd * uu;
+            for (int64_t n = 0; n < N; ++n) s += sso_widen(C, b * N * L + n * L + t, dtype) * hc[n];
+            double ds = dy[i * L + t];
+            if (z) {
+                double zz = sso_widen(z, ix, dtype);
+                double sg = sso_sigmoid(zz);
+                ds = dy[i * L + t] * zz * sg;
+                if (dz) dz[i * L + t] = dy[i * L + t] * s * sg * (1.0 + zz * (1.0 - sg));
+            }
+            dDc += ds * uu;
+            double duv = Dd * ds, ddt = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double An = (double)Ad[n];
+                double Bn = sso_widen(B, b * N * L + n * L + t, dtype);
+                double Cn = sso_widen(C, b * N * L + n * L + t, dtype);
+                double e = exp(dt * An);
+                double w = zoh ? sso_zoh_weight(dt, An) : dt;
+                double lam = mu[n] + Cn * ds;
+                dCc[n * L + t] = ds * hc[n];
+                dBc[n * L + t] = lam * w * uu;
+                duv += lam * w * Bn;
+                ddt += lam * (hp[n] * e * An + Bn * uu * (zoh ? e : 1.0));
+                dAc[n] += lam * (hp[n] * e * dt + (zoh ? Bn * uu * sso_zoh_weight_dA(dt, An) : 0.0));
+                mu[n] = e * lam;
+            }
+            double dx = softplus_flag ? ddt * sso_sigmoid(x) : ddt;
+            du[i * L + t] = duv;
+            ddelta[i * L + t] = dx;
+            dbc += dx;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            dA_part[i * N + n] = dAc[n];
+            if (dh0) dh0[i * N + n] = mu[n];
+        }
+        dD_part[i] = dDc;
+        dbias_part[i] = dbc;
+        if (dB || dC) {
+#pragma omp critical(sso_bwd_bc)
+            for (int64_t k = 0; k < N * L; ++k) {
+                if (dB) dB[b * N * L + k] += dBc[k];
+                if (dC) dC[b * N * L + k] += dCc[k];
+            }
+        }
+        free(hist); free(dts); free(mu); free(dBc); free(dCc); free(dAc);
+    }
+    return bad ? -1 : 0;
+}

@@ -439,8 +439,130 @@ def pin_conv_linear_causal(orc):
     assert np.array_equal(o3[:, :, :17], o1[:, :, :17]) and not np.array_equal(o3[:, :, 17:21], o1[:, :, 17:21])
 
 
+# ---------------------------------------------------------------- backward pass
+#
+# The gradients are pinned by finite differences of the forward oracle, which
+# the pins above fix independently: for every input element x, the fourth-order
+# central difference  (8 (L(x+h) - L(x-h)) - (L(x+2h) - L(x-2h))) / (12 h)  of
+#     L = sum(dy * y) + sum(dlast * h_last)
+# must match the oracle's adjoint.  h = 2^-10 keeps every perturbed fp32 input
+# exact (inputs are multiples of 2^-12 below 2^12 in size), so the difference quotient has only
+# its O(h^4) truncation error, far below the tolerance.
+
+FD_H = 2.0 ** -10
+
+
+def _fd_case(seed, softplus=True, zoh=False, gate=True, with_D=True, with_bias=True, h0=True, dlast=True):
+    p = rand_problem(seed, batch=2, dim=2, N=3, L=7, gate=gate, with_D=with_D, with_bias=with_bias)
+    r = np.random.default_rng(seed + 100)
+    if not softplus:                     # dt = raw + bias must stay positive without the softplus
+        p["delta"] = f32(np.abs(r.normal(size=p["u"].shape)) * 0.4 + 0.05)
+        if with_bias:
+            p["delta_bias"] = f32(r.uniform(0.0, 0.2, size=p["delta_bias"].shape))
+    for k, v in p.items():               # snap to a 2^-12 grid: x +- h, x +- 2h are then exact in fp32
+        if v is not None:
+            p[k] = f32(np.round(v.astype(np.float64) * 4096.0) / 4096.0)
+    nch = 4
+    extra = dict(
+        dy=r.normal(size=(2, 2, 7)),
+        dlast=r.normal(size=(nch, 3)) if dlast else None,
+        h0=r.normal(size=(nch, 3)) if h0 else None,
+    )
+    return p, extra, softplus, zoh
+
+
+def _fd_loss(orc, p, extra, softplus, zoh):
+    y, hl = orc.scan(**p, softplus=softplus, h0=extra["h0"], zoh=zoh)
+    out = float(np.sum(extra["dy"].reshape(y.shape) * y))
+    if extra["dlast"] is not None:
+        out += float(np.sum(extra["dlast"] * hl))
+    return out
+
+
+def _fd_check(orc, case, tol=1e-9):
+    p, extra, softplus, zoh = case
+    g = orc.scan_bwd(**p, softplus=softplus, dy=extra["dy"], dlast=extra["dlast"], h0=extra["h0"], zoh=zoh)
+    names = {"u": "du", "delta": "ddelta", "z": "dz", "B": "dB", "C": "dC", "A": "dA", "D": "dD",
+             "delta_bias": "ddelta_bias"}
+    checked = 0
+    for key, gkey in list(names.items()) + [("h0", "dh0")]:
+        src = extra if key == "h0" else p
+        if src[key] is None:
+            continue
+        base = src[key]
+        adj = np.asarray(g[gkey], dtype=np.float64).reshape(base.shape)
+        fd = np.zeros(base.shape)
+        for idx in np.ndindex(base.shape):
+            vals = []
+            for k in (1, -1, 2, -2):
+                pert = base.copy()
+                pert[idx] = pert[idx] + k * FD_H
+                assert float(pert[idx]) - float(base[idx]) == k * FD_H     # exact perturbation
+                if key == "h0":
+                    e2 = dict(extra, h0=pert)
+                    vals.append(_fd_loss(orc, p, e2, softplus, zoh))
+                else:
+                    vals.append(_fd_loss(orc, dict(p, **{key: pert}), extra, softplus, zoh))
+            fd[idx] = (8.0 * (vals[0] - vals[1]) - (vals[2] - vals[3])) / (12.0 * FD_H)
+        scale = max(1.0, float(np.max(np.abs(fd))))
+        err = float(np.max(np.abs(adj - fd)))
+        assert err <= tol * scale, f"d{key}: adjoint vs finite difference {err:.3e} (scale {scale:.3e})"
+        checked += 1
+    return checked
+
+
+def pin_bwd_finite_difference(orc):
+    """Every gradient of the full model (softplus step, bias, D, gate, h0, dlast)."""
+    assert _fd_check(orc, _fd_case(11)) == 9
+
+
+def pin_bwd_finite_difference_plain(orc):
+    """Softplus off, no bias, no D, no gate, zero initial state: the bare recurrence."""
+    assert _fd_check(orc, _fd_case(12, softplus=False, gate=False, with_D=False, with_bias=False, h0=False)) == 5
+
+
+def pin_bwd_finite_difference_zoh(orc):
+    """Zero-order-hold input weight: its derivatives in dt and A enter ddelta and dA."""
+    assert _fd_check(orc, _fd_case(13, zoh=True)) == 9
+
+
+def pin_bwd_finite_difference_zoh_small_A(orc):
+    """Zero-order hold where dt*A is tiny or zero (A = 0 and A = -2^-12): the
+    series form of the hold weight's A-derivative, including its A -> 0 limit dt^2/2."""
+    case = _fd_case(16, zoh=True)
+    case[0]["A"][:, 0] = 0.0
+    case[0]["A"][:, 1] = -(2.0 ** -12)
+    assert _fd_check(orc, case) == 9
+
+
+def pin_bwd_zero_cotangent(orc):
+    """Zero cotangents give exactly zero gradients (the map is linear in (dy, dlast))."""
+    p, extra, softplus, zoh = _fd_case(14)
+    g = orc.scan_bwd(**p, dy=np.zeros_like(extra["dy"]), dlast=None, h0=extra["h0"])
+    for k in ("du", "ddelta", "dz", "dB", "dC", "dA", "dD", "ddelta_bias", "dh0"):
+        assert np.all(g[k] == 0.0), k
+
+
+def pin_bwd_channel_subset(orc):
+    """Per-channel outputs for a subset of channels equal those of the full call."""
+    p, extra, softplus, zoh = _fd_case(15)
+    full = orc.scan_bwd(**p, dy=extra["dy"], dlast=extra["dlast"], h0=extra["h0"])
+    chans = np.array([3, 0])
+    sub = orc.scan_bwd(**p, dy=extra["dy"].reshape(4, 7)[chans], dlast=extra["dlast"][chans],
+                       h0=extra["h0"][chans], chans=chans, want_BC=False)
+    assert np.array_equal(sub["du"], full["du"].reshape(4, 7)[chans])
+    assert np.array_equal(sub["dh0"], full["dh0"][chans])
+    dA = sub["dA_part"]
+    assert np.allclose(full["dA"][1], dA[0] + orc.scan_bwd(**p, dy=extra["dy"].reshape(4, 7)[[1]],
+                                                            dlast=extra["dlast"][[1]], h0=extra["h0"][[1]],
+                                                            chans=[1], want_BC=False)["dA_part"][0],
+                       rtol=1e-14, atol=1e-14)
+
+
 PINS = [pin_tiny_example, pin_selective_toy, pin_lti_convolution, pin_unrolled_sum, pin_zero_step_keeps_state,
         pin_large_step_resets, pin_recurrence_equals_scan, pin_linear_and_causal, pin_gated_rnn_decay,
         pin_inverse_softplus_bias, pin_bf16_widening, pin_channel_subset, pin_degenerate_sizes,
         pin_conv_impulse_response, pin_conv_worked_sum, pin_conv_identity_silu, pin_conv_linear_causal,
-        pin_zoh_theorem1, pin_zoh_limits, pin_zoh_lti_convolution]
+        pin_zoh_theorem1, pin_zoh_limits, pin_zoh_lti_convolution,
+        pin_bwd_finite_difference, pin_bwd_finite_difference_plain, pin_bwd_finite_difference_zoh,
+        pin_bwd_finite_difference_zoh_small_A, pin_bwd_zero_cotangent, pin_bwd_channel_subset]

@@ -52,6 +52,31 @@ MUTANTS = [
     ("conv_bias_dropped", [("double s = bias ? (double)bias[d] : 0.0;", "double s = 0.0;")]),
     ("conv_silu_ignored", [("out[c * seqlen + t] = silu_flag ? sso_silu(s) : s;", "out[c * seqlen + t] = s;")]),
     ("conv_wrong_channel_taps", [("(double)w[d * 4 + k]", "(double)w[(d % 2) * 4 + k]")]),
+    # backward pass
+    ("bwd_carry_without_decay", [("mu[n] = e * lam;", "mu[n] = lam;")]),
+    ("bwd_lam_misses_readout", [("double lam = mu[n] + Cn * ds;", "double lam = mu[n];")]),
+    ("bwd_dC_uses_previous_state", [("dCc[n * L + t] = ds * hc[n];", "dCc[n * L + t] = ds * hp[n];")]),
+    ("bwd_dB_missing_weight", [("dBc[n * L + t] = lam * w * uu;", "dBc[n * L + t] = lam * uu;")]),
+    ("bwd_du_missing_skip", [("double duv = Dd * ds, ddt = 0.0;", "double duv = 0.0, ddt = 0.0;")]),
+    ("bwd_ddt_decay_sign", [("ddt += lam * (hp[n] * e * An +", "ddt += lam * (-hp[n] * e * An +")]),
+    ("bwd_ddt_missing_input_term", [("ddt += lam * (hp[n] * e * An + Bn * uu * (zoh ? e : 1.0));",
+                                     "ddt += lam * (hp[n] * e * An);")]),
+    ("bwd_softplus_derivative_dropped", [("double dx = softplus_flag ? ddt * sso_sigmoid(x) : ddt;",
+                                          "double dx = ddt;")]),
+    ("bwd_dA_missing_dt", [("dAc[n] += lam * (hp[n] * e * dt +", "dAc[n] += lam * (hp[n] * e +")]),
+    ("bwd_dA_uses_current_state", [("dAc[n] += lam * (hp[n] * e * dt", "dAc[n] += lam * (hc[n] * e * dt")]),
+    ("bwd_zoh_ddt_weight", [("Bn * uu * (zoh ? e : 1.0)", "Bn * uu")]),
+    ("bwd_zoh_dA_term_dropped", [("(zoh ? Bn * uu * sso_zoh_weight_dA(dt, An) : 0.0)", "0.0")]),
+    ("bwd_zoh_dA_series", [("0.5 + y * (1.0 / 3.0", "0.5 + y * (1.0 / 2.0")]),
+    ("bwd_zoh_dA_closed_form", [("return (dt * exp(y) - expm1(y) / A) / A;", "return (dt * exp(y) - expm1(y)) / A;")]),
+    ("bwd_dz_silu_derivative", [("sg * (1.0 + zz * (1.0 - sg))", "sg")]),
+    ("bwd_dz_without_skip", [("double s = Dd * uu;", "double s = 0.0;")]),
+    ("bwd_ds_ignores_gate", [("ds = dy[i * L + t] * zz * sg;", "ds = dy[i * L + t];")]),
+    ("bwd_dD_wrong_factor", [("dDc += ds * uu;", "dDc += ds;")]),
+    ("bwd_dh0_not_decayed", [("if (dh0) dh0[i * N + n] = mu[n];", "if (dh0) dh0[i * N + n] = mu[n] / exp(dts[0] * (double)Ad[n]);")]),
+    ("bwd_dlast_ignored", [("mu[n] = dlast ? dlast[i * N + n] : 0.0;", "mu[n] = 0.0;")]),
+    ("bwd_dB_wrong_batch", [("if (dB) dB[b * N * L + k] += dBc[k];", "if (dB) dB[k] += dBc[k];")]),
+    ("bwd_dbias_not_summed", [("dbc += dx;", "dbc = dx;")]),
 ]
 
 
