@@ -230,6 +230,47 @@ int ss_scan_chunked_static(const ss_dims* dims, const void* u, const void* delta
 int ss_causal_conv1d(const ss_dims* dims, const void* x, const float* weight, const float* bias, int silu_flag,
                      void* out, ss_stream_t stream);
 
+/*
+ * Backward pass: the gradients of
+ *
+ *     Loss = sum_{b,d,t} dy[b,d,t] y[b,d,t] + sum_{b,d,n} dlast_state[b,d,n] last_state[b,d,n]
+ *
+ * where (y, last_state) is the forward scan of ss_scan_fwd_h0 on the same
+ * inputs (Euler input weight; dims->flags must be 0).  The forward pass keeps
+ * no states: this call recomputes them ("Recomputation" in "Mamba: Linear-Time
+ * Sequence Modeling with Selective State Spaces", azimuth.plus: recompute the
+ * intermediate states in the backward pass instead of storing them; likewise
+ * "Fixed state instead of a growing cache", deepnoodle.ai).
+ *
+ * Inputs are those of ss_scan_fwd_h0 (h0 nullable), plus
+ *   dy           (batch, dim, seqlen) fp32, the gradient of y
+ *   dlast_state  (batch, dim, dstate) fp32 or NULL (zero), the gradient of last_state
+ * Outputs, all fp32, caller-owned:
+ *   du, ddelta   (batch, dim, seqlen)              required
+ *   dz           (batch, dim, seqlen) or NULL      only when z is given (SS_EINVAL otherwise)
+ *   dA           (dim, dstate)                     required
+ *   dB, dC       (batch, dstate, seqlen)           required
+ *   dD, ddelta_bias  (dim) or NULL                 the gradient at the given D / delta_bias
+ *                                                  (at 0 when those are NULL)
+ *   dh0          (batch, dim, dstate) or NULL      the gradient at the given h0 (at 0 when NULL)
+ * ddelta is the gradient of the raw delta (before the bias and the softplus).
+ * dA, dB, dC, dD and ddelta_bias are sums over many channels and steps; the
+ * call zeroes them (cudaMemsetAsync on `stream`) and accumulates with atomic
+ * adds, so their last bits may differ from run to run.
+ *
+ * Workspace: ss_scan_bwd_workspace_bytes(dims) bytes, 256-byte aligned, owned by
+ * the caller (for batch 1, dim 5120, N 16, L 65536: 692 MB).  Errors as
+ * ss_scan_chunked; SS_EALIGN if an fp32 array is not 4-byte aligned.
+ * Six kernels and up to five memsets on `stream`, asynchronous.
+ */
+size_t ss_scan_bwd_workspace_bytes(const ss_dims* dims);
+
+int ss_scan_bwd(const ss_dims* dims, const float* h0, const void* u, const void* delta, const float* A,
+                const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                int softplus_flag, const float* dy, const float* dlast_state, float* du, float* ddelta,
+                float* dA, float* dB, float* dC, float* dD, float* dz, float* ddelta_bias, float* dh0,
+                void* workspace, size_t workspace_bytes, ss_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* ss_status_string(int status);
 

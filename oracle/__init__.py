@@ -128,11 +128,12 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, 
 
     ``dy`` is (batch, dim, L) (or (nchan, L) with ``chans``), ``dlast`` and ``h0``
     (nchan, N); all three are taken as float64.  Returns a dict of float64 arrays:
-    du, ddelta, dz (None without z) shaped like u; dh0 (nchan, N) (None without
-    h0); dB, dC (batch, N, L) over the listed channels (None unless ``want_BC``).
-    Without ``chans``: dA (dim, N), dD, ddelta_bias (dim,) summed over the batch
-    rows (None when D / delta_bias are absent).  With ``chans``: dA_part
-    (nchan, N), dD_part, dbias_part (nchan,) are each channel's own terms."""
+    du, ddelta, dz (None without z) shaped like u; dh0 (nchan, N); dB, dC
+    (batch, N, L) over the listed channels (None unless ``want_BC``).  Without
+    ``chans``: dA (dim, N), dD, ddelta_bias (dim,) summed over the batch rows.
+    With ``chans``: dA_part (nchan, N), dD_part, dbias_part (nchan,) are each
+    channel's own terms.  dD, ddelta_bias and dh0 are the gradients at the given
+    D, delta_bias and h0, or at zero where those are absent."""
     code = _dtype_code(dtype)
     u, delta, B, C, z = (_in(x, code) for x in (u, delta, B, C, z))
     A, D, delta_bias = _f32(A), _f32(D), _f32(delta_bias)
@@ -147,7 +148,7 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, 
     du = np.zeros((nch, L)); ddelta = np.zeros((nch, L))
     dz = np.zeros((nch, L)) if z is not None else None
     dA_part = np.zeros((nch, N)); dD_part = np.zeros(nch); db_part = np.zeros(nch)
-    dh0 = np.zeros((nch, N)) if h0 is not None else None
+    dh0 = np.zeros((nch, N))
     dB = np.zeros((batch, N, L)) if want_BC else None
     dC = np.zeros((batch, N, L)) if want_BC else None
     rc = (lib or _load()).sso_scan_bwd(batch, dim, N, L, code, _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
@@ -163,8 +164,8 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, 
         if dz is not None:
             out["dz"] = dz.reshape(batch, dim, L)
         out["dA"] = dA_part.reshape(batch, dim, N).sum(axis=0)
-        out["dD"] = dD_part.reshape(batch, dim).sum(axis=0) if D is not None else None
-        out["ddelta_bias"] = db_part.reshape(batch, dim).sum(axis=0) if delta_bias is not None else None
+        out["dD"] = dD_part.reshape(batch, dim).sum(axis=0)
+        out["ddelta_bias"] = db_part.reshape(batch, dim).sum(axis=0)
     else:
         out.update(dA_part=dA_part, dD_part=dD_part, dbias_part=db_part)
     return out

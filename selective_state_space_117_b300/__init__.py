@@ -20,7 +20,7 @@ from typing import Optional
 
 import torch
 
-__all__ = ["scan_fwd", "scan_chunked", "state_update", "causal_conv1d", "chunked_workspace_bytes", "device_status",
+__all__ = ["scan_fwd", "scan_chunked", "scan_bwd", "bwd_workspace_bytes", "state_update", "causal_conv1d", "chunked_workspace_bytes", "device_status",
            "SSError",
            "library_path",
            "F32", "BF16", "MAX_DSTATE", "LAUNCHES"]
@@ -32,7 +32,7 @@ _lib = None
 F32, BF16 = 0, 1
 MAX_DSTATE = 64
 # Kernels launched per call (for launch accounting): chunked = local + carry + fix-up.
-LAUNCHES = {"scan_fwd": 1, "scan_chunked": 3, "state_update": 1}
+LAUNCHES = {"scan_fwd": 1, "scan_chunked": 3, "state_update": 1, "scan_bwd": 5}
 
 SS_OK, SS_EINVAL, SS_EALIGN, SS_EDTYPE, SS_EWORKSPACE, SS_ECUDA, SS_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 
@@ -89,6 +89,11 @@ def lib():
         L.ss_last_cuda_error.restype = ctypes.c_int
         L.ss_causal_conv1d.argtypes = [dp, vp, vp, vp, ctypes.c_int, vp, vp]
         L.ss_causal_conv1d.restype = ctypes.c_int
+        L.ss_scan_bwd_workspace_bytes.argtypes = [dp]
+        L.ss_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
+        L.ss_scan_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp,
+                                  vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.ss_scan_bwd.restype = ctypes.c_int
         L.ss_device_status.argtypes = [ctypes.c_int]
         L.ss_device_status.restype = ctypes.c_int
         _lib = L
@@ -219,6 +224,50 @@ def scan_chunked(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=Tr
     else:
         _check(lib().ss_scan_chunked_phase(int(phase), ctypes.byref(dims), *tail), f"ss_scan_chunked_phase({phase})")
     return (y, last_state) if last_state is not None else y
+
+
+def bwd_workspace_bytes(batch, dim, dstate, seqlen, dtype=F32) -> int:
+    dims = Dims(batch, dim, dstate, seqlen, dtype)
+    return int(lib().ss_scan_bwd_workspace_bytes(ctypes.byref(dims)))
+
+
+def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, dy, dlast=None, h0=None,
+             want_dD=True, want_dbias=True, want_dh0=None, workspace=None, stream=None):
+    """Backward pass of ``scan_fwd`` (ss_scan_bwd): the gradients of
+    sum(dy * y) + sum(dlast * last_state) for the forward scan on the same inputs.
+
+    dy is fp32 (batch, dim, L); dlast and h0 are fp32 (batch, dim, N) or None.
+    Returns a dict of fp32 tensors: du, ddelta (like u), dz (like u, or None
+    without z), dA (dim, N), dB, dC (batch, N, L), dD and ddelta_bias (dim,)
+    (None unless ``want_dD`` / ``want_dbias``), dh0 (batch, dim, N) (computed
+    when ``want_dh0``, by default when h0 is given).  ``workspace`` is an optional
+    uint8 CUDA tensor of at least ``bwd_workspace_bytes`` bytes."""
+    dims, _ = _scan_common(u, delta, A, B, C, D, z, delta_bias, dy, None)
+    batch, dim, N, L = dims.batch, dims.dim, dims.dstate, dims.seqlen
+    dev = u.device
+    _need(dlast, "dlast", (batch, dim, N), torch.float32, dev)
+    _need(h0, "h0", (batch, dim, N), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(du=torch.empty((batch, dim, L), **f32), ddelta=torch.empty((batch, dim, L), **f32),
+               dz=torch.empty((batch, dim, L), **f32) if z is not None else None,
+               dA=torch.empty((dim, N), **f32), dB=torch.empty((batch, N, L), **f32),
+               dC=torch.empty((batch, N, L), **f32),
+               dD=torch.empty((dim,), **f32) if want_dD else None,
+               ddelta_bias=torch.empty((dim,), **f32) if want_dbias else None,
+               dh0=torch.empty((batch, dim, N), **f32) if (want_dh0 if want_dh0 is not None else h0 is not None)
+               else None)
+    need = int(lib().ss_scan_bwd_workspace_bytes(ctypes.byref(dims)))
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+    if workspace.device != dev or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
+    st = lib().ss_scan_bwd(ctypes.byref(dims), _ptr(h0), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                           _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(dy), _ptr(dlast),
+                           _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]),
+                           _ptr(out["dD"]), _ptr(out["dz"]), _ptr(out["ddelta_bias"]), _ptr(out["dh0"]),
+                           _ptr(workspace), workspace.numel(), _stream(dev, stream))
+    _check(st, "ss_scan_bwd")
+    return out
 
 
 def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, y=None,

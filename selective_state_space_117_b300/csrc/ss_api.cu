@@ -295,6 +295,96 @@ int ss_causal_conv1d(const ss_dims* dims, const void* x, const float* weight, co
   return launched();
 }
 
+size_t ss_scan_bwd_workspace_bytes(const ss_dims* dims) {
+  if (!dims || dims->batch < 0 || dims->dim < 0 || dims->dstate < 0 || dims->seqlen < 0) return 0;
+  const int64_t K = ceil_div(dims->seqlen, ssk::kBwdChunk);
+  const size_t s_bytes = (size_t)(dims->batch * dims->dim * K) * sizeof(float);
+  const size_t h_bytes = (size_t)(dims->batch * dims->dim * K * dims->dstate) * sizeof(float);
+  return align_up(s_bytes, kWsAlign) + align_up(h_bytes, kWsAlign) + h_bytes;
+}
+
+int ss_scan_bwd(const ss_dims* dims, const float* h0, const void* u, const void* delta, const float* A,
+                const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+                int softplus_flag, const float* dy, const float* dlast_state, float* du, float* ddelta, float* dA,
+                float* dB, float* dC, float* dD, float* dz, float* ddelta_bias, float* dh0, void* workspace,
+                size_t workspace_bytes, ss_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int st = check_scan(dims, u, delta, A, B, C, D, z, delta_bias, dy, nullptr);
+  if (st != SS_OK) return st;
+  const ss_dims& d = *dims;
+  if (d.flags != 0) return SS_EINVAL;                       // Euler input weight only
+  const bool rows = d.batch > 0 && d.dim > 0 && d.seqlen > 0;
+  if (rows && (!du || !ddelta)) return SS_EINVAL;
+  if (rows && d.dstate > 0 && (!dB || !dC)) return SS_EINVAL;
+  if (d.dim > 0 && d.dstate > 0 && !dA) return SS_EINVAL;
+  if (dz && !z) return SS_EINVAL;
+  for (const void* p : {(const void*)h0, (const void*)dlast_state, (const void*)du, (const void*)ddelta,
+                        (const void*)dA, (const void*)dB, (const void*)dC, (const void*)dD, (const void*)dz,
+                        (const void*)ddelta_bias, (const void*)dh0})
+    if (!aligned(p, 4)) return SS_EALIGN;
+  const bool work = d.batch > 0 && d.dim > 0 && d.seqlen > 0;
+  const size_t need = ss_scan_bwd_workspace_bytes(dims);
+  if (work && (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes < need)) return SS_EWORKSPACE;
+  if (work && (int64_t)ceil_div(d.dim, ssk::kCh) * ceil_div(d.seqlen, ssk::kBwdChunk) > kMaxGridX) return SS_EINVAL;
+  if (work && (int64_t)ssk::bwd_main_ctiles(d.dim, d.dstate) * ceil_div(d.seqlen, ssk::kBwdChunk) > kMaxGridX)
+    return SS_EINVAL;
+
+  // Accumulated gradients start from zero.
+  auto zero = [&](float* p, int64_t n) -> int {
+    if (!p || n <= 0) return SS_OK;
+    const cudaError_t e = cudaMemsetAsync(p, 0, (size_t)n * sizeof(float), s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e);
+  };
+  int rc = SS_OK;
+  if ((rc = zero(dA, d.dim * d.dstate)) != SS_OK || (rc = zero(dB, d.batch * d.dstate * d.seqlen)) != SS_OK ||
+      (rc = zero(dC, d.batch * d.dstate * d.seqlen)) != SS_OK || (rc = zero(dD, d.dim)) != SS_OK ||
+      (rc = zero(ddelta_bias, d.dim)) != SS_OK)
+    return rc;
+  if (d.batch == 0 || d.dim == 0) return SS_OK;
+  if (d.seqlen == 0) {                                      // dh0 = dlast
+    if (!dh0) return SS_OK;
+    const size_t n = (size_t)(d.batch * d.dim * d.dstate) * sizeof(float);
+    if (n == 0) return SS_OK;
+    const cudaError_t e = dlast_state ? cudaMemcpyAsync(dh0, dlast_state, n, cudaMemcpyDeviceToDevice, s)
+                                      : cudaMemsetAsync(dh0, 0, n, s);
+    return e == cudaSuccess ? SS_OK : cuda_fail(e);
+  }
+
+  // The state entering every chunk: the forward local pass and carry at the backward's chunk length.
+  ssk::ScanArgs f = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, nullptr, nullptr,
+                                   ssk::kBwdChunk);
+  f.h0 = h0;
+  const int64_t K = f.nchunks;
+  char* ws = static_cast<char*>(workspace);
+  const size_t s_bytes = align_up((size_t)(d.batch * d.dim * K) * sizeof(float), kWsAlign);
+  const size_t h_bytes = align_up((size_t)(d.batch * d.dim * K * d.dstate) * sizeof(float), kWsAlign);
+  f.ws_S = reinterpret_cast<float*>(ws);
+  f.ws_H = reinterpret_cast<float*>(ws + s_bytes);
+  const bool bf = d.in_dtype == SS_BF16;
+  const dim3 grid((unsigned)(f.ctiles * K), (unsigned)d.batch);
+  if (!(ssk::tma_available(f, bf, ssk::kLocal) && ssk::launch_local_tma(f, bf, grid, s) == 0) &&
+      ssk::launch_scan_local(f, bf, grid, s) != 0)
+    return SS_EINVAL;
+  if (ssk::launch_carry(f, s) != 0) return SS_EINVAL;
+
+  ssk::BwdArgs a{};
+  a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias;
+  a.dy = dy; a.dlast = dlast_state;
+  a.du = du; a.ddelta = ddelta; a.dz = dz; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dbias = ddelta_bias;
+  a.dh0 = dh0;
+  a.ws_S = f.ws_S; a.ws_H = f.ws_H;
+  a.ws_G = reinterpret_cast<float*>(ws + s_bytes + h_bytes);
+  a.batch = d.batch; a.dim = d.dim; a.dstate = d.dstate; a.seqlen = d.seqlen; a.nchunks = K;
+  a.softplus = softplus_flag ? 1 : 0;
+  const size_t es = in_size(d.in_dtype);
+  const bool rows16 = (d.seqlen * (int64_t)es) % 16 == 0 && (d.seqlen * 4) % 16 == 0;
+  a.vec = (rows16 && aligned(u, 16) && aligned(delta, 16) && aligned(z, 16) && aligned(dy, 16) && aligned(du, 16) &&
+           aligned(ddelta, 16) && aligned(dz, 16) && aligned(dB, 8) && aligned(dC, 8)) ? 1 : 0;
+  a.vec_bc = ((d.seqlen * (int64_t)es) % 16 == 0 && aligned(B, 16) && aligned(C, 16)) ? 1 : 0;
+  if (ssk::launch_bwd(a, bf, z != nullptr, s) != 0) return SS_EINVAL;
+  return launched();
+}
+
 const char* ss_status_string(int status) {
   switch (status) {
     case SS_OK: return "SS_OK";

@@ -1,0 +1,542 @@
+// Backward pass of the selective scan (Euler input weight): the gradients of
+//     Loss = sum dy * y + sum dlast * h_last
+// with respect to u, delta, A, B, C, D, z, delta_bias and h0.
+//
+// The forward pass stores no states; the backward pass recomputes them
+// ("Recomputation", "Mamba: Linear-Time Sequence Modeling with Selective State
+// Spaces").  With e_t = exp(dt_t A), ds_t = dy_t silu(z_t) and lambda_t the
+// total gradient of h_t, the adjoint runs backward in time,
+//     lambda_t = C_t ds_t + e_{t+1} lambda_{t+1},
+// the same kind of linear recurrence as the forward one, so it is chunked the
+// same way.  Four launches after the forward local pass and carry (reused at
+// kBwdChunk-step chunks, they give the state entering every chunk):
+//   bwd_local_kernel  per chunk, the adjoint's zero-start sum
+//                       G[n] = sum_{t in chunk} exp(A[n] P_t) C_t[n] ds_t,  P_t = sum_{r=t0..t} dt_r
+//                     (the forward local pass mirrored: it walks the chunk forward);
+//   bwd_carry_kernel  mu_{K-1} = dlast, mu_{k-1} = G_k + exp(A S_k) mu_k over the chunks, last
+//                     first: mu_k is the gradient reaching the chunk's last state from later
+//                     steps, and mu_{-1} = e_0 lambda_0 is dh0;
+//   bwd_main_kernel   per chunk: a forward sweep from the entering state leaves a checkpoint
+//                     every kSub steps; then every kSub-step sub-block, last first, is
+//                     recomputed with its states and decays in registers and walked backward,
+//                     forming all gradients.
+#include "ss_device.cuh"
+#include "ss_dispatch.cuh"
+#include "ss_launch.h"
+#include "ss_occupancy.cuh"
+
+namespace ssk {
+
+namespace {
+
+constexpr int kSub = 8;                        // steps per sub-block of the main pass
+constexpr int kNsub = kBwdChunk / kSub;
+
+// sigmoid(x) = 1 / (1 + e^-x)
+__device__ __forceinline__ float sigm(float x) { return rcp(1.f + ex2(-x * kLog2e)); }
+
+// Eight consecutive elements of a row, [t, t + 8) clipped to t_end (zeros past it);
+// one 16-byte-aligned vector load when `vec` and the group is whole.
+template <bool BF>
+__device__ __forceinline__ void load_group(const void* p, int64_t off, int64_t t, int64_t t_end, bool vec, float (&v)[8]) {
+  using L = In<BF>;
+  if (vec && t + 8 <= t_end) {
+    const typename L::Raw8 r = L::load8(p, off);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const f2 x = L::pair(r, q);
+      v[2 * q] = lo(x);
+      v[2 * q + 1] = hi(x);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = t + j < t_end ? L::one(p, off + j) : 0.f;
+  }
+}
+
+__device__ __forceinline__ void load_group_f32(const float* p, int64_t off, int64_t t, int64_t t_end, bool vec,
+                                               float (&v)[8]) {
+  if (vec && t + 8 <= t_end) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p + off));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p + off) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = t + j < t_end ? __ldg(p + off + j) : 0.f;
+  }
+}
+
+// Stage rows [0, NT) x steps [t0, t0 + kBwdChunk) of a (b, N, L) array as fp32
+// [t][n] in shared memory; rows n >= N and steps past t_end are zeros.
+template <int NT, bool BF>
+__device__ __forceinline__ void stage_bc(float* s, const void* src, int64_t row0, int N, int64_t L, int64_t t0,
+                                         int64_t t_end, bool vec, int tid, int nthreads) {
+  constexpr int kG = kBwdChunk / 8;
+  for (int e = tid; e < NT * kG; e += nthreads) {
+    const int n = e / kG, g = e % kG;
+    float v[8];
+    if (n < N) {
+      load_group<BF>(src, row0 + (int64_t)n * L + t0 + 8 * g, t0 + 8 * g, t_end, vec, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[(8 * g + j) * NT + n] = v[j];
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------- adjoint local pass
+
+// One thread per (b, d, chunk), NT states as pairs; a block is kCh channels of one (b, chunk).
+template <int NT, bool BF, bool HAS_Z>
+__global__ void __launch_bounds__(kCh) bwd_local_kernel(const BwdArgs a) {
+  constexpr int NP = NT / 2;
+  __shared__ __align__(16) float sC[kBwdChunk * NT];
+  const int tid = threadIdx.x;
+  const int ct = blockIdx.x % a.ctiles;
+  const int64_t k = blockIdx.x / a.ctiles, b = blockIdx.y;
+  const int64_t d = (int64_t)ct * kCh + tid;
+  const bool active = d < a.dim;
+  const int N = (int)a.dstate;
+  const int64_t L = a.seqlen, t0 = k * kBwdChunk, t_end = min(L, t0 + kBwdChunk);
+
+  stage_bc<NT, BF>(sC, a.C, b * N * L, N, L, t0, t_end, a.vec_bc, tid, kCh);
+  __syncthreads();
+  if (!active) return;
+
+  f2 A2[NP], acc[NP];
+  const float* Arow = a.A + d * N;
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    A2[q] = pk(2 * q < N ? Arow[2 * q] * kLog2e : 0.f, 2 * q + 1 < N ? Arow[2 * q + 1] * kLog2e : 0.f);
+    acc[q] = pk(0.f, 0.f);
+  }
+  const float bias = a.delta_bias ? a.delta_bias[d] : 0.f;
+  const int64_t row = (b * a.dim + d) * L;
+  float P = 0.f;
+  for (int g = 0; g < kBwdChunk / 8; ++g) {
+    const int64_t t = t0 + 8 * g;
+    if (t >= t_end) break;
+    float xd[8], dyv[8], zv[8];
+    load_group<BF>(a.delta, row + t, t, t_end, a.vec, xd);
+    load_group_f32(a.dy, row + t, t, t_end, a.vec, dyv);
+    if (HAS_Z) load_group<BF>(a.z, row + t, t, t_end, a.vec, zv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (t + j < t_end) {
+        const float x = xd[j] + bias;
+        const float dt = a.softplus ? softplus(x) : x;
+        const float ds = HAS_Z ? dyv[j] * silu(zv[j]) : dyv[j];
+        P += dt;
+        const f2 Pp = pk(P, P), dsp = pk(ds, ds);
+        const float* rc = sC + (8 * g + j) * NT;
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+          const f2 c2 = *reinterpret_cast<const f2*>(rc + 2 * q);
+          acc[q] = fma2(ex2x2(mul2(Pp, A2[q])), mul2(dsp, c2), acc[q]);
+        }
+      }
+    }
+  }
+  float* G = a.ws_G + ((b * a.dim + d) * a.nchunks + k) * N;
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    if (2 * q < N) G[2 * q] = lo(acc[q]);
+    if (2 * q + 1 < N) G[2 * q + 1] = hi(acc[q]);
+  }
+}
+
+// ---------------------------------------------------------------------------- adjoint carry
+
+// One thread per (b, d, n): the chunks' adjoint sums G_k become mu_k, last chunk first;
+// the value after chunk 0 is dh0.  Loads run 8 chunks ahead of the dependent chain.
+__global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t N = a.dstate;
+  if (i >= a.batch * a.dim * N) return;
+  const int64_t n = i % N, bd = i / N, d = bd % a.dim;
+  const float A2 = a.A[d * N + n] * kLog2e;
+  const int64_t K = a.nchunks;
+  float* G = a.ws_G + bd * K * N + n;
+  const float* S = a.ws_S + bd * K;
+  float mu = a.dlast ? a.dlast[bd * N + n] : 0.f;
+  for (int64_t k0 = K - 1; k0 >= 0; k0 -= 8) {
+    float gv[8], sv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool ok = k0 - u >= 0;
+      gv[u] = ok ? G[(k0 - u) * N] : 0.f;
+      sv[u] = ok ? S[k0 - u] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (k0 - u >= 0) {
+        G[(k0 - u) * N] = mu;
+        mu = fmaf(ex2(A2 * sv[u]), mu, gv[u]);
+      }
+    }
+  }
+  if (a.dh0) a.dh0[bd * N + n] = mu;
+}
+
+// ---------------------------------------------------------------------------- main pass
+
+// Geometry: a lane owns 4 consecutive states (two f32x2 pairs) of one channel,
+// kLpc = NT / 4 lanes per channel, kCpb channels per block.
+template <int NT>
+struct BwdGeom {
+  static constexpr int kLpc = NT / 4;
+  static constexpr int kThreads = NT >= 8 ? 128 : 64;
+  static constexpr int kCpb = kThreads / kLpc;
+  // dB/dC staging: [q][channel][step pair][n][2], channel rows padded by 2 floats
+  // so that the 16 lanes of a 64-bit store phase hit distinct banks.
+  static constexpr int kRedRow = 8 * NT + 2;
+  static constexpr int kFloats = 2 * kBwdChunk * NT          // sB, sC
+                                 + 2 * kBwdChunk * kCpb      // sDt (dt, du)
+                                 + 4 * kNsub * kThreads      // sCk checkpoints
+                                 + 4 * kSub * kCpb           // sE (ds, sigmoid(x), dz factor, u)
+                                 + 4 * kSub * kThreads       // sPQR partial sums
+                                 + 2 * kCpb * kRedRow;       // sRed
+  static constexpr size_t kBytes = (size_t)kFloats * 4;
+};
+
+// Per-lane work of the main pass (NT states per channel, BF input dtype, HAS_Z gate).
+template <int NT, bool BF, bool HAS_Z>
+__global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const BwdArgs a) {
+  using G = BwdGeom<NT>;
+  constexpr int kLpc = G::kLpc, kCpb = G::kCpb, kT = G::kThreads;
+  extern __shared__ __align__(16) float smem[];
+  float* sB = smem;
+  float* sC = sB + kBwdChunk * NT;
+  float2* sDt = reinterpret_cast<float2*>(sC + kBwdChunk * NT);          // [t][ci]
+  float4* sCk = reinterpret_cast<float4*>(sDt + kBwdChunk * kCpb);       // [sb][tid]
+  float4* sE = sCk + kNsub * kT;                                          // [j][ci]
+  float4* sPQR = sE + kSub * kCpb;                                        // [j][tid]
+  float* sRed = reinterpret_cast<float*>(sPQR + kSub * kT);               // [q][ci][jp][n][2]
+
+  const int tid = threadIdx.x;
+  const int ct = blockIdx.x % a.ctiles;
+  const int64_t k = blockIdx.x / a.ctiles, b = blockIdx.y;
+  const int ci = tid / kLpc, li = tid % kLpc, n0 = 4 * li;
+  const int64_t d0 = (int64_t)ct * kCpb, d = d0 + ci;
+  const bool active = d < a.dim;
+  const int N = (int)a.dstate;
+  const int64_t L = a.seqlen, t0 = k * kBwdChunk, t_end = min(L, t0 + kBwdChunk);
+  const int64_t bc_row = b * N * L;
+
+  // ---- prologue: B and C of the chunk; dt and du of every (channel, step)
+  stage_bc<NT, BF>(sB, a.B, bc_row, N, L, t0, t_end, a.vec_bc, tid, kT);
+  stage_bc<NT, BF>(sC, a.C, bc_row, N, L, t0, t_end, a.vec_bc, tid, kT);
+  for (int e = tid; e < kCpb * (kBwdChunk / 8); e += kT) {
+    const int c = e / (kBwdChunk / 8), g = e % (kBwdChunk / 8);
+    const int64_t dc = d0 + c, t = t0 + 8 * g;
+    float xd[8], uv[8];
+    if (dc < a.dim) {
+      const int64_t row = (b * a.dim + dc) * L;
+      load_group<BF>(a.delta, row + t, t, t_end, a.vec, xd);
+      load_group<BF>(a.u, row + t, t, t_end, a.vec, uv);
+    }
+    const float bias = (dc < a.dim && a.delta_bias) ? a.delta_bias[dc] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float dt = 0.f, du = 0.f;
+      if (dc < a.dim && t + j < t_end) {
+        const float x = xd[j] + bias;
+        dt = a.softplus ? softplus(x) : x;
+        du = dt * uv[j];
+      }
+      sDt[(8 * g + j) * kCpb + c] = make_float2(dt, du);
+    }
+  }
+
+  // This lane's states n0..n0+3 as pairs (q = 0: n0, n0+1; q = 1: n0+2, n0+3).
+  f2 A2[2], h[2], mu[2], dA[2];
+  {
+    const int64_t ws = ((b * a.dim + (active ? d : 0)) * a.nchunks + k) * N;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float av[2], hv[2], mv[2];
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int n = n0 + 2 * q + s;
+        const bool ok = active && n < N;
+        av[s] = ok ? a.A[d * N + n] * kLog2e : 0.f;
+        hv[s] = ok ? a.ws_H[ws + n] : 0.f;
+        mv[s] = ok ? a.ws_G[ws + n] : 0.f;
+      }
+      A2[q] = pk(av[0], av[1]);
+      h[q] = pk(hv[0], hv[1]);
+      mu[q] = pk(mv[0], mv[1]);
+      dA[q] = pk(0.f, 0.f);
+    }
+  }
+  __syncthreads();
+
+  // ---- forward sweep over the chunk: a checkpoint before every sub-block
+  for (int sb = 0; sb < kNsub; ++sb) {
+    sCk[sb * kT + tid] = make_float4(lo(h[0]), hi(h[0]), lo(h[1]), hi(h[1]));
+#pragma unroll
+    for (int j = 0; j < kSub; ++j) {
+      const int t = sb * kSub + j;
+      const float2 s = sDt[t * kCpb + ci];
+      const f2 dtp = pk(s.x, s.x), dup = pk(s.y, s.y);
+      const float4 bv = *reinterpret_cast<const float4*>(sB + t * NT + n0);
+      h[0] = fma2(ex2x2(mul2(dtp, A2[0])), h[0], mul2(dup, pk(bv.x, bv.y)));
+      h[1] = fma2(ex2x2(mul2(dtp, A2[1])), h[1], mul2(dup, pk(bv.z, bv.w)));
+    }
+  }
+
+  // Epilogue items of a sub-block: (channel ci_e, step pair jp_e), jp fastest.
+  constexpr int kItems = kCpb * (kSub / 2);
+  constexpr int kSlots = (kItems + kT - 1) / kT;
+  float dD_acc[kSlots], db_acc[kSlots];
+#pragma unroll
+  for (int r = 0; r < kSlots; ++r) dD_acc[r] = db_acc[r] = 0.f;
+  const float* Dp = a.D;
+
+  // ---- sub-blocks, last first
+  for (int sb = kNsub - 1; sb >= 0; --sb) {
+    const int64_t ts = t0 + sb * kSub;
+    // per-(channel, step) scalars of the backward sweep
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r) {
+      const int it = tid + r * kT;
+      if (it < kItems) {
+        const int c = it / (kSub / 2), jp = it % (kSub / 2);
+        const int64_t dc = d0 + c;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const int j = 2 * jp + s;
+          const int64_t t = ts + j;
+          float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (dc < a.dim && t < t_end) {
+            const int64_t ix = (b * a.dim + dc) * L + t;
+            const float dyv = __ldg(a.dy + ix);
+            const float uu = In<BF>::one(a.u, ix);
+            const float x = In<BF>::one(a.delta, ix) + (a.delta_bias ? a.delta_bias[dc] : 0.f);
+            e.y = a.softplus ? sigm(x) : 1.f;
+            e.w = uu;
+            if (HAS_Z) {
+              const float zz = In<BF>::one(a.z, ix);
+              const float sg = sigm(zz);
+              e.x = dyv * zz * sg;                              // ds = dy silu(z)
+              e.z = dyv * sg * fmaf(zz, 1.f - sg, 1.f);         // dy silu'(z)
+            } else {
+              e.x = dyv;
+            }
+          }
+          sE[j * kCpb + c] = e;
+        }
+      }
+    }
+    // recompute the sub-block's states from its checkpoint
+    f2 ev[kSub][2], hv[kSub][2];
+    {
+      const float4 c4 = sCk[sb * kT + tid];
+      f2 hp0 = pk(c4.x, c4.y), hp1 = pk(c4.z, c4.w);
+#pragma unroll
+      for (int j = 0; j < kSub; ++j) {
+        const int t = sb * kSub + j;
+        const float2 s = sDt[t * kCpb + ci];
+        const f2 dtp = pk(s.x, s.x), dup = pk(s.y, s.y);
+        const float4 bv = *reinterpret_cast<const float4*>(sB + t * NT + n0);
+        ev[j][0] = ex2x2(mul2(dtp, A2[0]));
+        ev[j][1] = ex2x2(mul2(dtp, A2[1]));
+        hp0 = fma2(ev[j][0], hp0, mul2(dup, pk(bv.x, bv.y)));
+        hp1 = fma2(ev[j][1], hp1, mul2(dup, pk(bv.z, bv.w)));
+        hv[j][0] = hp0;
+        hv[j][1] = hp1;
+      }
+    }
+    const float4 ck = sCk[sb * kT + tid];
+    __syncthreads();   // sE written; the previous sub-block's sPQR / sRed readers are done
+
+    // walk the sub-block backward
+    f2 dBn[2], dCn[2];   // the later step's dB / dC of this lane (written in step pairs)
+#pragma unroll
+    for (int j = kSub - 1; j >= 0; --j) {
+      const int t = sb * kSub + j;
+      const float2 s = sDt[t * kCpb + ci];
+      const float4 e = sE[j * kCpb + ci];
+      const f2 dtp = pk(s.x, s.x), dup = pk(s.y, s.y), dsp = pk(e.x, e.x);
+      const float4 bv = *reinterpret_cast<const float4*>(sB + t * NT + n0);
+      const float4 cv = *reinterpret_cast<const float4*>(sC + t * NT + n0);
+      const f2 B2[2] = {pk(bv.x, bv.y), pk(bv.z, bv.w)};
+      const f2 C2[2] = {pk(cv.x, cv.y), pk(cv.z, cv.w)};
+      const f2 hprev[2] = {j > 0 ? hv[j > 0 ? j - 1 : 0][0] : pk(ck.x, ck.y),
+                           j > 0 ? hv[j > 0 ? j - 1 : 0][1] : pk(ck.z, ck.w)};
+      f2 lam[2], g[2], dBv[2], dCv[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        lam[q] = fma2(dsp, C2[q], mu[q]);        // total gradient of h_t
+        mu[q] = mul2(ev[j][q], lam[q]);          // carried to step t - 1
+        g[q] = mul2(mu[q], hprev[q]);            // lambda e h_{t-1}
+        dA[q] = fma2(g[q], dtp, dA[q]);
+        dBv[q] = mul2(lam[q], dup);
+        dCv[q] = mul2(dsp, hv[j][q]);
+      }
+      const f2 P = fma2(lam[1], B2[1], mul2(lam[0], B2[0]));
+      const f2 Q = fma2(g[1], A2[1], mul2(g[0], A2[0]));
+      float Rs = 0.f;
+      if (HAS_Z) {
+        const f2 R = fma2(C2[1], hv[j][1], mul2(C2[0], hv[j][0]));
+        Rs = lo(R) + hi(R);
+      }
+      sPQR[j * kT + tid] = make_float4(lo(P) + hi(P), lo(Q) + hi(Q), Rs, 0.f);
+      if (j & 1) {
+        dBn[0] = dBv[0]; dBn[1] = dBv[1];
+        dCn[0] = dCv[0]; dCn[1] = dCv[1];
+      } else {
+        float* rB = sRed + ci * G::kRedRow + (j / 2) * NT * 2 + n0 * 2;
+        float* rC = rB + kCpb * G::kRedRow;
+        *reinterpret_cast<float2*>(rB + 0) = make_float2(lo(dBv[0]), lo(dBn[0]));
+        *reinterpret_cast<float2*>(rB + 2) = make_float2(hi(dBv[0]), hi(dBn[0]));
+        *reinterpret_cast<float2*>(rB + 4) = make_float2(lo(dBv[1]), lo(dBn[1]));
+        *reinterpret_cast<float2*>(rB + 6) = make_float2(hi(dBv[1]), hi(dBn[1]));
+        *reinterpret_cast<float2*>(rC + 0) = make_float2(lo(dCv[0]), lo(dCn[0]));
+        *reinterpret_cast<float2*>(rC + 2) = make_float2(hi(dCv[0]), hi(dCn[0]));
+        *reinterpret_cast<float2*>(rC + 4) = make_float2(lo(dCv[1]), lo(dCn[1]));
+        *reinterpret_cast<float2*>(rC + 6) = make_float2(hi(dCv[1]), hi(dCn[1]));
+      }
+    }
+    __syncthreads();
+
+    // per-(channel, step) gradients: du, ddelta, dz
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r) {
+      const int it = tid + r * kT;
+      if (it < kItems) {
+        const int c = it / (kSub / 2), jp = it % (kSub / 2);
+        const int64_t dc = d0 + c;
+        if (dc < a.dim) {
+          const float Dd = Dp ? Dp[dc] : 0.f;
+          float o_du[2], o_dd[2], o_dz[2];
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            const int j = 2 * jp + s;
+            float P = 0.f, Q = 0.f, R = 0.f;
+#pragma unroll
+            for (int l = 0; l < kLpc; ++l) {
+              const float4 v = sPQR[j * kT + c * kLpc + l];
+              P += v.x; Q += v.y; R += v.z;
+            }
+            const float4 e = sE[j * kCpb + c];
+            const float dt = sDt[(sb * kSub + j) * kCpb + c].x;
+            const float ddt = fmaf(e.w, P, Q * kLn2);        // u P + sum lambda e h A
+            o_du[s] = fmaf(Dd, e.x, dt * P);
+            o_dd[s] = ddt * e.y;
+            o_dz[s] = fmaf(Dd, e.w, R) * e.z;
+            dD_acc[r] = fmaf(e.x, e.w, dD_acc[r]);
+            db_acc[r] += o_dd[s];
+          }
+          const int64_t ix = (b * a.dim + dc) * L + ts + 2 * jp;
+          const int64_t t = ts + 2 * jp;
+          if (a.vec && t + 2 <= t_end) {
+            *reinterpret_cast<float2*>(a.du + ix) = make_float2(o_du[0], o_du[1]);
+            *reinterpret_cast<float2*>(a.ddelta + ix) = make_float2(o_dd[0], o_dd[1]);
+            if (HAS_Z && a.dz) *reinterpret_cast<float2*>(a.dz + ix) = make_float2(o_dz[0], o_dz[1]);
+          } else {
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              if (t + s < t_end) {
+                a.du[ix + s] = o_du[s];
+                a.ddelta[ix + s] = o_dd[s];
+                if (HAS_Z && a.dz) a.dz[ix + s] = o_dz[s];
+              }
+            }
+          }
+        }
+      }
+    }
+    // dB, dC: sums over the block's channels, one atomic add per (b, n, step pair)
+    for (int o = tid; o < 2 * (kSub / 2) * NT; o += kT) {
+      const int n = o % NT, jp = (o / NT) % (kSub / 2), q = o / (NT * (kSub / 2));
+      const int64_t t = ts + 2 * jp;
+      if (n < N && t < t_end) {
+        const float* src = sRed + q * kCpb * G::kRedRow + jp * NT * 2 + n * 2;
+        f2 acc = pk(0.f, 0.f);
+#pragma unroll 8
+        for (int c = 0; c < kCpb; ++c) acc = add2(acc, *reinterpret_cast<const f2*>(src + c * G::kRedRow));
+        float* dst = (q ? a.dC : a.dB) + bc_row + (int64_t)n * L + t;
+        if (a.vec && t + 2 <= t_end) {            // 8-byte aligned: dB, dC checked, L % 8 == 0, t even
+          atomicAdd(reinterpret_cast<float2*>(dst), make_float2(lo(acc), hi(acc)));
+        } else {
+          atomicAdd(dst, lo(acc));
+          if (t + 1 < t_end) atomicAdd(dst + 1, hi(acc));
+        }
+      }
+    }
+  }
+
+  // ---- per-channel sums
+  if (active) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int n = n0 + 2 * q + s;
+        if (n < N) atomicAdd(a.dA + d * N + n, s ? hi(dA[q]) : lo(dA[q]));
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kSlots; ++r) {
+    // the 4 items of a channel sit on 4 consecutive lanes
+    float v0 = dD_acc[r], v1 = db_acc[r];
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+    const int it = tid + r * kT;
+    const int64_t dc = d0 + it / (kSub / 2);
+    if (it < kItems && it % (kSub / 2) == 0 && dc < a.dim) {
+      if (a.dD) atomicAdd(a.dD + dc, v0);
+      if (a.dbias) atomicAdd(a.dbias + dc, v1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------- launchers
+
+template <int NT, bool BF, bool Z>
+static int go_bwd(const BwdArgs& a0, cudaStream_t s) {
+  BwdArgs a = a0;
+  // adjoint local pass
+  a.ctiles = (int)((a.dim + kCh - 1) / kCh);
+  const dim3 g1((unsigned)(a.ctiles * a.nchunks), (unsigned)a.batch);
+  bwd_local_kernel<NT, BF, Z><<<g1, kCh, 0, s>>>(a);
+  // adjoint carry
+  const int64_t total = a.batch * a.dim * a.dstate;
+  if (total > 0) bwd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(a);
+  // main pass
+  using G = BwdGeom<NT>;
+  auto k = bwd_main_kernel<NT, BF, Z>;
+  if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kBytes) != cudaSuccess)
+    return 1;
+  a.ctiles = (int)((a.dim + G::kCpb - 1) / G::kCpb);
+  const dim3 g3((unsigned)(a.ctiles * a.nchunks), (unsigned)a.batch);
+  k<<<g3, G::kThreads, G::kBytes, s>>>(a);
+  return 0;
+}
+
+int bwd_main_ctiles(int64_t dim, int64_t dstate) {
+  int cpb = 0;
+  SSK_DISPATCH_NT(dstate, { cpb = BwdGeom<NT>::kCpb; });
+  return (int)((dim + cpb - 1) / cpb);
+}
+
+int launch_bwd(const BwdArgs& a, bool bf16, bool has_z, cudaStream_t s) {
+  SSK_DISPATCH_NT(a.dstate, {
+    if (bf16) {
+      return has_z ? go_bwd<NT, true, true>(a, s) : go_bwd<NT, true, false>(a, s);
+    } else {
+      return has_z ? go_bwd<NT, false, true>(a, s) : go_bwd<NT, false, false>(a, s);
+    }
+  });
+  return -1;
+}
+
+}  // namespace ssk

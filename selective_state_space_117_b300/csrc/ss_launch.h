@@ -27,6 +27,12 @@ inline int launch_scan_local(const ScanArgs& a, bool bf16, dim3 grid, cudaStream
 int launch_carry(const ScanArgs& a, cudaStream_t s);
 int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
 
+// Backward pass after the forward local pass and carry: adjoint local pass, adjoint carry, main
+// pass (ss_bwd.cu).  Returns 0 when launched.
+int launch_bwd(const BwdArgs& a, bool bf16, bool has_z, cudaStream_t s);
+// Channel tiles of the main backward kernel (its grid is tiles x chunks x batch).
+int bwd_main_ctiles(int64_t dim, int64_t dstate);
+
 // Causal depthwise conv1d (width 4) with optional SiLU; segments of a row per warp.
 int launch_conv1d(const ConvArgs& a, bool bf16, bool silu_on, cudaStream_t s);
 int64_t conv1d_segments(int64_t seqlen);

@@ -34,6 +34,43 @@ struct ScanArgs {
   int zoh;           // 1: zero-order-hold input weight (exp(dt A) - 1) / A instead of dt
 };
 
+// Backward pass.  Chunks of kBwdChunk steps; the workspace holds, per (b, d, chunk k):
+//   ws_S[k]    sum of dt over the chunk (written by the forward local pass)
+//   ws_H[k][n] the state entering chunk k (forward local pass, then the carry)
+//   ws_G[k][n] the chunk's adjoint sum, then mu_k = exp(A dt_{t1}) lambda_{t1}: the
+//              gradient reaching the chunk's last state from the steps after it
+constexpr int kBwdChunk = 64;
+
+struct BwdArgs {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* delta_bias;
+  const float* dy;       // (batch, dim, L) fp32
+  const float* dlast;    // (batch, dim, N) or null
+  float* du;             // (batch, dim, L)
+  float* ddelta;         // (batch, dim, L)
+  float* dz;             // (batch, dim, L) or null (only with z)
+  float* dA;             // (dim, N), accumulated
+  float* dB;             // (batch, N, L), accumulated
+  float* dC;             // (batch, N, L), accumulated
+  float* dD;             // (dim) or null, accumulated
+  float* dbias;          // (dim) or null, accumulated
+  float* dh0;            // (batch, dim, N) or null
+  const float* ws_S;
+  const float* ws_H;
+  float* ws_G;
+  int64_t batch, dim, dstate, seqlen, nchunks;
+  int ctiles;            // channel tiles per (b, chunk) of the launched kernel
+  int softplus;
+  int vec;               // 1: u/delta/z rows, dy and the fp32 gradient rows allow 16-byte group loads
+  int vec_bc;            // 1: B/C rows allow 16-byte loads of 8-step groups
+};
+
 // Causal depthwise conv1d of width 4 over (rows = batch * dim, seqlen).
 struct ConvArgs {
   const void* x;

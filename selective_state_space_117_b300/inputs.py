@@ -187,6 +187,27 @@ def decode_stream(*, seed=4, batch=256, dim=5120, dstate=16, steps=1024, dtype=t
     return st
 
 
+@dataclass
+class Cotangents:
+    """The backward pass's extra inputs: the gradient of y, of the final state,
+    and an initial state (fp32)."""
+    dy: torch.Tensor                 # (batch, dim, L)
+    dlast: Optional[torch.Tensor]    # (batch, dim, N)
+    h0: Optional[torch.Tensor]       # (batch, dim, N)
+
+
+def cotangents(*, seed, batch, dim, dstate, seqlen, with_dlast=True, with_h0=True, device="cpu",
+               gen_device=None) -> Cotangents:
+    """dy ~ N(0, 1); dlast, h0 ~ N(0, 1/4).  Drawn in the order dy, dlast, h0."""
+    gd = gen_device or device
+    g = _gen(seed, gd)
+    dy = _normal((batch, dim, seqlen), 1.0, g, gd)
+    dlast = _normal((batch, dim, dstate), 0.5, g, gd) if with_dlast else None
+    h0 = _normal((batch, dim, dstate), 0.5, g, gd) if with_h0 else None
+    mv = lambda t: None if t is None else t.to(device)
+    return Cotangents(mv(dy), mv(dlast), mv(h0))
+
+
 def to_wire(t: Optional[torch.Tensor]):
     """Host numpy view of a tensor in the oracle's wire format (fp32, or bf16 as uint16 bits)."""
     import numpy as np

@@ -100,6 +100,41 @@ def test_workspace_bytes():
     assert ss.chunked_workspace_bytes(2, 3, 5, 7, 3) == 256 + 2 * 3 * 3 * 5 * 4
 
 
+def _bwd(dims, ws=P, ws_bytes=1 << 40, **over):
+    a = dict(h0=None, u=P, delta=P, A=P, B=P, C=P, D=None, z=None, bias=None, dy=P, dlast=None, du=P, ddelta=P,
+             dA=P, dB=P, dC=P, dD=None, dz=None, dbias=None, dh0=None)
+    a.update(over)
+    return ss.lib().ss_scan_bwd(ctypes.byref(dims), a["h0"], a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"],
+                                a["z"], a["bias"], 1, a["dy"], a["dlast"], a["du"], a["ddelta"], a["dA"], a["dB"],
+                                a["dC"], a["dD"], a["dz"], a["dbias"], a["dh0"], ws, ws_bytes, None)
+
+
+def test_bwd_validation():
+    zoh = _dims()
+    zoh.flags = 1                                           # the backward pass is Euler only
+    assert _bwd(zoh) == ss.SS_EINVAL
+    assert _bwd(_dims(dt=5)) == ss.SS_EDTYPE
+    assert _bwd(_dims(), dy=None) == ss.SS_EINVAL
+    assert _bwd(_dims(), du=None) == ss.SS_EINVAL
+    assert _bwd(_dims(), ddelta=None) == ss.SS_EINVAL
+    assert _bwd(_dims(), dB=None) == ss.SS_EINVAL
+    assert _bwd(_dims(), dA=None) == ss.SS_EINVAL
+    assert _bwd(_dims(), dz=P) == ss.SS_EINVAL                # dz without a gate
+    assert _bwd(_dims(), dA=P + 2) == ss.SS_EALIGN
+    assert _bwd(_dims(), dh0=P + 1) == ss.SS_EALIGN
+    assert _bwd(_dims(), ws=None) == ss.SS_EWORKSPACE
+    assert _bwd(_dims(), ws=P + 16) == ss.SS_EWORKSPACE
+    assert _bwd(_dims(), ws_bytes=ss.bwd_workspace_bytes(1, 4, 4, 16) - 1) == ss.SS_EWORKSPACE
+
+
+def test_bwd_workspace_bytes():
+    # S: batch*dim*K floats, then H and G: batch*dim*K*N floats each, the first two padded to 256 B
+    assert ss.bwd_workspace_bytes(1, 4, 4, 16) == 256 + 256 + 1 * 4 * 1 * 4 * 4
+    K = 65536 // 64
+    assert ss.bwd_workspace_bytes(1, 5120, 16, 65536) == 5120 * K * 4 + 2 * 5120 * K * 16 * 4
+    assert ss.bwd_workspace_bytes(2, 3, 5, 130) == 256 + 512 + 2 * 3 * 3 * 5 * 4   # K = 3
+
+
 def test_state_update_validation():
     lib = ss.lib()
     d = _dims()

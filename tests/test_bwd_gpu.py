@@ -1,0 +1,184 @@
+"""GPU parity of the backward pass (ss_scan_bwd) against the fp64 oracle's
+adjoint, which the finite-difference pins fix.
+
+Every gradient is compared element by element:
+    |g - g_ref| <= TOL_GRAD * max(|g_ref|, rms(g_ref))
+for fp32 and bf16 inputs alike (both sides read the same bf16 bytes; the
+arithmetic is fp32 on the GPU).  TOL_GRAD = 1e-4, the bound of the fp32
+forward scan: the adjoint and the recomputed states chain decays that are each
+a MUFU.EX2 with ~2^-22 relative error, and dA, dD, ddelta_bias, dB, dC are fp32
+sums of up to L or dim terms.  The errors measured on B300 stay below 4e-6.
+
+At the long-sequence size (batch 1, dim 5120, N 16, L 65536, bf16) the oracle
+computes sampled channels one by one; dB, dC and du over all channels are
+checked by Euler's identity for functions homogeneous of degree one: y and
+h_last are linear in B, in C and in u (with h0 = 0), so
+    sum dB B = sum dC C = sum dy (y - D u silu(z)) + sum dlast h_last   (dC: without dlast)
+    sum du u = sum dy y + sum dlast h_last.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_117_b300 as ss
+from selective_state_space_117_b300 import inputs as I
+from parity import host, rms
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL_GRAD = 1e-4
+NAMES = ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0")
+
+
+def grad_err(g, ref):
+    g = np.asarray(g, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.all(np.isfinite(g))
+    if ref.size == 0:
+        return 0.0
+    scale = np.maximum(np.abs(ref), max(rms(ref), 1e-30))
+    return float(np.max(np.abs(g - ref) / scale))
+
+
+def make(seed, batch, dim, N, L, dtype, gate=True, with_D=True, with_bias=True, h0=True, dlast=True, softplus=True):
+    p = I.selective_problem("bwd", seed=seed, batch=batch, dim=dim, dstate=N, seqlen=L, dtype=dtype, bc_std=0.5,
+                            d_mode="normal", gate=gate, device=DEV, gen_device="cpu")
+    if not with_D:
+        p.D = None
+    if not with_bias:
+        p.delta_bias = None
+    if not softplus:     # dt = raw (+ bias) is then used as is: keep it positive
+        g = torch.Generator().manual_seed(seed + 7)
+        p.delta = (torch.rand((batch, dim, L), generator=g) * 0.2 + 0.005).to(dtype).to(DEV)
+        if with_bias:
+            p.delta_bias = torch.full((dim,), 0.01, device=DEV)
+        p.softplus = False
+    ct = I.cotangents(seed=seed + 1000, batch=batch, dim=dim, dstate=N, seqlen=L, with_dlast=dlast, with_h0=h0,
+                      device=DEV, gen_device="cpu")
+    return p, ct
+
+
+def gpu_grads(p, ct):
+    return ss.scan_bwd(p.u, p.delta, p.A, p.B, p.C, D=p.D, z=p.z, delta_bias=p.delta_bias, softplus=p.softplus,
+                       dy=ct.dy, dlast=ct.dlast, h0=ct.h0, want_dh0=True)
+
+
+def oracle_grads(p, ct, chans=None):
+    w = I.to_wire
+    nb, nd, N = p.batch, p.dim, p.dstate
+    dy, dl, h0 = host(ct.dy).reshape(nb * nd, -1), ct.dlast, ct.h0
+    dl = None if dl is None else host(dl).reshape(nb * nd, N)
+    h0 = None if h0 is None else host(h0).reshape(nb * nd, N)
+    if chans is not None:
+        dy = dy[chans]
+        dl = None if dl is None else dl[chans]
+        h0 = None if h0 is None else h0[chans]
+    return oracle.scan_bwd(w(p.u), w(p.delta), w(p.A), w(p.B), w(p.C), D=w(p.D), z=w(p.z),
+                           delta_bias=w(p.delta_bias), softplus=p.softplus,
+                           dtype="bf16" if p.in_dtype == I.BF16 else "f32", dy=dy, dlast=dl, h0=h0,
+                           chans=chans, want_BC=chans is None)
+
+
+def compare_all(g, r, p):
+    """Every gradient; dD, ddelta_bias and dh0 are the gradients at 0 where D, delta_bias or h0 are absent,
+    on both sides."""
+    errs = {}
+    for k in NAMES:
+        got = g[k]
+        want = r[k]
+        if k == "dz" and p.z is None:
+            assert got is None and want is None
+            continue
+        errs[k] = grad_err(host(got), np.asarray(want).reshape(tuple(got.shape)))
+        assert errs[k] <= TOL_GRAD, f"{k}: error {errs[k]:.3e} > {TOL_GRAD}"
+    return errs
+
+
+CASES = [
+    # seed, batch, dim, N, L, dtype, options
+    (1, 2, 70, 16, 200, torch.float32, {}),                                   # 3 channel tiles, ragged last chunk
+    (2, 1, 64, 16, 2048, torch.bfloat16, {}),                                 # 32 chunks
+    (3, 2, 33, 13, 77, torch.float32, {}),                                    # padded states, L % 8 != 0 (no vectors)
+    (4, 1, 40, 4, 130, torch.bfloat16, dict(gate=False, with_D=False)),
+    (5, 1, 20, 8, 64, torch.float32, dict(h0=False, dlast=False)),            # exactly one chunk
+    (6, 1, 24, 32, 96, torch.bfloat16, {}),
+    (7, 1, 10, 64, 72, torch.float32, dict(with_bias=False)),
+    (8, 2, 17, 16, 1, torch.float32, {}),                                     # one step
+    (9, 1, 30, 16, 150, torch.float32, dict(softplus=False)),
+    (10, 3, 100, 16, 520, torch.bfloat16, dict(h0=False)),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"s{c[0]}b{c[1]}d{c[2]}n{c[3]}L{c[4]}" for c in CASES])
+def test_bwd_matches_oracle(case):
+    seed, batch, dim, N, L, dtype, opt = case
+    p, ct = make(seed, batch, dim, N, L, dtype, **opt)
+    g = gpu_grads(p, ct)
+    torch.cuda.synchronize()
+    r = oracle_grads(p.to("cpu"), ct)
+    compare_all(g, r, p)
+    assert ss.device_status() == ss.SS_OK
+
+
+def test_bwd_zero_cotangent_gives_zero():
+    p, ct = make(11, 1, 40, 16, 128, torch.float32)
+    ct.dy.zero_()
+    ct.dlast.zero_()
+    g = gpu_grads(p, ct)
+    for k in NAMES:
+        assert torch.count_nonzero(g[k]).item() == 0, k
+
+
+def test_bwd_length_zero():
+    p, ct = make(12, 2, 8, 16, 0, torch.float32)
+    g = gpu_grads(p, ct)
+    assert torch.equal(g["dh0"], ct.dlast)
+    assert torch.count_nonzero(g["dA"]).item() == 0
+
+
+def test_bwd_repeated_calls_agree():
+    """Only the atomically accumulated sums may differ between runs, and only in the last bits."""
+    p, ct = make(13, 1, 96, 16, 512, torch.bfloat16)
+    g1, g2 = gpu_grads(p, ct), gpu_grads(p, ct)
+    for k in ("du", "ddelta", "dz", "dh0"):
+        assert torch.equal(g1[k], g2[k]), k
+    for k in ("dA", "dB", "dC", "dD", "ddelta_bias"):
+        assert grad_err(host(g1[k]), host(g2[k])) <= 1e-5, k
+
+
+def test_bwd_long_sequence_sampled_and_identities():
+    """Batch 1, dim 5120, N 16, L 65536 (bf16, gate): the size and call the benchmark times."""
+    p = I.workload("mamba2p8b_long_bf16", device=DEV, gen_device="cuda")
+    ct = I.cotangents(seed=103, batch=1, dim=p.dim, dstate=p.dstate, seqlen=p.seqlen, with_h0=False, device=DEV,
+                      gen_device="cuda")
+    g = gpu_grads(p, ct)
+    y, hl = ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, D=p.D, z=p.z, delta_bias=p.delta_bias, chunk_len=2048,
+                            return_last_state=True)
+    torch.cuda.synchronize()
+    # sampled channels against the oracle
+    chans = np.array([0, 1, 63, 64, 2047, 3001, 5119])
+    r = oracle_grads(p.to("cpu"), ct, chans=chans)
+    dy_rows = lambda t: host(t).reshape(p.dim, p.seqlen)[chans]
+    for k in ("du", "ddelta", "dz"):
+        e = grad_err(dy_rows(g[k]), r[k])
+        assert e <= TOL_GRAD, f"{k}: {e:.3e}"
+    assert grad_err(host(g["dA"])[chans], r["dA_part"]) <= TOL_GRAD
+    assert grad_err(host(g["dD"])[chans], r["dD_part"]) <= TOL_GRAD
+    assert grad_err(host(g["ddelta_bias"])[chans], r["dbias_part"]) <= TOL_GRAD
+    # Euler's identity for dB, dC, du over every channel (float64 sums on the GPU)
+    f = lambda t: t.double()
+    ds_u = f(p.D)[None, :, None] * f(p.u) * torch.nn.functional.silu(f(p.z))
+    lin_y = (f(ct.dy) * (f(y) - ds_u)).sum()
+    lin_last = (f(ct.dlast) * f(hl)).sum()
+    checks = {
+        "dB": ((f(g["dB"]) * f(p.B)).sum(), lin_y + lin_last, (f(g["dB"]) * f(p.B)).abs().sum()),
+        "dC": ((f(g["dC"]) * f(p.C)).sum(), lin_y, (f(g["dC"]) * f(p.C)).abs().sum()),
+        "du": ((f(g["du"]) * f(p.u)).sum(), (f(ct.dy) * f(y)).sum() + lin_last, (f(g["du"]) * f(p.u)).abs().sum()),
+    }
+    for k, (lhs, rhs, scale) in checks.items():
+        rel = abs(float(lhs - rhs)) / float(scale)
+        assert rel <= 1e-4, f"{k}: Euler identity off by {rel:.3e} of sum |terms|"
