@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kCh) bwd_local_kernel(const BwdArgs a) {
       }
     }
   }
-  float* G = a.ws_G + ((b * a.dim + d) * a.nchunks + k) * N;
+  float* G = a.ws_G + (k * a.batch * a.dim + b * a.dim + d) * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     if (2 * q < N) G[2 * q] = lo(acc[q]);
@@ -159,22 +159,22 @@ __global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a) {
   if (i >= a.batch * a.dim * N) return;
   const int64_t n = i % N, bd = i / N, d = bd % a.dim;
   const float A2 = a.A[d * N + n] * kLog2e;
-  const int64_t K = a.nchunks;
-  float* G = a.ws_G + bd * K * N + n;
-  const float* S = a.ws_S + bd * K;
+  const int64_t K = a.nchunks, BD = a.batch * a.dim;
+  float* G = a.ws_G + bd * N + n;            // chunk k at G[k * BD * N]
+  const float* S = a.ws_S + bd;              // chunk k at S[k * BD]
   float mu = a.dlast ? a.dlast[bd * N + n] : 0.f;
   for (int64_t k0 = K - 1; k0 >= 0; k0 -= 8) {
     float gv[8], sv[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const bool ok = k0 - u >= 0;
-      gv[u] = ok ? G[(k0 - u) * N] : 0.f;
-      sv[u] = ok ? S[k0 - u] : 0.f;
+      gv[u] = ok ? G[(k0 - u) * BD * N] : 0.f;
+      sv[u] = ok ? S[(k0 - u) * BD] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (k0 - u >= 0) {
-        G[(k0 - u) * N] = mu;
+        G[(k0 - u) * BD * N] = mu;
         mu = fmaf(ex2(A2 * sv[u]), mu, gv[u]);
       }
     }
@@ -197,10 +197,17 @@ struct BwdGeom {
   static constexpr int kFloats = 2 * kBwdChunk * NT          // sB, sC
                                  + 2 * kBwdChunk * kCpb      // sDt (dt, du)
                                  + 4 * kNsub * kThreads      // sCk checkpoints
-                                 + 4 * kSub * kCpb           // sE (ds, sigmoid(x), dz factor, u)
+                                 + kSub * kCpb               // sDs: ds = dy silu(z)
                                  + 4 * kSub * kThreads       // sPQR partial sums
                                  + 2 * kCpb * kRedRow;       // sRed
   static constexpr size_t kBytes = (size_t)kFloats * 4;
+  // Slot of lane l's partial sums for step j of channel c in sPQR ([j][l][c] in
+  // 16-byte units): the channel index is XOR-swizzled with the lane and the step
+  // pair, so that both the writes (4 lanes of 2 channels per 8-lane phase) and
+  // the epilogue's reads (4 step pairs of 2 channels) fall on 8 distinct bank groups.
+  static __device__ __forceinline__ int pqr(int j, int l, int c) {
+    return (j * kLpc + l) * kCpb + (c ^ ((2 * ((l ^ (j >> 1)) & 3)) & (kCpb - 1)));
+  }
 };
 
 // Per-lane work of the main pass (NT states per channel, BF input dtype, HAS_Z gate).
@@ -213,8 +220,8 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   float* sC = sB + kBwdChunk * NT;
   float2* sDt = reinterpret_cast<float2*>(sC + kBwdChunk * NT);          // [t][ci]
   float4* sCk = reinterpret_cast<float4*>(sDt + kBwdChunk * kCpb);       // [sb][tid]
-  float4* sE = sCk + kNsub * kT;                                          // [j][ci]
-  float4* sPQR = sE + kSub * kCpb;                                        // [j][tid]
+  float* sDs = reinterpret_cast<float*>(sCk + kNsub * kT);                // [j][ci]
+  float4* sPQR = reinterpret_cast<float4*>(sDs + kSub * kCpb);            // G::pqr(j, l, c)
   float* sRed = reinterpret_cast<float*>(sPQR + kSub * kT);               // [q][ci][jp][n][2]
 
   const int tid = threadIdx.x;
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   // This lane's states n0..n0+3 as pairs (q = 0: n0, n0+1; q = 1: n0+2, n0+3).
   f2 A2[2], h[2], mu[2], dA[2];
   {
-    const int64_t ws = ((b * a.dim + (active ? d : 0)) * a.nchunks + k) * N;
+    const int64_t ws = (k * a.batch * a.dim + b * a.dim + (active ? d : 0)) * N;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       float av[2], hv[2], mv[2];
@@ -273,6 +280,34 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
       dA[q] = pk(0.f, 0.f);
     }
   }
+
+  // Items of a sub-block: (channel c, step pair jp), jp fastest, so that 4 lanes
+  // cover 8 consecutive steps of one channel in global memory.  Their raw inputs
+  // are fetched one sub-block ahead.
+  constexpr int kItems = kCpb * (kSub / 2);
+  constexpr int kSlots = (kItems + kT - 1) / kT;
+  const float* Dp = a.D;
+  float rdy[kSlots][2], ru[kSlots][2], rx[kSlots][2], rz[kSlots][2];
+  auto fetch = [&](int sb) {
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r) {
+      const int it = tid + r * kT;
+      const int c = it / (kSub / 2), jp = it % (kSub / 2);
+      const int64_t dc = d0 + c, t = t0 + sb * kSub + 2 * jp;
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        rdy[r][s] = ru[r][s] = rx[r][s] = rz[r][s] = 0.f;
+        if (it < kItems && dc < a.dim && t + s < t_end) {
+          const int64_t ix = (b * a.dim + dc) * L + t + s;
+          rdy[r][s] = __ldg(a.dy + ix);
+          ru[r][s] = In<BF>::one(a.u, ix);
+          rx[r][s] = In<BF>::one(a.delta, ix);
+          if (HAS_Z) rz[r][s] = In<BF>::one(a.z, ix);
+        }
+      }
+    }
+  };
+  fetch(kNsub - 1);
   __syncthreads();
 
   // ---- forward sweep over the chunk: a checkpoint before every sub-block
@@ -289,54 +324,52 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
     }
   }
 
-  // Epilogue items of a sub-block: (channel ci_e, step pair jp_e), jp fastest.
-  constexpr int kItems = kCpb * (kSub / 2);
-  constexpr int kSlots = (kItems + kT - 1) / kT;
-  float dD_acc[kSlots], db_acc[kSlots];
+  float dD_acc[kSlots], db_acc[kSlots], slot_bias[kSlots], slot_D[kSlots];
 #pragma unroll
-  for (int r = 0; r < kSlots; ++r) dD_acc[r] = db_acc[r] = 0.f;
-  const float* Dp = a.D;
+  for (int r = 0; r < kSlots; ++r) {
+    dD_acc[r] = db_acc[r] = 0.f;
+    const int it = tid + r * kT;
+    const int64_t dc = d0 + it / (kSub / 2);
+    const bool ok = it < kItems && dc < a.dim;
+    slot_bias[r] = (ok && a.delta_bias) ? a.delta_bias[dc] : 0.f;
+    slot_D[r] = (ok && Dp) ? Dp[dc] : 0.f;
+  }
 
   // ---- sub-blocks, last first
   for (int sb = kNsub - 1; sb >= 0; --sb) {
     const int64_t ts = t0 + sb * kSub;
-    // per-(channel, step) scalars of the backward sweep
+    // per-(channel, step) scalars of the items: ds for every lane (shared memory),
+    // sigmoid(x), the dz factor and u kept by the item's thread for its epilogue
+    float e_ds[kSlots][2], e_sig[kSlots][2], e_dzf[kSlots][2], e_u[kSlots][2];
 #pragma unroll
     for (int r = 0; r < kSlots; ++r) {
       const int it = tid + r * kT;
-      if (it < kItems) {
-        const int c = it / (kSub / 2), jp = it % (kSub / 2);
-        const int64_t dc = d0 + c;
+      const int c = it / (kSub / 2), jp = it % (kSub / 2);
+      const int64_t dc = d0 + c;
+      const float bias = slot_bias[r];
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const int j = 2 * jp + s;
-          const int64_t t = ts + j;
-          float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (dc < a.dim && t < t_end) {
-            const int64_t ix = (b * a.dim + dc) * L + t;
-            const float dyv = __ldg(a.dy + ix);
-            const float uu = In<BF>::one(a.u, ix);
-            const float x = In<BF>::one(a.delta, ix) + (a.delta_bias ? a.delta_bias[dc] : 0.f);
-            e.y = a.softplus ? sigm(x) : 1.f;
-            e.w = uu;
-            if (HAS_Z) {
-              const float zz = In<BF>::one(a.z, ix);
-              const float sg = sigm(zz);
-              e.x = dyv * zz * sg;                              // ds = dy silu(z)
-              e.z = dyv * sg * fmaf(zz, 1.f - sg, 1.f);         // dy silu'(z)
-            } else {
-              e.x = dyv;
-            }
-          }
-          sE[j * kCpb + c] = e;
+      for (int s = 0; s < 2; ++s) {
+        // steps past the sequence's end (and absent channels) contribute nothing
+        const bool ok = it < kItems && dc < a.dim && ts + 2 * jp + s < t_end;
+        e_u[r][s] = ru[r][s];
+        e_sig[r][s] = ok ? (a.softplus ? sigm(rx[r][s] + bias) : 1.f) : 0.f;
+        if (HAS_Z) {
+          const float zz = rz[r][s], sg = sigm(zz);
+          e_ds[r][s] = rdy[r][s] * zz * sg;                        // ds = dy silu(z)
+          e_dzf[r][s] = rdy[r][s] * sg * fmaf(zz, 1.f - sg, 1.f);  // dy silu'(z)
+        } else {
+          e_ds[r][s] = rdy[r][s];
+          e_dzf[r][s] = 0.f;
         }
+        if (it < kItems) sDs[(2 * jp + s) * kCpb + c] = e_ds[r][s];
       }
     }
+    if (sb > 0) fetch(sb - 1);
     // recompute the sub-block's states from its checkpoint
     f2 ev[kSub][2], hv[kSub][2];
+    const float4 ck = sCk[sb * kT + tid];
     {
-      const float4 c4 = sCk[sb * kT + tid];
-      f2 hp0 = pk(c4.x, c4.y), hp1 = pk(c4.z, c4.w);
+      f2 hp0 = pk(ck.x, ck.y), hp1 = pk(ck.z, ck.w);
 #pragma unroll
       for (int j = 0; j < kSub; ++j) {
         const int t = sb * kSub + j;
@@ -351,55 +384,55 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
         hv[j][1] = hp1;
       }
     }
-    const float4 ck = sCk[sb * kT + tid];
-    __syncthreads();   // sE written; the previous sub-block's sPQR / sRed readers are done
+    __syncthreads();   // sDs written; the previous sub-block's sPQR / sRed readers are done
 
-    // walk the sub-block backward
-    f2 dBn[2], dCn[2];   // the later step's dB / dC of this lane (written in step pairs)
+    // walk the sub-block backward; every result stays in registers until the walk ends
+    float oP[kSub], oQ[kSub], oR[kSub];
+    f2 oB[kSub][2], oC[kSub][2];
 #pragma unroll
     for (int j = kSub - 1; j >= 0; --j) {
       const int t = sb * kSub + j;
       const float2 s = sDt[t * kCpb + ci];
-      const float4 e = sE[j * kCpb + ci];
-      const f2 dtp = pk(s.x, s.x), dup = pk(s.y, s.y), dsp = pk(e.x, e.x);
+      const float ds = sDs[j * kCpb + ci];
+      const f2 dtp = pk(s.x, s.x), dup = pk(s.y, s.y), dsp = pk(ds, ds);
       const float4 bv = *reinterpret_cast<const float4*>(sB + t * NT + n0);
       const float4 cv = *reinterpret_cast<const float4*>(sC + t * NT + n0);
       const f2 B2[2] = {pk(bv.x, bv.y), pk(bv.z, bv.w)};
       const f2 C2[2] = {pk(cv.x, cv.y), pk(cv.z, cv.w)};
       const f2 hprev[2] = {j > 0 ? hv[j > 0 ? j - 1 : 0][0] : pk(ck.x, ck.y),
                            j > 0 ? hv[j > 0 ? j - 1 : 0][1] : pk(ck.z, ck.w)};
-      f2 lam[2], g[2], dBv[2], dCv[2];
+      f2 lam[2], g[2];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         lam[q] = fma2(dsp, C2[q], mu[q]);        // total gradient of h_t
         mu[q] = mul2(ev[j][q], lam[q]);          // carried to step t - 1
         g[q] = mul2(mu[q], hprev[q]);            // lambda e h_{t-1}
         dA[q] = fma2(g[q], dtp, dA[q]);
-        dBv[q] = mul2(lam[q], dup);
-        dCv[q] = mul2(dsp, hv[j][q]);
+        oB[j][q] = mul2(lam[q], dup);            // dB: lambda dt u
+        oC[j][q] = mul2(dsp, hv[j][q]);          // dC: ds h_t
       }
       const f2 P = fma2(lam[1], B2[1], mul2(lam[0], B2[0]));
       const f2 Q = fma2(g[1], A2[1], mul2(g[0], A2[0]));
-      float Rs = 0.f;
+      oP[j] = lo(P) + hi(P);
+      oQ[j] = lo(Q) + hi(Q);
+      oR[j] = 0.f;
       if (HAS_Z) {
         const f2 R = fma2(C2[1], hv[j][1], mul2(C2[0], hv[j][0]));
-        Rs = lo(R) + hi(R);
+        oR[j] = lo(R) + hi(R);
       }
-      sPQR[j * kT + tid] = make_float4(lo(P) + hi(P), lo(Q) + hi(Q), Rs, 0.f);
-      if (j & 1) {
-        dBn[0] = dBv[0]; dBn[1] = dBv[1];
-        dCn[0] = dCv[0]; dCn[1] = dCv[1];
-      } else {
-        float* rB = sRed + ci * G::kRedRow + (j / 2) * NT * 2 + n0 * 2;
-        float* rC = rB + kCpb * G::kRedRow;
-        *reinterpret_cast<float2*>(rB + 0) = make_float2(lo(dBv[0]), lo(dBn[0]));
-        *reinterpret_cast<float2*>(rB + 2) = make_float2(hi(dBv[0]), hi(dBn[0]));
-        *reinterpret_cast<float2*>(rB + 4) = make_float2(lo(dBv[1]), lo(dBn[1]));
-        *reinterpret_cast<float2*>(rB + 6) = make_float2(hi(dBv[1]), hi(dBn[1]));
-        *reinterpret_cast<float2*>(rC + 0) = make_float2(lo(dCv[0]), lo(dCn[0]));
-        *reinterpret_cast<float2*>(rC + 2) = make_float2(hi(dCv[0]), hi(dCn[0]));
-        *reinterpret_cast<float2*>(rC + 4) = make_float2(lo(dCv[1]), lo(dCn[1]));
-        *reinterpret_cast<float2*>(rC + 6) = make_float2(hi(dCv[1]), hi(dCn[1]));
+    }
+#pragma unroll
+    for (int j = 0; j < kSub; ++j) sPQR[G::pqr(j, li, ci)] = make_float4(oP[j], oQ[j], oR[j], 0.f);
+#pragma unroll
+    for (int jp = 0; jp < kSub / 2; ++jp) {
+      float* rB = sRed + ci * G::kRedRow + jp * NT * 2 + n0 * 2;
+      float* rC = rB + kCpb * G::kRedRow;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        *reinterpret_cast<float2*>(rB + 4 * q) = make_float2(lo(oB[2 * jp][q]), lo(oB[2 * jp + 1][q]));
+        *reinterpret_cast<float2*>(rB + 4 * q + 2) = make_float2(hi(oB[2 * jp][q]), hi(oB[2 * jp + 1][q]));
+        *reinterpret_cast<float2*>(rC + 4 * q) = make_float2(lo(oC[2 * jp][q]), lo(oC[2 * jp + 1][q]));
+        *reinterpret_cast<float2*>(rC + 4 * q + 2) = make_float2(hi(oC[2 * jp][q]), hi(oC[2 * jp + 1][q]));
       }
     }
     __syncthreads();
@@ -408,44 +441,41 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
 #pragma unroll
     for (int r = 0; r < kSlots; ++r) {
       const int it = tid + r * kT;
-      if (it < kItems) {
-        const int c = it / (kSub / 2), jp = it % (kSub / 2);
-        const int64_t dc = d0 + c;
-        if (dc < a.dim) {
-          const float Dd = Dp ? Dp[dc] : 0.f;
-          float o_du[2], o_dd[2], o_dz[2];
+      const int c = it / (kSub / 2), jp = it % (kSub / 2);
+      const int64_t dc = d0 + c;
+      if (it < kItems && dc < a.dim) {
+        const float Dd = slot_D[r];
+        float o_du[2], o_dd[2], o_dz[2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const int j = 2 * jp + s;
+          float P = 0.f, Q = 0.f, R = 0.f;
+#pragma unroll
+          for (int l = 0; l < kLpc; ++l) {
+            const float4 v = sPQR[G::pqr(j, l, c)];
+            P += v.x; Q += v.y; R += v.z;
+          }
+          const float dt = sDt[(sb * kSub + j) * kCpb + c].x;
+          const float ddt = fmaf(e_u[r][s], P, Q * kLn2);        // u P + sum lambda e h A
+          o_du[s] = fmaf(Dd, e_ds[r][s], dt * P);
+          o_dd[s] = ddt * e_sig[r][s];
+          o_dz[s] = fmaf(Dd, e_u[r][s], R) * e_dzf[r][s];
+          dD_acc[r] = fmaf(e_ds[r][s], e_u[r][s], dD_acc[r]);
+          db_acc[r] += o_dd[s];
+        }
+        const int64_t ix = (b * a.dim + dc) * L + ts + 2 * jp;
+        const int64_t t = ts + 2 * jp;
+        if (a.vec && t + 2 <= t_end) {
+          *reinterpret_cast<float2*>(a.du + ix) = make_float2(o_du[0], o_du[1]);
+          *reinterpret_cast<float2*>(a.ddelta + ix) = make_float2(o_dd[0], o_dd[1]);
+          if (HAS_Z && a.dz) *reinterpret_cast<float2*>(a.dz + ix) = make_float2(o_dz[0], o_dz[1]);
+        } else {
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
-            const int j = 2 * jp + s;
-            float P = 0.f, Q = 0.f, R = 0.f;
-#pragma unroll
-            for (int l = 0; l < kLpc; ++l) {
-              const float4 v = sPQR[j * kT + c * kLpc + l];
-              P += v.x; Q += v.y; R += v.z;
-            }
-            const float4 e = sE[j * kCpb + c];
-            const float dt = sDt[(sb * kSub + j) * kCpb + c].x;
-            const float ddt = fmaf(e.w, P, Q * kLn2);        // u P + sum lambda e h A
-            o_du[s] = fmaf(Dd, e.x, dt * P);
-            o_dd[s] = ddt * e.y;
-            o_dz[s] = fmaf(Dd, e.w, R) * e.z;
-            dD_acc[r] = fmaf(e.x, e.w, dD_acc[r]);
-            db_acc[r] += o_dd[s];
-          }
-          const int64_t ix = (b * a.dim + dc) * L + ts + 2 * jp;
-          const int64_t t = ts + 2 * jp;
-          if (a.vec && t + 2 <= t_end) {
-            *reinterpret_cast<float2*>(a.du + ix) = make_float2(o_du[0], o_du[1]);
-            *reinterpret_cast<float2*>(a.ddelta + ix) = make_float2(o_dd[0], o_dd[1]);
-            if (HAS_Z && a.dz) *reinterpret_cast<float2*>(a.dz + ix) = make_float2(o_dz[0], o_dz[1]);
-          } else {
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-              if (t + s < t_end) {
-                a.du[ix + s] = o_du[s];
-                a.ddelta[ix + s] = o_dd[s];
-                if (HAS_Z && a.dz) a.dz[ix + s] = o_dz[s];
-              }
+            if (t + s < t_end) {
+              a.du[ix + s] = o_du[s];
+              a.ddelta[ix + s] = o_dd[s];
+              if (HAS_Z && a.dz) a.dz[ix + s] = o_dz[s];
             }
           }
         }

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
     iA2[q] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
     float h0 = 0.f, h1 = 0.f;
     const float* H = nullptr;
-    if (MODE == kFixup) H = a.ws_H + (w.bd * a.nchunks + w.k) * N;  // carry-in of this chunk
+    if (MODE == kFixup) H = a.ws_H + (w.k * a.batch * a.dim + w.bd) * N;  // carry-in of this chunk
     else if (a.h0) H = a.h0 + w.bd * N;                             // caller's initial state
     if (H && w.active) {
       if (n0 < N) h0 = H[n0];
@@ -336,8 +336,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
   }
 
   if (!w.active) return;
-  a.ws_S[w.bd * a.nchunks + w.k] = R;
-  float* H = a.ws_H + (w.bd * a.nchunks + w.k) * N;
+  a.ws_S[w.k * a.batch * a.dim + w.bd] = R;
+  float* H = a.ws_H + (w.k * a.batch * a.dim + w.bd) * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
     if (2 * q < N) H[2 * q] = lo(acc[q]);

@@ -15,22 +15,22 @@ __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
   if (i >= a.batch * a.dim * N) return;
   const int64_t n = i % N, bd = i / N, d = bd % a.dim;
   const float A2 = a.A[d * N + n] * kLog2e;
-  const int64_t K = a.nchunks;
-  float* H = a.ws_H + bd * K * N + n;
-  const float* S = a.ws_S + bd * K;
+  const int64_t K = a.nchunks, BD = a.batch * a.dim;
+  float* H = a.ws_H + bd * N + n;            // chunk k at H[k * BD * N]
+  const float* S = a.ws_S + bd;              // chunk k at S[k * BD]
   float c = a.h0 ? a.h0[bd * N + n] : 0.f;  // the state entering chunk 0
   for (int64_t k0 = 0; k0 < K; k0 += 8) {
     float he[8], sk[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const bool ok = k0 + u < K;
-      he[u] = ok ? H[(k0 + u) * N] : 0.f;
-      sk[u] = ok ? S[k0 + u] : 0.f;
+      he[u] = ok ? H[(k0 + u) * BD * N] : 0.f;
+      sk[u] = ok ? S[(k0 + u) * BD] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (k0 + u < K) {
-        H[(k0 + u) * N] = c;
+        H[(k0 + u) * BD * N] = c;
         c = fmaf(ex2(A2 * sk[u]), c, he[u]);
       }
     }

@@ -23,8 +23,8 @@ struct ScanArgs {
   float* y;
   float* last_state;
   const float* h0;   // (batch, dim, N) initial state, or null for zeros
-  float* ws_S;       // (batch, dim, nchunks): sum of dt over each chunk
-  float* ws_H;       // (batch, dim, nchunks, N): chunk end state, then carry-in
+  float* ws_S;       // (nchunks, batch, dim): sum of dt over each chunk
+  float* ws_H;       // (nchunks, batch, dim, N): chunk end state, then carry-in
   int64_t batch, dim, dstate, seqlen, chunk_len, nchunks;
   int ctiles;        // channel tiles (blocks) per (b, chunk)
   int softplus;
@@ -34,7 +34,8 @@ struct ScanArgs {
   int zoh;           // 1: zero-order-hold input weight (exp(dt A) - 1) / A instead of dt
 };
 
-// Backward pass.  Chunks of kBwdChunk steps; the workspace holds, per (b, d, chunk k):
+// Backward pass.  Chunks of kBwdChunk steps; the workspace holds, per (chunk k, b, d),
+// chunk-major like the forward's:
 //   ws_S[k]    sum of dt over the chunk (written by the forward local pass)
 //   ws_H[k][n] the state entering chunk k (forward local pass, then the carry)
 //   ws_G[k][n] the chunk's adjoint sum, then mu_k = exp(A dt_{t1}) lambda_{t1}: the
