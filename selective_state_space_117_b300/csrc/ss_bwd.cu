@@ -218,9 +218,9 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   extern __shared__ __align__(16) float smem[];
   float* sB = smem;
   float* sC = sB + kBwdChunk * NT;
-  float2* sDt = reinterpret_cast<float2*>(sC + kBwdChunk * NT);          // [t][ci]
+  float2* sDt = reinterpret_cast<float2*>(sC + kBwdChunk * NT);          // [t][ci]: (dt, du)
   float4* sCk = reinterpret_cast<float4*>(sDt + kBwdChunk * kCpb);       // [sb][tid]
-  float* sDs = reinterpret_cast<float*>(sCk + kNsub * kT);                // [j][ci]
+  float* sDs = reinterpret_cast<float*>(sCk + kNsub * kT);                // [j][ci]: ds
   float4* sPQR = reinterpret_cast<float4*>(sDs + kSub * kCpb);            // G::pqr(j, l, c)
   float* sRed = reinterpret_cast<float*>(sPQR + kSub * kT);               // [q][ci][jp][n][2]
 
@@ -234,30 +234,60 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   const int64_t L = a.seqlen, t0 = k * kBwdChunk, t_end = min(L, t0 + kBwdChunk);
   const int64_t bc_row = b * N * L;
 
-  // ---- prologue: B and C of the chunk; dt and du of every (channel, step)
-  stage_bc<NT, BF>(sB, a.B, bc_row, N, L, t0, t_end, a.vec_bc, tid, kT);
-  stage_bc<NT, BF>(sC, a.C, bc_row, N, L, t0, t_end, a.vec_bc, tid, kT);
-  for (int e = tid; e < kCpb * (kBwdChunk / 8); e += kT) {
-    const int c = e / (kBwdChunk / 8), g = e % (kBwdChunk / 8);
-    const int64_t dc = d0 + c, t = t0 + 8 * g;
-    float xd[8], uv[8];
-    if (dc < a.dim) {
-      const int64_t row = (b * a.dim + dc) * L;
-      load_group<BF>(a.delta, row + t, t, t_end, a.vec, xd);
-      load_group<BF>(a.u, row + t, t, t_end, a.vec, uv);
-    }
-    const float bias = (dc < a.dim && a.delta_bias) ? a.delta_bias[dc] : 0.f;
+  // ---- prologue: B and C of the chunk, dt and du of every (channel, step), this
+  // lane's A, entering state and carried gradient.  All of its global loads are
+  // issued (read-only path) before the first shared-memory store, so the block
+  // waits for one round trip.
+  constexpr int kG = kBwdChunk / 8;                  // 8-step groups per chunk
+  constexpr int kBcSlots = (NT * kG + kT - 1) / kT;  // (state row, group) items of B and of C
+  constexpr int kDtItems = kCpb * kG;                // (channel, group) items of delta and u
+  constexpr int kDtRound = kDtItems / kT < 2 ? (kDtItems + kT - 1) / kT : 2;
+  float rb8[kBcSlots][8], rc8[kBcSlots][8], rx8[kDtRound][8], ru8[kDtRound][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float dt = 0.f, du = 0.f;
-      if (dc < a.dim && t + j < t_end) {
-        const float x = xd[j] + bias;
-        dt = a.softplus ? softplus(x) : x;
-        du = dt * uv[j];
-      }
-      sDt[(8 * g + j) * kCpb + c] = make_float2(dt, du);
+  for (int r = 0; r < kBcSlots; ++r) {
+    const int e = tid + r * kT, n = e / kG, g = e % kG;
+    if (e < NT * kG && n < N) {
+      const int64_t off = bc_row + (int64_t)n * L + t0 + 8 * g;
+      load_group<BF>(a.B, off, t0 + 8 * g, t_end, a.vec_bc, rb8[r]);
+      load_group<BF>(a.C, off, t0 + 8 * g, t_end, a.vec_bc, rc8[r]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) rb8[r][j] = rc8[r][j] = 0.f;
     }
   }
+  auto load_dt = [&](int round) {
+#pragma unroll
+    for (int r = 0; r < kDtRound; ++r) {
+      const int e = tid + (round * kDtRound + r) * kT, c = e / kG, g = e % kG;
+      const int64_t dc = d0 + c, t = t0 + 8 * g;
+      if (e < kDtItems && dc < a.dim) {
+        const int64_t row = (b * a.dim + dc) * L;
+        load_group<BF>(a.delta, row + t, t, t_end, a.vec, rx8[r]);
+        load_group<BF>(a.u, row + t, t, t_end, a.vec, ru8[r]);
+      }
+    }
+  };
+  auto store_dt = [&](int round) {
+#pragma unroll
+    for (int r = 0; r < kDtRound; ++r) {
+      const int e = tid + (round * kDtRound + r) * kT, c = e / kG, g = e % kG;
+      const int64_t dc = d0 + c, t = t0 + 8 * g;
+      if (e < kDtItems) {
+        const float bias = (dc < a.dim && a.delta_bias) ? __ldg(a.delta_bias + dc) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float dt = 0.f, du = 0.f;
+          if (dc < a.dim && t + j < t_end) {
+            const float x = rx8[r][j] + bias;
+            dt = a.softplus ? softplus(x) : x;
+            du = dt * ru8[r][j];
+          }
+          sDt[(8 * g + j) * kCpb + c] = make_float2(dt, du);
+        }
+      }
+    }
+  };
+  load_dt(0);
 
   // This lane's states n0..n0+3 as pairs (q = 0: n0, n0+1; q = 1: n0+2, n0+3).
   f2 A2[2], h[2], mu[2], dA[2];
@@ -270,9 +300,9 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
       for (int s = 0; s < 2; ++s) {
         const int n = n0 + 2 * q + s;
         const bool ok = active && n < N;
-        av[s] = ok ? a.A[d * N + n] * kLog2e : 0.f;
-        hv[s] = ok ? a.ws_H[ws + n] : 0.f;
-        mv[s] = ok ? a.ws_G[ws + n] : 0.f;
+        av[s] = ok ? __ldg(a.A + d * N + n) * kLog2e : 0.f;
+        hv[s] = ok ? __ldg(a.ws_H + ws + n) : 0.f;
+        mv[s] = ok ? __ldg(a.ws_G + ws + n) : 0.f;
       }
       A2[q] = pk(av[0], av[1]);
       h[q] = pk(hv[0], hv[1]);
@@ -308,6 +338,24 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
     }
   };
   fetch(kNsub - 1);
+
+  // the prologue's shared-memory stores
+#pragma unroll
+  for (int r = 0; r < kBcSlots; ++r) {
+    const int e = tid + r * kT, n = e / kG, g = e % kG;
+    if (e < NT * kG) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sB[(8 * g + j) * NT + n] = rb8[r][j];
+        sC[(8 * g + j) * NT + n] = rc8[r][j];
+      }
+    }
+  }
+  store_dt(0);
+  for (int round = 1; round * kDtRound * kT < kDtItems; ++round) {
+    load_dt(round);
+    store_dt(round);
+  }
   __syncthreads();
 
   // ---- forward sweep over the chunk: a checkpoint before every sub-block
