@@ -51,10 +51,10 @@ EX2_PER_CLK_PER_SM = 32          # MUFU.EX2 issue rate of sm_103 (31.85/clk/SM m
 # to the kernel sources with the hash below; after any change to those sources
 # they no longer describe the running kernels and the bench reports null.
 TRAFFIC = {
-    "sources": "acb3f189cad1e7d1",
-    "local": 1361127000,     # local_tma_kernel: 1.347880 GB read + 0.013247 GB written
-    "carry": 11479000,       # carry_kernel: 0.011479 GB read (writes stay in L2)
-    "fixup": 3348035000,     # scan_tma_kernel (fix-up): 2.035321 GB read + 1.312714 GB written
+    "sources": "ce78e1fe1b3bb9f0",
+    "local": 1360371000,     # local_tma_kernel: 1.347037 GB read + 0.013334 GB written
+    "carry": 11482000,       # carry_kernel: 0.011482 GB read (writes stay in L2)
+    "fixup": 3344774000,     # scan_tma_kernel (fix-up): 2.033431 GB read + 1.311343 GB written
 }
 
 
@@ -300,6 +300,10 @@ def run_ours(args):
     pk = peaks()
     p = I.workload(WORKLOAD, device="cuda", gen_device="cuda", dim=args.dim, seqlen=args.seqlen)
     Bt, Dm, N, L = p.batch, p.dim, p.dstate, p.seqlen
+    if args.bwd_only:                  # the backward leg alone (for profiling it); one JSON line
+        if rank == 0:
+            print(json.dumps({"bwd": bench_bwd(ss, I, torch, p, pk, None, reps=max(1, args.steps))}), flush=True)
+        return 0
     elems, byts, exps = workload_counts(Bt, Dm, N, L)
     y = torch.empty((Bt, Dm, L), dtype=torch.float32, device="cuda")
     hl = torch.empty((Bt, Dm, N), dtype=torch.float32, device="cuda")
@@ -354,6 +358,7 @@ def run_ours(args):
     if not args.no_decode:
         side["zoh"] = bench_zoh_step(ss, torch, p, kw, elems)
         side["fwd_layer"] = bench_fwd_layer(ss, I, torch, pk)
+        side["bwd"] = bench_bwd(ss, I, torch, p, pk, ms)
 
     line = {
         "metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": world, "steps": args.steps,
@@ -465,6 +470,54 @@ def bench_zoh_step(ss, torch, p, kw, elems, reps=5):
             "elem_per_s": elems / (ms * 1e-3), "gpu_launches": 3 * reps}
 
 
+def bwd_counts(batch, dim, dstate, seqlen, in_bytes=2):
+    """Algorithmic bytes and exponentials of one backward pass with a gate.
+    bytes: u, delta, z read once (in_bytes each) and dy once (fp32); du, ddelta, dz written
+    once (fp32); B, C read and dB, dC written once per batch row; A, D, delta_bias, dlast read
+    and dA, dD, ddelta_bias, dh0 written once.
+    exps: N decays per element (each needed by both the state and its adjoint), and one each
+    for the step size, its derivative sigmoid(x) and the gate's sigmoid(z)."""
+    elems = batch * dim * seqlen
+    byts = elems * (3 * in_bytes + 4 + 3 * 4) + batch * dstate * seqlen * (2 * in_bytes + 2 * 4) \
+        + dim * dstate * 4 * 2 + dim * 4 * 4 + batch * dim * dstate * 4 * 2
+    exps = elems * (dstate + 3)
+    return elems, byts, exps
+
+
+def bench_bwd(ss, I, torch, p, pk, fwd_ms, reps=5):
+    """ss_scan_bwd on the long-sequence workload: the gradients of sum(dy y) + sum(dlast h_last)
+    for every input (forward local pass and carry at 64-step chunks, adjoint local pass and
+    carry, main pass: five kernels and five memsets per call)."""
+    ct = I.cotangents(seed=103, batch=p.batch, dim=p.dim, dstate=p.dstate, seqlen=p.seqlen, with_h0=False,
+                      device="cuda", gen_device="cuda")
+    ws = torch.empty((ss.bwd_workspace_bytes(p.batch, p.dim, p.dstate, p.seqlen, ss.BF16),), dtype=torch.uint8,
+                     device="cuda")
+
+    def call():
+        return ss.scan_bwd(p.u, p.delta, p.A, p.B, p.C, D=p.D, z=p.z, delta_bias=p.delta_bias, dy=ct.dy,
+                           dlast=ct.dlast, workspace=ws)
+
+    for _ in range(2):
+        g = call()
+    del g
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    elems, byts, exps = bwd_counts(p.batch, p.dim, p.dstate, p.seqlen)
+    roof = roofline_terms(byts, exps, ms, pk)
+    del ct, ws
+    return {"workload": f"{WORKLOAD}: batch={p.batch}, D={p.dim}, N={p.dstate}, L={p.seqlen}, bf16 inputs, gate, "
+                        "fp32 gradients",
+            "entry_point": "ss_scan_bwd", "ms": round(ms, 4), "elem_per_s": elems / (ms * 1e-3),
+            "algorithmic_bytes": byts, "exps": exps, "roofline": roof,
+            "time_vs_forward_step": round(ms / fwd_ms, 2) if fwd_ms else None, "gpu_launches": 5 * reps}
+
+
 def bench_conv(ss, torch, pk, batch=1, dim=5120, seqlen=65536, reps=20):
     """The short convolution in front of the scan (ss_causal_conv1d with SiLU) on the
     long-sequence shape, bf16 in and out: 2 x 2 B of traffic per element."""
@@ -544,6 +597,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dim", type=int, default=5120, help="channels (5120 = the workload; smaller only for profiling)")
     ap.add_argument("--seqlen", type=int, default=65536, help="steps (65536 = the workload; shorter only for profiling)")
+    ap.add_argument("--bwd-only", action="store_true",
+                    help="time only the backward pass (ss_scan_bwd), --steps calls after 2 warm-ups")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
