@@ -32,6 +32,14 @@ namespace {
 constexpr int kSub = 8;                        // steps per sub-block of the main pass
 constexpr int kNsub = kBwdChunk / kSub;
 
+// 4- and 8-byte asynchronous copies global -> shared (L1-allocating).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
 // sigmoid(x) = 1 / (1 + e^-x)
 __device__ __forceinline__ float sigm(float x) { return rcp(1.f + ex2(-x * kLog2e)); }
 
@@ -194,12 +202,16 @@ struct BwdGeom {
   // dB/dC staging: [q][channel][step pair][n][2], channel rows padded by 2 floats
   // so that the 16 lanes of a 64-bit store phase hit distinct banks.
   static constexpr int kRedRow = 8 * NT + 2;
+  // Items of a sub-block: (channel, step pair); kItemSlots = their count rounded up to the block.
+  static constexpr int kItems = kCpb * (kSub / 2);
+  static constexpr int kItemSlots = (kItems + kThreads - 1) / kThreads * kThreads;
   static constexpr int kFloats = 2 * kBwdChunk * NT          // sB, sC
                                  + 2 * kBwdChunk * kCpb      // sDt (dt, du)
                                  + 4 * kNsub * kThreads      // sCk checkpoints
                                  + kSub * kCpb               // sDs: ds = dy silu(z)
                                  + 4 * kSub * kThreads       // sPQR partial sums
-                                 + 2 * kCpb * kRedRow;       // sRed
+                                 + 2 * kCpb * kRedRow        // sRed
+                                 + 4 * 2 * kItemSlots;       // sRaw: 4 fields x 8 bytes per item
   static constexpr size_t kBytes = (size_t)kFloats * 4;
   // Slot of lane l's partial sums for step j of channel c in sPQR ([j][l][c] in
   // 16-byte units): the channel index is XOR-swizzled with the lane and the step
@@ -223,6 +235,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   float* sDs = reinterpret_cast<float*>(sCk + kNsub * kT);                // [j][ci]: ds
   float4* sPQR = reinterpret_cast<float4*>(sDs + kSub * kCpb);            // G::pqr(j, l, c)
   float* sRed = reinterpret_cast<float*>(sPQR + kSub * kT);               // [q][ci][jp][n][2]
+  uint2* sRaw = reinterpret_cast<uint2*>(sRed + 2 * kCpb * G::kRedRow);    // [field][item]
 
   const int tid = threadIdx.x;
   const int ct = blockIdx.x % a.ctiles;
@@ -317,25 +330,59 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   constexpr int kItems = kCpb * (kSub / 2);
   constexpr int kSlots = (kItems + kT - 1) / kT;
   const float* Dp = a.D;
-  float rdy[kSlots][2], ru[kSlots][2], rx[kSlots][2], rz[kSlots][2];
+  // The raw per-step inputs of the items (dy, u, delta, z for two steps) are copied
+  // into shared memory one sub-block ahead, by cp.async where the pair is whole and
+  // aligned; each thread later reads back only the slots it filled, before it
+  // refills them (one buffer suffices).  A slot holds the pair as two fp32 (dy, and
+  // u/delta/z for fp32 inputs) or one bf16x2 word.
+  auto slot = [&](int field, int r) -> uint2* { return sRaw + field * G::kItemSlots + r * kT + tid; };
+  // Each item slot's row offset at the chunk start (fixed for the whole block).
+  int64_t slot_ix0[kSlots];
+#pragma unroll
+  for (int r = 0; r < kSlots; ++r) {
+    const int it = tid + r * kT;
+    const int64_t dc = d0 + it / (kSub / 2);
+    slot_ix0[r] = (b * a.dim + (dc < a.dim ? dc : 0)) * L + t0 + 2 * (it % (kSub / 2));
+  }
   auto fetch = [&](int sb) {
 #pragma unroll
     for (int r = 0; r < kSlots; ++r) {
       const int it = tid + r * kT;
       const int c = it / (kSub / 2), jp = it % (kSub / 2);
       const int64_t dc = d0 + c, t = t0 + sb * kSub + 2 * jp;
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        rdy[r][s] = ru[r][s] = rx[r][s] = rz[r][s] = 0.f;
-        if (it < kItems && dc < a.dim && t + s < t_end) {
-          const int64_t ix = (b * a.dim + dc) * L + t + s;
-          rdy[r][s] = __ldg(a.dy + ix);
-          ru[r][s] = In<BF>::one(a.u, ix);
-          rx[r][s] = In<BF>::one(a.delta, ix);
-          if (HAS_Z) rz[r][s] = In<BF>::one(a.z, ix);
+      const int64_t ix = slot_ix0[r] + sb * kSub;
+      if (a.vec && it < kItems && dc < a.dim && t + 2 <= t_end) {
+        cp_async8(slot(0, r), a.dy + ix);
+        if (BF) {
+          cp_async4(slot(1, r), In<BF>::addr(a.u, ix));
+          cp_async4(slot(2, r), In<BF>::addr(a.delta, ix));
+          if (HAS_Z) cp_async4(slot(3, r), In<BF>::addr(a.z, ix));
+        } else {
+          cp_async8(slot(1, r), In<BF>::addr(a.u, ix));
+          cp_async8(slot(2, r), In<BF>::addr(a.delta, ix));
+          if (HAS_Z) cp_async8(slot(3, r), In<BF>::addr(a.z, ix));
         }
+      } else {
+        float v[4][2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const bool ok = it < kItems && dc < a.dim && t + s < t_end;
+          v[0][s] = ok ? __ldg(a.dy + ix + s) : 0.f;
+          v[1][s] = ok ? In<BF>::one(a.u, ix + s) : 0.f;
+          v[2][s] = ok ? In<BF>::one(a.delta, ix + s) : 0.f;
+          v[3][s] = (ok && HAS_Z) ? In<BF>::one(a.z, ix + s) : 0.f;
+        }
+        *slot(0, r) = make_uint2(__float_as_uint(v[0][0]), __float_as_uint(v[0][1]));
+#pragma unroll
+        for (int f = 1; f < 4; ++f)
+          *slot(f, r) = BF ? make_uint2((__float_as_uint(v[f][0]) >> 16) | (__float_as_uint(v[f][1]) & 0xffff0000u), 0u)
+                                : make_uint2(__float_as_uint(v[f][0]), __float_as_uint(v[f][1]));
       }
     }
+    cp_async_commit();
+  };
+  auto pair_of = [&](uint2 w, bool wide) -> f2 {
+    return wide ? pk(__uint_as_float(w.x), __uint_as_float(w.y)) : bf16x2(w.x);
   };
   fetch(kNsub - 1);
 
@@ -383,12 +430,36 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
     slot_D[r] = (ok && Dp) ? Dp[dc] : 0.f;
   }
 
+  // dB/dC reduction outputs of this thread: (q, n, step pair), fixed for the block.
+  constexpr int kRedOut = 2 * (kSub / 2) * NT;
+  constexpr int kRedSlots = (kRedOut + kT - 1) / kT;
+  int red_src[kRedSlots];
+  float* red_dst[kRedSlots];
+#pragma unroll
+  for (int r = 0; r < kRedSlots; ++r) {
+    const int o = tid + r * kT;
+    const int n = o % NT, jp = (o / NT) % (kSub / 2), q = (o / (NT * (kSub / 2))) & 1;
+    red_src[r] = q * kCpb * G::kRedRow + jp * NT * 2 + n * 2;
+    red_dst[r] = (q ? a.dC : a.dB) + bc_row + (int64_t)(n < N ? n : 0) * L + t0 + 2 * jp;
+  }
+
   // ---- sub-blocks, last first
   for (int sb = kNsub - 1; sb >= 0; --sb) {
     const int64_t ts = t0 + sb * kSub;
     // per-(channel, step) scalars of the items: ds for every lane (shared memory),
     // sigmoid(x), the dz factor and u kept by the item's thread for its epilogue
     float e_ds[kSlots][2], e_sig[kSlots][2], e_dzf[kSlots][2], e_u[kSlots][2];
+    cp_async_wait<0>();
+    float rdy[kSlots][2], ru[kSlots][2], rx[kSlots][2], rz[kSlots][2];
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r) {
+      const f2 dy2 = pair_of(*slot(0, r), true), u2 = pair_of(*slot(1, r), !BF),
+               x2 = pair_of(*slot(2, r), !BF), z2 = HAS_Z ? pair_of(*slot(3, r), !BF) : pk(0.f, 0.f);
+      rdy[r][0] = lo(dy2); rdy[r][1] = hi(dy2);
+      ru[r][0] = lo(u2); ru[r][1] = hi(u2);
+      rx[r][0] = lo(x2); rx[r][1] = hi(x2);
+      rz[r][0] = lo(z2); rz[r][1] = hi(z2);
+    }
 #pragma unroll
     for (int r = 0; r < kSlots; ++r) {
       const int it = tid + r * kT;
@@ -511,7 +582,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
           dD_acc[r] = fmaf(e_ds[r][s], e_u[r][s], dD_acc[r]);
           db_acc[r] += o_dd[s];
         }
-        const int64_t ix = (b * a.dim + dc) * L + ts + 2 * jp;
+        const int64_t ix = slot_ix0[r] + sb * kSub;
         const int64_t t = ts + 2 * jp;
         if (a.vec && t + 2 <= t_end) {
           *reinterpret_cast<float2*>(a.du + ix) = make_float2(o_du[0], o_du[1]);
@@ -530,15 +601,17 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
       }
     }
     // dB, dC: sums over the block's channels, one atomic add per (b, n, step pair)
-    for (int o = tid; o < 2 * (kSub / 2) * NT; o += kT) {
-      const int n = o % NT, jp = (o / NT) % (kSub / 2), q = o / (NT * (kSub / 2));
+#pragma unroll
+    for (int r = 0; r < kRedSlots; ++r) {
+      const int o = tid + r * kT;
+      const int n = o % NT, jp = (o / NT) % (kSub / 2);
       const int64_t t = ts + 2 * jp;
-      if (n < N && t < t_end) {
-        const float* src = sRed + q * kCpb * G::kRedRow + jp * NT * 2 + n * 2;
+      if (o < kRedOut && n < N && t < t_end) {
+        const float* src = sRed + red_src[r];
         f2 acc = pk(0.f, 0.f);
 #pragma unroll 8
         for (int c = 0; c < kCpb; ++c) acc = add2(acc, *reinterpret_cast<const f2*>(src + c * G::kRedRow));
-        float* dst = (q ? a.dC : a.dB) + bc_row + (int64_t)n * L + t;
+        float* dst = red_dst[r] + sb * kSub;
         if (a.vec && t + 2 <= t_end) {            // 8-byte aligned: dB, dC checked, L % 8 == 0, t even
           atomicAdd(reinterpret_cast<float2*>(dst), make_float2(lo(acc), hi(acc)));
         } else {
