@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   float rb8[kBcSlots][8], rc8[kBcSlots][8], rx8[kDtRound][8], ru8[kDtRound][8];
 #pragma unroll
   for (int r = 0; r < kBcSlots; ++r) {
-    const int e = tid + r * kT, n = e / kG, g = e % kG;
+    const int e = tid + r * kT, n = e % NT, g = e / NT;     // consecutive lanes: consecutive states
     if (e < NT * kG && n < N) {
       const int64_t off = bc_row + (int64_t)n * L + t0 + 8 * g;
       load_group<BF>(a.B, off, t0 + 8 * g, t_end, a.vec_bc, rb8[r]);
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   auto load_dt = [&](int round) {
 #pragma unroll
     for (int r = 0; r < kDtRound; ++r) {
-      const int e = tid + (round * kDtRound + r) * kT, c = e / kG, g = e % kG;
+      const int e = tid + (round * kDtRound + r) * kT, c = e % kCpb, g = e / kCpb;  // consecutive lanes: channels
       const int64_t dc = d0 + c, t = t0 + 8 * g;
       if (e < kDtItems && dc < a.dim) {
         const int64_t row = (b * a.dim + dc) * L;
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   auto store_dt = [&](int round) {
 #pragma unroll
     for (int r = 0; r < kDtRound; ++r) {
-      const int e = tid + (round * kDtRound + r) * kT, c = e / kG, g = e % kG;
+      const int e = tid + (round * kDtRound + r) * kT, c = e % kCpb, g = e / kCpb;
       const int64_t dc = d0 + c, t = t0 + 8 * g;
       if (e < kDtItems) {
         const float bias = (dc < a.dim && a.delta_bias) ? __ldg(a.delta_bias + dc) : 0.f;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   // the prologue's shared-memory stores
 #pragma unroll
   for (int r = 0; r < kBcSlots; ++r) {
-    const int e = tid + r * kT, n = e / kG, g = e % kG;
+    const int e = tid + r * kT, n = e % NT, g = e / NT;
     if (e < NT * kG) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
