@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(kCh) bwd_local_kernel(const BwdArgs a) {
 // ---------------------------------------------------------------------------- adjoint carry
 
 // One thread per (b, d, n): the chunks' adjoint sums G_k become mu_k, last chunk first;
-// the value after chunk 0 is dh0.  Loads run 8 chunks ahead of the dependent chain.
+// the value after chunk 0 is dh0.  Loads run in batches of 8 chunks, the next batch
+// requested before the current one is consumed.
 __global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t N = a.dstate;
@@ -171,20 +172,29 @@ __global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a) {
   float* G = a.ws_G + bd * N + n;            // chunk k at G[k * BD * N]
   const float* S = a.ws_S + bd;              // chunk k at S[k * BD]
   float mu = a.dlast ? a.dlast[bd * N + n] : 0.f;
-  for (int64_t k0 = K - 1; k0 >= 0; k0 -= 8) {
-    float gv[8], sv[8];
+  float gv[8], sv[8], gn[8] = {}, sn[8] = {};
+  auto load = [&](int64_t k0, float (&g)[8], float (&sg)[8]) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const bool ok = k0 - u >= 0;
-      gv[u] = ok ? G[(k0 - u) * BD * N] : 0.f;
-      sv[u] = ok ? S[(k0 - u) * BD] : 0.f;
+      g[u] = ok ? G[(k0 - u) * BD * N] : 0.f;
+      sg[u] = ok ? S[(k0 - u) * BD] : 0.f;
     }
+  };
+  load(K - 1, gv, sv);
+  for (int64_t k0 = K - 1; k0 >= 0; k0 -= 8) {
+    if (k0 - 8 >= 0) load(k0 - 8, gn, sn);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (k0 - u >= 0) {
         G[(k0 - u) * BD * N] = mu;
         mu = fmaf(ex2(A2 * sv[u]), mu, gv[u]);
       }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      gv[u] = gn[u];
+      sv[u] = sn[u];
     }
   }
   if (a.dh0) a.dh0[bd * N + n] = mu;

@@ -8,7 +8,8 @@ namespace ssk {
 // (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2), one thread per (b, d, n):
 //   carry_0 = h0 (zeros without one),   carry_{k+1} = P_k * carry_k + H_k.
 // Overwrites the workspace's H_k with carry_k (the true state entering chunk k) and writes the
-// final state after the last chunk.  Loads are issued 8 chunks ahead of the dependent chain.
+// final state after the last chunk.  The dependent chain is latency-bound: loads run in
+// batches of 8 chunks, and the next batch is requested before the current one is consumed.
 __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t N = a.dstate;
@@ -19,20 +20,29 @@ __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
   float* H = a.ws_H + bd * N + n;            // chunk k at H[k * BD * N]
   const float* S = a.ws_S + bd;              // chunk k at S[k * BD]
   float c = a.h0 ? a.h0[bd * N + n] : 0.f;  // the state entering chunk 0
-  for (int64_t k0 = 0; k0 < K; k0 += 8) {
-    float he[8], sk[8];
+  float he[8], sk[8], hn[8] = {}, sn[8] = {};
+  auto load = [&](int64_t k0, float (&hv)[8], float (&sv)[8]) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const bool ok = k0 + u < K;
-      he[u] = ok ? H[(k0 + u) * BD * N] : 0.f;
-      sk[u] = ok ? S[(k0 + u) * BD] : 0.f;
+      hv[u] = ok ? H[(k0 + u) * BD * N] : 0.f;
+      sv[u] = ok ? S[(k0 + u) * BD] : 0.f;
     }
+  };
+  load(0, he, sk);
+  for (int64_t k0 = 0; k0 < K; k0 += 8) {
+    if (k0 + 8 < K) load(k0 + 8, hn, sn);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (k0 + u < K) {
         H[(k0 + u) * BD * N] = c;
         c = fmaf(ex2(A2 * sk[u]), c, he[u]);
       }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      he[u] = hn[u];
+      sk[u] = sn[u];
     }
   }
   if (a.last_state) a.last_state[bd * N + n] = c;
