@@ -236,7 +236,7 @@ int ss_causal_conv1d(const ss_dims* dims, const void* x, const float* weight, co
  *     Loss = sum_{b,d,t} dy[b,d,t] y[b,d,t] + sum_{b,d,n} dlast_state[b,d,n] last_state[b,d,n]
  *
  * where (y, last_state) is the forward scan of ss_scan_fwd_h0 on the same
- * inputs (Euler input weight; dims->flags must be 0).  The forward pass keeps
+ * inputs, with the input weight dims->flags selects (Euler, or SS_FLAG_ZOH).  The forward pass keeps
  * no states: this call recomputes them ("Recomputation" in "Mamba: Linear-Time
  * Sequence Modeling with Selective State Spaces", azimuth.plus: recompute the
  * intermediate states in the backward pass instead of storing them; likewise

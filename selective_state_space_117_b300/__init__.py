@@ -232,7 +232,7 @@ def bwd_workspace_bytes(batch, dim, dstate, seqlen, dtype=F32) -> int:
 
 
 def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, dy, dlast=None, h0=None,
-             want_dD=True, want_dbias=True, want_dh0=None, workspace=None, stream=None):
+             want_dD=True, want_dbias=True, want_dh0=None, zoh=False, workspace=None, stream=None):
     """Backward pass of ``scan_fwd`` (ss_scan_bwd): the gradients of
     sum(dy * y) + sum(dlast * last_state) for the forward scan on the same inputs.
 
@@ -241,8 +241,10 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, 
     without z), dA (dim, N), dB, dC (batch, N, L), dD and ddelta_bias (dim,)
     (None unless ``want_dD`` / ``want_dbias``), dh0 (batch, dim, N) (computed
     when ``want_dh0``, by default when h0 is given).  ``workspace`` is an optional
-    uint8 CUDA tensor of at least ``bwd_workspace_bytes`` bytes."""
+    uint8 CUDA tensor of at least ``bwd_workspace_bytes`` bytes.  ``zoh``: the
+    forward scan used the zero-order-hold input weight (SS_FLAG_ZOH)."""
     dims, _ = _scan_common(u, delta, A, B, C, D, z, delta_bias, dy, None)
+    dims.flags = FLAG_ZOH if zoh else 0
     batch, dim, N, L = dims.batch, dims.dim, dims.dstate, dims.seqlen
     dev = u.device
     _need(dlast, "dlast", (batch, dim, N), torch.float32, dev)

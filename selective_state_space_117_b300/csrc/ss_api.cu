@@ -312,7 +312,7 @@ int ss_scan_bwd(const ss_dims* dims, const float* h0, const void* u, const void*
   const int st = check_scan(dims, u, delta, A, B, C, D, z, delta_bias, dy, nullptr);
   if (st != SS_OK) return st;
   const ss_dims& d = *dims;
-  if (d.flags != 0) return SS_EINVAL;                       // Euler input weight only
+
   const bool rows = d.batch > 0 && d.dim > 0 && d.seqlen > 0;
   if (rows && (!du || !ddelta)) return SS_EINVAL;
   if (rows && d.dstate > 0 && (!dB || !dC)) return SS_EINVAL;
@@ -376,6 +376,7 @@ int ss_scan_bwd(const ss_dims* dims, const float* h0, const void* u, const void*
   a.ws_G = reinterpret_cast<float*>(ws + s_bytes + h_bytes);
   a.batch = d.batch; a.dim = d.dim; a.dstate = d.dstate; a.seqlen = d.seqlen; a.nchunks = K;
   a.softplus = softplus_flag ? 1 : 0;
+  a.zoh = (d.flags & SS_FLAG_ZOH) ? 1 : 0;
   const size_t es = in_size(d.in_dtype);
   const bool rows16 = (d.seqlen * (int64_t)es) % 16 == 0 && (d.seqlen * 4) % 16 == 0;
   a.vec = (rows16 && aligned(u, 16) && aligned(delta, 16) && aligned(z, 16) && aligned(dy, 16) && aligned(du, 16) &&

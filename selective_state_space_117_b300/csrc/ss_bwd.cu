@@ -1,4 +1,4 @@
-// Backward pass of the selective scan (Euler input weight): the gradients of
+// Backward pass of the selective scan (Euler or zero-order-hold input weight): the gradients of
 //     Loss = sum dy * y + sum dlast * h_last
 // with respect to u, delta, A, B, C, D, z, delta_bias and h0.
 //
@@ -38,6 +38,22 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async8(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+// d/dA of the zero-order-hold weight w = (exp(dt A) - 1) / A, for a state pair, given
+// arg = dt A log2(e), e = exp(dt A), w and inv_a = 1/A: (dt e - w) / A.  Where |dt A| < 1/10
+// that difference cancels and the derivative is dt^2 (1/2 + y/3 + y^2/8 + y^3/30), y = dt A
+// (the derivative of the series of (e^y - 1)/y; truncation below 2e-6 relative); above,
+// the closed form loses at most about 2 x 2^-22 / 0.1 relative.
+__device__ __forceinline__ f2 hold_dA2(f2 arg, f2 e, f2 dtp, f2 w, f2 inv_a) {
+  const f2 y = mul2(arg, splat(kLn2));
+  f2 p = fma2(y, splat(1.f / 30.f), splat(1.f / 8.f));
+  p = fma2(p, y, splat(1.f / 3.f));
+  p = fma2(p, y, splat(0.5f));
+  const f2 small = mul2(p, mul2(dtp, dtp));
+  const f2 large = mul2(fma2(dtp, e, mul2(w, splat(-1.f))), inv_a);
+  return pk(fabsf(lo(y)) < kHoldSeriesBelow ? lo(small) : lo(large),
+            fabsf(hi(y)) < kHoldSeriesBelow ? hi(small) : hi(large));
 }
 
 // sigmoid(x) = 1 / (1 + e^-x)
@@ -232,15 +248,18 @@ struct BwdGeom {
   }
 };
 
-// Per-lane work of the main pass (NT states per channel, BF input dtype, HAS_Z gate).
-template <int NT, bool BF, bool HAS_Z>
+// Per-lane work of the main pass (NT states per channel, BF input dtype, HAS_Z gate, ZOH
+// zero-order-hold input weight).  With the Euler weight sDt holds (dt, dt u); with ZOH
+// (dt, u), and the weight w = (exp(dt A) - 1)/A and its A-derivative are recomputed
+// per state and step from the decay.
+template <int NT, bool BF, bool HAS_Z, bool ZOH>
 __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const BwdArgs a) {
   using G = BwdGeom<NT>;
   constexpr int kLpc = G::kLpc, kCpb = G::kCpb, kT = G::kThreads;
   extern __shared__ __align__(16) float smem[];
   float* sB = smem;
   float* sC = sB + kBwdChunk * NT;
-  float2* sDt = reinterpret_cast<float2*>(sC + kBwdChunk * NT);          // [t][ci]: (dt, du)
+  float2* sDt = reinterpret_cast<float2*>(sC + kBwdChunk * NT);          // [t][ci]: (dt, du) or (dt, u)
   float4* sCk = reinterpret_cast<float4*>(sDt + kBwdChunk * kCpb);       // [sb][tid]
   float* sDs = reinterpret_cast<float*>(sCk + kNsub * kT);                // [j][ci]: ds
   float4* sPQR = reinterpret_cast<float4*>(sDs + kSub * kCpb);            // G::pqr(j, l, c)
@@ -303,7 +322,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
           if (dc < a.dim && t + j < t_end) {
             const float x = rx8[r][j] + bias;
             dt = a.softplus ? softplus(x) : x;
-            du = dt * ru8[r][j];
+            du = ZOH ? ru8[r][j] : dt * ru8[r][j];
           }
           sDt[(8 * g + j) * kCpb + c] = make_float2(dt, du);
         }
@@ -313,7 +332,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   load_dt(0);
 
   // This lane's states n0..n0+3 as pairs (q = 0: n0, n0+1; q = 1: n0+2, n0+3).
-  f2 A2[2], h[2], mu[2], dA[2];
+  f2 A2[2], iA2[2], h[2], mu[2], dA[2];
   {
     const int64_t ws = (k * a.batch * a.dim + b * a.dim + (active ? d : 0)) * N;
 #pragma unroll
@@ -323,11 +342,12 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
       for (int s = 0; s < 2; ++s) {
         const int n = n0 + 2 * q + s;
         const bool ok = active && n < N;
-        av[s] = ok ? __ldg(a.A + d * N + n) * kLog2e : 0.f;
+        av[s] = ok ? __ldg(a.A + d * N + n) : 0.f;
         hv[s] = ok ? __ldg(a.ws_H + ws + n) : 0.f;
         mv[s] = ok ? __ldg(a.ws_G + ws + n) : 0.f;
       }
-      A2[q] = pk(av[0], av[1]);
+      A2[q] = pk(av[0] * kLog2e, av[1] * kLog2e);
+      iA2[q] = pk(av[0] != 0.f ? 1.f / av[0] : 0.f, av[1] != 0.f ? 1.f / av[1] : 0.f);
       h[q] = pk(hv[0], hv[1]);
       mu[q] = pk(mv[0], mv[1]);
       dA[q] = pk(0.f, 0.f);
@@ -424,8 +444,13 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
       const float2 s = sDt[t * kCpb + ci];
       const f2 dtp = pk(s.x, s.x), dup = pk(s.y, s.y);
       const float4 bv = *reinterpret_cast<const float4*>(sB + t * NT + n0);
-      h[0] = fma2(ex2x2(mul2(dtp, A2[0])), h[0], mul2(dup, pk(bv.x, bv.y)));
-      h[1] = fma2(ex2x2(mul2(dtp, A2[1])), h[1], mul2(dup, pk(bv.z, bv.w)));
+      const f2 Bq[2] = {pk(bv.x, bv.y), pk(bv.z, bv.w)};
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const f2 arg = mul2(dtp, A2[q]), e = ex2x2(arg);
+        // dup is dt u (Euler) or u (ZOH, times the hold weight)
+        h[q] = fma2(e, h[q], ZOH ? mul2(hold2(arg, e, dtp, iA2[q]), mul2(dup, Bq[q])) : mul2(dup, Bq[q]));
+      }
     }
   }
 
@@ -505,10 +530,12 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
         const float2 s = sDt[t * kCpb + ci];
         const f2 dtp = pk(s.x, s.x), dup = pk(s.y, s.y);
         const float4 bv = *reinterpret_cast<const float4*>(sB + t * NT + n0);
-        ev[j][0] = ex2x2(mul2(dtp, A2[0]));
-        ev[j][1] = ex2x2(mul2(dtp, A2[1]));
-        hp0 = fma2(ev[j][0], hp0, mul2(dup, pk(bv.x, bv.y)));
-        hp1 = fma2(ev[j][1], hp1, mul2(dup, pk(bv.z, bv.w)));
+        const f2 arg0 = mul2(dtp, A2[0]), arg1 = mul2(dtp, A2[1]);
+        ev[j][0] = ex2x2(arg0);
+        ev[j][1] = ex2x2(arg1);
+        const f2 x0 = mul2(dup, pk(bv.x, bv.y)), x1 = mul2(dup, pk(bv.z, bv.w));
+        hp0 = fma2(ev[j][0], hp0, ZOH ? mul2(hold2(arg0, ev[j][0], dtp, iA2[0]), x0) : x0);
+        hp1 = fma2(ev[j][1], hp1, ZOH ? mul2(hold2(arg1, ev[j][1], dtp, iA2[1]), x1) : x1);
         hv[j][0] = hp0;
         hv[j][1] = hp1;
       }
@@ -530,20 +557,37 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
       const f2 C2[2] = {pk(cv.x, cv.y), pk(cv.z, cv.w)};
       const f2 hprev[2] = {j > 0 ? hv[j > 0 ? j - 1 : 0][0] : pk(ck.x, ck.y),
                            j > 0 ? hv[j > 0 ? j - 1 : 0][1] : pk(ck.z, ck.w)};
-      f2 lam[2], g[2];
+      f2 lam[2], g[2], lw[2];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         lam[q] = fma2(dsp, C2[q], mu[q]);        // total gradient of h_t
         mu[q] = mul2(ev[j][q], lam[q]);          // carried to step t - 1
         g[q] = mul2(mu[q], hprev[q]);            // lambda e h_{t-1}
         dA[q] = fma2(g[q], dtp, dA[q]);
-        oB[j][q] = mul2(lam[q], dup);            // dB: lambda dt u
+        if constexpr (ZOH) {
+          // w = hold weight; dw/ddt = e; dw/dA = hold_dA2; dup holds (u, u)
+          const f2 arg = mul2(dtp, A2[q]);
+          const f2 w = hold2(arg, ev[j][q], dtp, iA2[q]);
+          lw[q] = mul2(lam[q], w);                                          // lambda w
+          dA[q] = fma2(mul2(lam[q], mul2(B2[q], dup)), hold_dA2(arg, ev[j][q], dtp, w, iA2[q]), dA[q]);
+          oB[j][q] = mul2(lw[q], dup);           // dB: lambda w u
+        } else {
+          lw[q] = lam[q];
+          oB[j][q] = mul2(lam[q], dup);          // dB: lambda dt u
+        }
         oC[j][q] = mul2(dsp, hv[j][q]);          // dC: ds h_t
       }
-      const f2 P = fma2(lam[1], B2[1], mul2(lam[0], B2[0]));
+      // Euler: P = sum lambda B (du = D ds + dt P), Q = sum g A (ddt = u P + Q).
+      // ZOH:   P = sum lambda w B (du = D ds + P), Q = sum g A + u sum mu B (ddt = Q),
+      // since dw/ddt = e and mu = e lambda.
+      const f2 P = fma2(lw[1], B2[1], mul2(lw[0], B2[0]));
       const f2 Q = fma2(g[1], A2[1], mul2(g[0], A2[0]));
       oP[j] = lo(P) + hi(P);
-      oQ[j] = lo(Q) + hi(Q);
+      oQ[j] = lo(Q) + hi(Q);                     // in units of log2(e) (A2 = A log2(e))
+      if constexpr (ZOH) {
+        const f2 Pe = fma2(mu[1], B2[1], mul2(mu[0], B2[0]));
+        oQ[j] = fmaf(s.y, lo(Pe) + hi(Pe), oQ[j] * kLn2);
+      }
       oR[j] = 0.f;
       if (HAS_Z) {
         const f2 R = fma2(C2[1], hv[j][1], mul2(C2[0], hv[j][0]));
@@ -585,8 +629,8 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
             P += v.x; Q += v.y; R += v.z;
           }
           const float dt = sDt[(sb * kSub + j) * kCpb + c].x;
-          const float ddt = fmaf(e_u[r][s], P, Q * kLn2);        // u P + sum lambda e h A
-          o_du[s] = fmaf(Dd, e_ds[r][s], dt * P);
+          const float ddt = ZOH ? Q : fmaf(e_u[r][s], P, Q * kLn2);   // see P and Q above
+          o_du[s] = fmaf(Dd, e_ds[r][s], ZOH ? P : dt * P);
           o_dd[s] = ddt * e_sig[r][s];
           o_dz[s] = fmaf(Dd, e_u[r][s], R) * e_dzf[r][s];
           dD_acc[r] = fmaf(e_ds[r][s], e_u[r][s], dD_acc[r]);
@@ -662,7 +706,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
 
 // ---------------------------------------------------------------------------- launchers
 
-template <int NT, bool BF, bool Z>
+template <int NT, bool BF, bool Z, bool ZOH>
 static int go_bwd(const BwdArgs& a0, cudaStream_t s) {
   BwdArgs a = a0;
   // adjoint local pass
@@ -674,7 +718,7 @@ static int go_bwd(const BwdArgs& a0, cudaStream_t s) {
   if (total > 0) bwd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(a);
   // main pass
   using G = BwdGeom<NT>;
-  auto k = bwd_main_kernel<NT, BF, Z>;
+  auto k = bwd_main_kernel<NT, BF, Z, ZOH>;
   if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kBytes) != cudaSuccess)
     return 1;
   a.ctiles = (int)((a.dim + G::kCpb - 1) / G::kCpb);
@@ -691,11 +735,12 @@ int bwd_main_ctiles(int64_t dim, int64_t dstate) {
 
 int launch_bwd(const BwdArgs& a, bool bf16, bool has_z, cudaStream_t s) {
   SSK_DISPATCH_NT(a.dstate, {
-    if (bf16) {
-      return has_z ? go_bwd<NT, true, true>(a, s) : go_bwd<NT, true, false>(a, s);
-    } else {
-      return has_z ? go_bwd<NT, false, true>(a, s) : go_bwd<NT, false, false>(a, s);
+    if (a.zoh) {
+      if (bf16) return has_z ? go_bwd<NT, true, true, true>(a, s) : go_bwd<NT, true, false, true>(a, s);
+      return has_z ? go_bwd<NT, false, true, true>(a, s) : go_bwd<NT, false, false, true>(a, s);
     }
+    if (bf16) return has_z ? go_bwd<NT, true, true, false>(a, s) : go_bwd<NT, true, false, false>(a, s);
+    return has_z ? go_bwd<NT, false, true, false>(a, s) : go_bwd<NT, false, false, false>(a, s);
   });
   return -1;
 }

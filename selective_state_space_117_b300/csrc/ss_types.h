@@ -70,6 +70,7 @@ struct BwdArgs {
   int softplus;
   int vec;               // 1: u/delta/z rows, dy and the fp32 gradient rows allow 16-byte group loads
   int vec_bc;            // 1: B/C rows allow 16-byte loads of 8-step groups
+  int zoh;               // 1: zero-order-hold input weight
 };
 
 // Causal depthwise conv1d of width 4 over (rows = batch * dim, seqlen).

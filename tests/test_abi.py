@@ -110,9 +110,9 @@ def _bwd(dims, ws=P, ws_bytes=1 << 40, **over):
 
 
 def test_bwd_validation():
-    zoh = _dims()
-    zoh.flags = 1                                           # the backward pass is Euler only
-    assert _bwd(zoh) == ss.SS_EINVAL
+    bad = _dims()
+    bad.flags = 2                                           # unknown discretisation bit
+    assert _bwd(bad) == ss.SS_EINVAL
     assert _bwd(_dims(dt=5)) == ss.SS_EDTYPE
     assert _bwd(_dims(), dy=None) == ss.SS_EINVAL
     assert _bwd(_dims(), du=None) == ss.SS_EINVAL

@@ -18,6 +18,8 @@ h_last are linear in B, in C and in u (with h0 = 0), so
 """
 from __future__ import annotations
 
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -44,9 +46,15 @@ def grad_err(g, ref):
     return float(np.max(np.abs(g - ref) / scale))
 
 
-def make(seed, batch, dim, N, L, dtype, gate=True, with_D=True, with_bias=True, h0=True, dlast=True, softplus=True):
+def make(seed, batch, dim, N, L, dtype, gate=True, with_D=True, with_bias=True, h0=True, dlast=True, softplus=True,
+         zoh=False):
     p = I.selective_problem("bwd", seed=seed, batch=batch, dim=dim, dstate=N, seqlen=L, dtype=dtype, bc_std=0.5,
                             d_mode="normal", gate=gate, device=DEV, gen_device="cpu")
+    p.extra["zoh"] = zoh
+    if zoh:   # decay rates from -0.01 to -50: both branches of the hold weight and of its A-derivative
+        n = torch.arange(N, dtype=torch.float32)
+        row = -0.01 * torch.exp(n * (math.log(5000.0) / max(N - 1, 1)))
+        p.A = row.unsqueeze(0).expand(dim, N).contiguous().to(DEV)
     if not with_D:
         p.D = None
     if not with_bias:
@@ -64,7 +72,7 @@ def make(seed, batch, dim, N, L, dtype, gate=True, with_D=True, with_bias=True, 
 
 def gpu_grads(p, ct):
     return ss.scan_bwd(p.u, p.delta, p.A, p.B, p.C, D=p.D, z=p.z, delta_bias=p.delta_bias, softplus=p.softplus,
-                       dy=ct.dy, dlast=ct.dlast, h0=ct.h0, want_dh0=True)
+                       dy=ct.dy, dlast=ct.dlast, h0=ct.h0, want_dh0=True, zoh=p.extra.get("zoh", False))
 
 
 def oracle_grads(p, ct, chans=None):
@@ -80,7 +88,7 @@ def oracle_grads(p, ct, chans=None):
     return oracle.scan_bwd(w(p.u), w(p.delta), w(p.A), w(p.B), w(p.C), D=w(p.D), z=w(p.z),
                            delta_bias=w(p.delta_bias), softplus=p.softplus,
                            dtype="bf16" if p.in_dtype == I.BF16 else "f32", dy=dy, dlast=dl, h0=h0,
-                           chans=chans, want_BC=chans is None)
+                           chans=chans, want_BC=chans is None, zoh=p.extra.get("zoh", False))
 
 
 def compare_all(g, r, p):
@@ -110,10 +118,17 @@ CASES = [
     (8, 2, 17, 16, 1, torch.float32, {}),                                     # one step
     (9, 1, 30, 16, 150, torch.float32, dict(softplus=False)),
     (10, 3, 100, 16, 520, torch.bfloat16, dict(h0=False)),
+    # zero-order-hold input weight
+    (20, 2, 70, 16, 200, torch.float32, dict(zoh=True)),
+    (21, 1, 64, 16, 2048, torch.bfloat16, dict(zoh=True)),
+    (22, 2, 33, 13, 77, torch.float32, dict(zoh=True, with_D=False)),
+    (23, 1, 24, 64, 96, torch.bfloat16, dict(zoh=True, h0=False)),
+    (24, 1, 30, 16, 150, torch.float32, dict(zoh=True, softplus=False)),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=[f"s{c[0]}b{c[1]}d{c[2]}n{c[3]}L{c[4]}" for c in CASES])
+@pytest.mark.parametrize("case", CASES, ids=[f"s{c[0]}b{c[1]}d{c[2]}n{c[3]}L{c[4]}{'zoh' if c[6].get('zoh') else ''}"
+                                              for c in CASES])
 def test_bwd_matches_oracle(case):
     seed, batch, dim, N, L, dtype, opt = case
     p, ct = make(seed, batch, dim, N, L, dtype, **opt)
