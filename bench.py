@@ -508,6 +508,17 @@ def bench_bwd(ss, I, torch, p, pk, fwd_ms, reps=5):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
+    # the same call with the zero-order-hold input weight
+    zcall = lambda: ss.scan_bwd(p.u, p.delta, p.A, p.B, p.C, D=p.D, z=p.z, delta_bias=p.delta_bias, dy=ct.dy,
+                                dlast=ct.dlast, workspace=ws, zoh=True)
+    zcall()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        zcall()
+    e1.record()
+    torch.cuda.synchronize()
+    zoh_ms = e0.elapsed_time(e1) / reps
     elems, byts, exps = bwd_counts(p.batch, p.dim, p.dstate, p.seqlen)
     roof = roofline_terms(byts, exps, ms, pk)
     del ct, ws
@@ -515,7 +526,8 @@ def bench_bwd(ss, I, torch, p, pk, fwd_ms, reps=5):
                         "fp32 gradients",
             "entry_point": "ss_scan_bwd", "ms": round(ms, 4), "elem_per_s": elems / (ms * 1e-3),
             "algorithmic_bytes": byts, "exps": exps, "roofline": roof,
-            "time_vs_forward_step": round(ms / fwd_ms, 2) if fwd_ms else None, "gpu_launches": 5 * reps}
+            "time_vs_forward_step": round(ms / fwd_ms, 2) if fwd_ms else None,
+            "zoh_ms": round(zoh_ms, 4), "gpu_launches": 5 * (2 * reps + 1)}
 
 
 def bench_conv(ss, torch, pk, batch=1, dim=5120, seqlen=65536, reps=20):
