@@ -382,7 +382,9 @@ int ss_scan_bwd(const ss_dims* dims, const float* h0, const void* u, const void*
   a.vec = (rows16 && aligned(u, 16) && aligned(delta, 16) && aligned(z, 16) && aligned(dy, 16) && aligned(du, 16) &&
            aligned(ddelta, 16) && aligned(dz, 16) && aligned(dB, 8) && aligned(dC, 8)) ? 1 : 0;
   a.vec_bc = ((d.seqlen * (int64_t)es) % 16 == 0 && aligned(B, 16) && aligned(C, 16)) ? 1 : 0;
-  if (ssk::launch_bwd(a, bf, z != nullptr, s) != 0) return SS_EINVAL;
+  const int lrc = ssk::launch_bwd(a, bf, z != nullptr, s);
+  if (lrc < 0) return SS_EINVAL;                             // unsupported dstate (caught above)
+  if (lrc > 0) return cuda_fail(cudaGetLastError());         // the kernel attribute could not be set
   return launched();
 }
 

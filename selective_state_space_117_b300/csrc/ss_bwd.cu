@@ -708,6 +708,11 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
 
 template <int NT, bool BF, bool Z, bool ZOH>
 static int go_bwd(const BwdArgs& a0, cudaStream_t s) {
+  using G = BwdGeom<NT>;
+  auto k = bwd_main_kernel<NT, BF, Z, ZOH>;
+  // before anything is enqueued, so that a failure leaves no partial work behind
+  if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kBytes) != cudaSuccess)
+    return 1;
   BwdArgs a = a0;
   // adjoint local pass
   a.ctiles = (int)((a.dim + kCh - 1) / kCh);
@@ -717,10 +722,6 @@ static int go_bwd(const BwdArgs& a0, cudaStream_t s) {
   const int64_t total = a.batch * a.dim * a.dstate;
   if (total > 0) bwd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(a);
   // main pass
-  using G = BwdGeom<NT>;
-  auto k = bwd_main_kernel<NT, BF, Z, ZOH>;
-  if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kBytes) != cudaSuccess)
-    return 1;
   a.ctiles = (int)((a.dim + G::kCpb - 1) / G::kCpb);
   const dim3 g3((unsigned)(a.ctiles * a.nchunks), (unsigned)a.batch);
   k<<<g3, G::kThreads, G::kBytes, s>>>(a);
