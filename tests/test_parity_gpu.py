@@ -457,3 +457,44 @@ def test_prompt_state_handoff(impl):
     # L = 0 returns the initial state
     _, h_empty = call(512, 512, h0=h2)
     assert torch.equal(h_empty, h2)
+
+
+def test_decode_cuda_graph_matches_eager():
+    """The multi-step decode replayed from a CUDA graph (as a server would run it) gives
+    bitwise the eager steps' y and final state, and both match the oracle's recurrence."""
+    batch, dim, N, steps = 4, 300, 16, 64
+    st_in = I.decode_stream(seed=41, batch=batch, dim=dim, dstate=N, steps=steps, device=DEV, gen_device="cpu")
+
+    def run(state, ys):
+        for t in range(steps):
+            ss.state_update(state, st_in.u[t], st_in.delta[t], st_in.A, st_in.B[t], st_in.C[t], D=st_in.D,
+                            z=st_in.z[t], delta_bias=st_in.delta_bias, y=ys[t])
+
+    s_e = torch.zeros((batch, dim, N), device=DEV)
+    y_e = torch.empty((steps, batch, dim), device=DEV)
+    run(s_e, y_e)
+    s_g = torch.zeros((batch, dim, N), device=DEV)
+    y_g = torch.empty((steps, batch, dim), device=DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run(s_g, y_g)                                   # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(s_g, y_g)
+    for _ in range(2):                                  # replays start from a reset state
+        s_g.zero_()
+        y_g.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y_g, y_e) and torch.equal(s_g, s_e)
+    w = I.to_wire
+    sref = np.zeros((batch * dim, N))
+    yref = np.empty((steps, batch * dim))
+    for t in range(steps):
+        yref[t] = oracle.state_update(sref, w(st_in.u[t]), w(st_in.delta[t]), w(st_in.A), w(st_in.B[t]),
+                                      w(st_in.C[t]), D=w(st_in.D), z=w(st_in.z[t]), delta_bias=w(st_in.delta_bias),
+                                      dtype="bf16")
+    check(y_e.reshape(steps, -1).cpu().numpy(), yref, True, "graph decode y")
+    check(s_e.reshape(-1, N).cpu().numpy(), sref, True, "graph decode state")
