@@ -197,3 +197,28 @@ def test_bwd_long_sequence_sampled_and_identities():
     for k, (lhs, rhs, scale) in checks.items():
         rel = abs(float(lhs - rhs)) / float(scale)
         assert rel <= 1e-4, f"{k}: Euler identity off by {rel:.3e} of sum |terms|"
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_bwd_unaligned_pointers(dtype):
+    """Every array one element past a 16-byte boundary (L a multiple of 8): the kernels take
+    their element-by-element paths and scalar atomics; the gradients are the same."""
+    p, ct = make(31, 2, 40, 16, 136, dtype)
+    shift = lambda t: None if t is None else _offset_copy(t)
+    q = I.Problem(p.name, shift(p.u), shift(p.delta), shift(p.A), shift(p.B), shift(p.C), shift(p.D), shift(p.z),
+                  shift(p.delta_bias), p.softplus, 0, dict(p.extra))
+    cq = I.Cotangents(shift(ct.dy), shift(ct.dlast), shift(ct.h0))
+    for t in (q.u, q.B, cq.dy):
+        assert t.data_ptr() % 16 != 0
+    g = gpu_grads(q, cq)
+    torch.cuda.synchronize()
+    r = oracle_grads(p.to("cpu"), ct)
+    compare_all(g, r, p)
+
+
+def _offset_copy(t):
+    """A copy of t whose storage starts one element past a 16-byte aligned address."""
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    out = buf[1:].view(t.shape)
+    out.copy_(t)
+    return out
