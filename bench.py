@@ -246,8 +246,16 @@ def cpu_baseline(p, budget_s=20.0):
     sample = oracle_sample(p, nchan)
     dt = time_oracle(sample, threads)
     elems = p.batch * nchan * L
+    # one core, on a few channels; per-channel work is the same for every channel, so the
+    # whole workload's single-core time is this scaled linearly
+    n1 = 4
+    t1 = time_oracle(oracle_sample(p, n1), 1)
+    one = p.batch * n1 * L / t1
     return {"value": elems / dt, "unit": "elem/s", "cores": threads, "kind": "oracle",
-            "sample": f"{nchan} of {p.dim} channels x L={L} (fp64 C oracle, OpenMP over channels), {dt:.1f} s"}
+            "sample": f"{nchan} of {p.dim} channels x L={L} (fp64 C oracle, OpenMP over channels), {dt:.1f} s",
+            "single_core": {"value": one, "unit": "elem/s", "sample": f"{n1} channels x L={L} on 1 thread, {t1:.2f} s",
+                            "scaled_workload_s": round(p.batch * p.dim * L / one, 1),
+                            "note": "scaled linearly from the sample to all channels"}}
 
 
 # ----------------------------------------------------------------- the reference arm
