@@ -345,6 +345,7 @@ def run_ours(args):
     ms = total_ms / args.steps
     per_kernel = {name: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps))
                   for i, (_, name) in enumerate(phases)}
+    step_median = statistics.median(ev[k][0].elapsed_time(ev[k][len(phases)]) for k in range(args.steps))
     ksum = sum(per_kernel.values())
     dominant = max(per_kernel, key=per_kernel.get)
     value = elems * world / (ms * 1e-3)
@@ -370,7 +371,8 @@ def run_ours(args):
 
     line = {
         "metric": METRIC, "value": value, "unit": "elem/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": round(step_median, 4),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD}: batch=1, D={Dm}, N=16, L={L}, chunk {CHUNK}",
                    "entry_point": "ss_scan_chunked (phases local, carry, fixup)",
