@@ -124,6 +124,8 @@ CASES = [
     (22, 2, 33, 13, 77, torch.float32, dict(zoh=True, with_D=False)),
     (23, 1, 24, 64, 96, torch.bfloat16, dict(zoh=True, h0=False)),
     (24, 1, 30, 16, 150, torch.float32, dict(zoh=True, softplus=False)),
+    # the medium fp32 configuration's shape
+    (25, 2, 256, 16, 2048, torch.float32, {}),
 ]
 
 
@@ -222,3 +224,23 @@ def _offset_copy(t):
     out = buf[1:].view(t.shape)
     out.copy_(t)
     return out
+
+
+def test_bwd_long_sequence_zoh_sampled():
+    """The zero-order-hold backward pass at batch 1, dim 5120, N 16, L 65536 (bf16, gate):
+    sampled channels against the oracle."""
+    p = I.workload("mamba2p8b_long_bf16", device=DEV, gen_device="cuda")
+    p.extra["zoh"] = True
+    ct = I.cotangents(seed=104, batch=1, dim=p.dim, dstate=p.dstate, seqlen=p.seqlen, with_h0=False, device=DEV,
+                      gen_device="cuda")
+    g = gpu_grads(p, ct)
+    torch.cuda.synchronize()
+    chans = np.array([2, 100, 2500, 5118])
+    r = oracle_grads(p.to("cpu"), ct, chans=chans)
+    rows = lambda t: host(t).reshape(p.dim, p.seqlen)[chans]
+    for k in ("du", "ddelta", "dz"):
+        e = grad_err(rows(g[k]), r[k])
+        assert e <= TOL_GRAD, f"{k}: {e:.3e}"
+    assert grad_err(host(g["dA"])[chans], r["dA_part"]) <= TOL_GRAD
+    assert grad_err(host(g["dD"])[chans], r["dD_part"]) <= TOL_GRAD
+    assert grad_err(host(g["ddelta_bias"])[chans], r["dbias_part"]) <= TOL_GRAD
