@@ -265,6 +265,7 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
   a.batch = d.batch; a.dim = d.dim; a.dstate = d.dstate;
   a.softplus = softplus_flag ? 1 : 0;
   a.zoh = (d.flags & SS_FLAG_ZOH) ? 1 : 0;
+  a.err = device_status_word();
   const uintptr_t bc_align = d.in_dtype == SS_BF16 ? 8 : 16;
   a.vec = (d.dstate % 4 == 0 && aligned(state, 16) && aligned(A, 16) && aligned(B, bc_align) && aligned(C, bc_align))
               ? 1 : 0;

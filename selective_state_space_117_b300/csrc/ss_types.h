@@ -99,6 +99,7 @@ struct DecodeArgs {
   int softplus;
   int vec;           // 1: N % 4 == 0 and state, A, B, C rows allow 16/8-byte vector access
   int zoh;           // 1: zero-order-hold input weight
+  int* err;          // device status word (a bounded wait records a timeout here), may be null
 };
 
 }  // namespace ssk
