@@ -286,7 +286,7 @@ static void go_decode(const DecodeArgs& a, cudaStream_t s) {
   constexpr int G = NT < kDecodeSpl ? 1 : NT / kDecodeSpl;
   const int64_t threads = a.dim * G;
   const dim3 g2((unsigned)((threads + kDecodeThreads - 1) / kDecodeThreads), (unsigned)a.batch);
-  if constexpr (NT >= 8) {
+  if constexpr (NT >= kDecodeSpl) {
     if (a.vec) {   // bulk copies of the state need 16-byte rows (N % 4 == 0) and 16-byte alignment
       if (a.zoh) decode_bulk_kernel<NT, BF, Z, true><<<g2, kDecodeThreads, 0, s>>>(a);
       else decode_bulk_kernel<NT, BF, Z, false><<<g2, kDecodeThreads, 0, s>>>(a);
