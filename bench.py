@@ -51,10 +51,10 @@ EX2_PER_CLK_PER_SM = 32          # MUFU.EX2 issue rate of sm_103 (31.85/clk/SM m
 # to the kernel sources with the hash below; after any change to those sources
 # they no longer describe the running kernels and the bench reports null.
 TRAFFIC = {
-    "sources": "cf85f16d662a7709",
-    "local": 1360390000,     # local_tma_kernel: 1.346966 GB read + 0.013424 GB written
+    "sources": "f8e178b7f0512df0",
+    "local": 1359613000,     # local_tma_kernel: 1.347018 GB read + 0.012595 GB written
     "carry": 11485000,       # carry_kernel: 0.011485 GB read (writes stay in L2)
-    "fixup": 3345678000,     # scan_tma_kernel (fix-up): 2.033408 GB read + 1.312270 GB written
+    "fixup": 3345591000,     # scan_tma_kernel (fix-up): 2.034115 GB read + 1.311476 GB written
 }
 
 
