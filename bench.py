@@ -367,6 +367,7 @@ def run_ours(args):
     if not args.no_decode:
         side["zoh"] = bench_zoh_step(ss, torch, p, kw, elems)
         side["fwd_layer"] = bench_fwd_layer(ss, I, torch, pk)
+        side["fwd_schedules"] = bench_fwd_schedules(ss, I, torch)
         side["bwd"] = bench_bwd(ss, I, torch, p, pk, ms)
 
     line = {
@@ -473,14 +474,11 @@ def bench_e2e(ss, torch, p, y, hl, ws, world, elems, e2e_steps):
             "pipelined": "upload / scan / download on three streams, two buffer sets"}
 
 
-def bench_fwd_layer(ss, I, torch, pk, reps=20):
-    """ss_scan_fwd on the Mamba-130M-shaped layer (batch 8, D 1536, N 16, L 2048, bf16
-    inputs, gate), the single-pass entry point's own workload."""
-    p = I.workload("mamba130m_layer_bf16", device="cuda", gen_device="cuda")
-    elems, byts, exps = workload_counts(p.batch, p.dim, p.dstate, p.seqlen)
+def time_scan_fwd(ss, torch, p, schedule, reps):
+    """Average ms of ss_scan_fwd over reps calls (CUDA events around the loop)."""
     y = torch.empty((p.batch, p.dim, p.seqlen), device="cuda")
     hl = torch.empty((p.batch, p.dim, p.dstate), device="cuda")
-    kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, y=y, last_state=hl)
+    kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, softplus=p.softplus, y=y, last_state=hl, schedule=schedule)
     for _ in range(3):
         ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, **kw)
     torch.cuda.synchronize()
@@ -490,12 +488,35 @@ def bench_fwd_layer(ss, I, torch, pk, reps=20):
         ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, **kw)
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+    return e0.elapsed_time(e1) / reps
+
+
+def bench_fwd_layer(ss, I, torch, pk, reps=20):
+    """ss_scan_fwd on the Mamba-130M-shaped layer (batch 8, D 1536, N 16, L 2048, bf16
+    inputs, gate), the single-pass entry point's own workload."""
+    p = I.workload("mamba130m_layer_bf16", device="cuda", gen_device="cuda")
+    elems, byts, exps = workload_counts(p.batch, p.dim, p.dstate, p.seqlen)
+    ms = time_scan_fwd(ss, torch, p, None, reps)
     roof = roofline_terms(byts, exps, ms, pk)
     return {"workload": "mamba130m_layer_bf16: batch=8, D=1536, N=16, L=2048, bf16 inputs, gate",
-            "entry_point": "ss_scan_fwd", "ms": round(ms, 4), "elem_per_s": elems / (ms * 1e-3),
-            "roofline": roof, "note": "inputs 0.25 GB, about twice the L2: no flush between repetitions",
-            "gpu_launches": reps}
+            "entry_point": "ss_scan_fwd", "schedule": "thread (12288 channels)", "ms": round(ms, 4),
+            "elem_per_s": elems / (ms * 1e-3), "roofline": roof,
+            "note": "inputs 0.25 GB, about twice the L2: no flush between repetitions", "gpu_launches": reps}
+
+
+def bench_fwd_schedules(ss, I, torch, reps=50):
+    """ss_scan_fwd under both schedules on the medium workload (batch 2, D 256, N 16,
+    L 2048, fp32 inputs, gate): 512 channels, too few to fill the GPU one thread each."""
+    p = I.workload("medium_fp32_gate", device="cuda", gen_device="cuda")
+    elems = p.batch * p.dim * p.seqlen
+    out = {"workload": "medium_fp32_gate: batch=2, D=256, N=16, L=2048, fp32 inputs, gate",
+           "entry_point": "ss_scan_fwd", "note": "inputs 13 MB stay in L2 between repetitions",
+           "gpu_launches": 2 * reps}
+    for sched in ("warp", "thread"):
+        ms = time_scan_fwd(ss, torch, p, sched, reps)
+        out[f"ms_{sched}"] = round(ms, 4)
+        out[f"elem_per_s_{sched}"] = elems / (ms * 1e-3)
+    return out
 
 
 def bench_zoh_step(ss, torch, p, kw, elems, reps=5):

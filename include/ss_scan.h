@@ -76,13 +76,33 @@ typedef enum {
  */
 #define SS_FLAG_ZOH 1
 
+/*
+ * Schedule flags, accepted by ss_scan_fwd and ss_scan_fwd_h0 only (other entry
+ * points reject them with SS_EINVAL).  Both schedules compute the same
+ * recurrence; results differ only in rounding order.
+ *   SS_FLAG_SCHED_THREAD  one thread per channel holds the channel's N states
+ *                         and walks all L steps.
+ *   SS_FLAG_SCHED_WARP    one warp per channel: each lane owns 16 consecutive
+ *                         steps of a 512-step segment, and the lanes' (decay
+ *                         product, state) pairs are combined by a warp-shuffle
+ *                         scan under the associative operator of the recurrence
+ *                         ("Parallel scan", azimuth.plus).  Needs the Euler
+ *                         weight, 1 <= N <= 16, L a multiple of 8 and 16-byte
+ *                         aligned u, delta, z, y, B and C; otherwise SS_EINVAL.
+ * With neither flag the library picks: the warp schedule where it is available
+ * and batch * dim < 9216 (too few channels to fill the GPU one thread each),
+ * else the thread schedule.  Both flags together: SS_EINVAL.
+ */
+#define SS_FLAG_SCHED_THREAD 2
+#define SS_FLAG_SCHED_WARP 4
+
 typedef struct {
     int64_t batch;     /* >= 0; at most 65535 */
     int64_t dim;       /* channels D, >= 0 */
     int64_t dstate;    /* state size N, 0 .. SS_MAX_DSTATE */
     int64_t seqlen;    /* sequence length L, >= 0 (ignored by ss_state_update) */
     int32_t in_dtype;  /* ss_dtype of u, delta, B, C, z */
-    int32_t flags;     /* 0 or SS_FLAG_ZOH; other bits are rejected with SS_EINVAL */
+    int32_t flags;     /* SS_FLAG_ZOH, plus SS_FLAG_SCHED_* where accepted; other bits: SS_EINVAL */
 } ss_dims;
 
 /*

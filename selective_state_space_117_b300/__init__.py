@@ -46,6 +46,8 @@ class SSError(RuntimeError):
 
 
 FLAG_ZOH = 1
+FLAG_SCHED_THREAD, FLAG_SCHED_WARP = 2, 4
+_SCHED = {None: 0, "thread": FLAG_SCHED_THREAD, "warp": FLAG_SCHED_WARP}
 
 
 class Dims(ctypes.Structure):
@@ -167,13 +169,17 @@ def _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state):
 
 
 def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, y=None, last_state=None,
-             return_last_state=False, h0=None, zoh=False, stream=None):
+             return_last_state=False, h0=None, zoh=False, schedule=None, stream=None):
     """Full-sequence selective scan.  Returns y (fp32, (batch, dim, L)), or
     (y, last_state) when ``return_last_state`` or ``last_state`` is given.
     ``h0`` (fp32, (batch, dim, N)) starts the scan from that state (ss_scan_fwd_h0).
-    ``zoh`` uses the zero-order-hold input weight (SS_FLAG_ZOH)."""
+    ``zoh`` uses the zero-order-hold input weight (SS_FLAG_ZOH).  ``schedule``:
+    None (the library picks), "thread" (one thread per channel) or "warp" (one
+    warp per channel, lanes split time; SS_FLAG_SCHED_*)."""
+    if schedule not in _SCHED:
+        raise ValueError(f"schedule must be one of {sorted(k for k in _SCHED if k)} or None")
     dims, y = _scan_common(u, delta, A, B, C, D, z, delta_bias, y, last_state)
-    dims.flags = FLAG_ZOH if zoh else 0
+    dims.flags = (FLAG_ZOH if zoh else 0) | _SCHED[schedule]
     _need(h0, "h0", (dims.batch, dims.dim, dims.dstate), torch.float32, u.device)
     if return_last_state and last_state is None:
         last_state = torch.empty((dims.batch, dims.dim, dims.dstate), dtype=torch.float32, device=u.device)

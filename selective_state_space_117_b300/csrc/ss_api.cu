@@ -33,6 +33,8 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 constexpr int64_t kMaxGridX = 2147483647;
 constexpr int64_t kMaxGridY = 65535;
 constexpr size_t kWsAlign = 256;
+// ss_scan_fwd takes the one-warp-per-channel schedule below this many channels (batch * dim).
+constexpr int64_t kWarpBelowChannels = 9216;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -59,12 +61,13 @@ int* device_status_word() {
 // Shape, dtype and pointer checks shared by the two full-sequence entry points.
 int check_scan(const ss_dims* dims, const void* u, const void* delta, const float* A, const void* B,
                const void* C, const float* D, const void* z, const float* delta_bias, const float* y,
-               const float* last_state) {
+               const float* last_state, int32_t allowed_flags = SS_FLAG_ZOH) {
   if (!dims) return SS_EINVAL;
   const ss_dims& d = *dims;
   if (d.in_dtype != SS_F32 && d.in_dtype != SS_BF16) return SS_EDTYPE;
   if (d.batch < 0 || d.dim < 0 || d.dstate < 0 || d.seqlen < 0) return SS_EINVAL;
-  if ((d.flags & ~SS_FLAG_ZOH) != 0) return SS_EINVAL;
+  if ((d.flags & ~allowed_flags) != 0) return SS_EINVAL;
+  if ((d.flags & SS_FLAG_SCHED_THREAD) && (d.flags & SS_FLAG_SCHED_WARP)) return SS_EINVAL;
   if (d.dstate > SS_MAX_DSTATE || d.batch > kMaxGridY) return SS_EINVAL;
   if (ceil_div(d.dim, ssk::kCh) > kMaxGridX) return SS_EINVAL;
   const size_t es = in_size(d.in_dtype);
@@ -116,7 +119,8 @@ int initial_state(const ss_dims& d, const float* h0, float* last_state, cudaStre
 int scan_fwd_impl(const ss_dims* dims, const float* h0, const void* u, const void* delta, const float* A,
                   const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
                   int softplus_flag, float* y, float* last_state, cudaStream_t s) {
-  const int st = check_scan(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state);
+  const int st = check_scan(dims, u, delta, A, B, C, D, z, delta_bias, y, last_state,
+                            SS_FLAG_ZOH | SS_FLAG_SCHED_THREAD | SS_FLAG_SCHED_WARP);
   if (st != SS_OK) return st;
   if (!aligned(h0, 4)) return SS_EALIGN;
   const ss_dims& d = *dims;
@@ -127,6 +131,20 @@ int scan_fwd_impl(const ss_dims* dims, const float* h0, const void* u, const voi
   a.h0 = h0;
   const dim3 grid((unsigned)a.ctiles, (unsigned)d.batch);
   const bool bf = d.in_dtype == SS_BF16;
+  // Schedule.  One thread per channel advances a channel by about one step per 110 ns
+  // while the GPU is far from full, and one warp per channel moves about 90 G
+  // elements/s (B300, N = 16): the two meet near 10 K channels, whatever L is.
+  const bool warp_ok = ssk::warp_scan_available(a, bf);
+  if (d.flags & SS_FLAG_SCHED_WARP) {
+    if (!warp_ok) return SS_EINVAL;
+  }
+  const bool use_warp = (d.flags & SS_FLAG_SCHED_WARP) ||
+                        (!(d.flags & SS_FLAG_SCHED_THREAD) && warp_ok && d.batch * d.dim < kWarpBelowChannels);
+  if (use_warp) {
+    const int rc = ssk::launch_scan_warp(a, bf, z != nullptr, s);
+    if (rc != 0) return cuda_fail((cudaError_t)rc);
+    return launched();
+  }
   if (ssk::tma_available(a, bf, ssk::kFull) && ssk::launch_scan_tma(a, bf, z != nullptr, ssk::kFull, grid, s) == 0)
     return launched();
   if (ssk::launch_scan_full(a, bf, z != nullptr, grid, s) != 0) return SS_EINVAL;

@@ -61,11 +61,16 @@ def _chunked(dims, chunk=8, ws=P, ws_bytes=1 << 30, **over):
                                     a["bias"], 1, a["y"], a["last"], chunk, ws, ws_bytes, None)
 
 
+def _flagged(flags, **kw):
+    d = _dims(**kw)
+    d.flags = flags
+    return d
+
+
 def test_validation_status_codes():
     assert _fwd(_dims(dt=7)) == ss.SS_EDTYPE
-    bad = _dims()
-    bad.flags = 2                                           # unknown discretisation bit
-    assert _fwd(bad) == ss.SS_EINVAL
+    assert _fwd(_flagged(8)) == ss.SS_EINVAL                # unknown flag bit
+    assert _fwd(_flagged(1 << 30)) == ss.SS_EINVAL
     assert _fwd(_dims(L=-1)) == ss.SS_EINVAL
     assert _fwd(_dims(n=65)) == ss.SS_EINVAL
     assert _fwd(_dims(b=70000)) == ss.SS_EINVAL
@@ -80,6 +85,25 @@ def test_validation_status_codes():
     # sizes of zero are valid no-ops and return before any launch
     assert _fwd(_dims(b=0), u=None, delta=None, y=None) == ss.SS_OK
     assert _fwd(_dims(d=0), u=None, delta=None, y=None, A=None) == ss.SS_OK
+
+
+def test_schedule_flags():
+    # every case fails on the host before any launch
+    both = ss.FLAG_SCHED_THREAD | ss.FLAG_SCHED_WARP
+    assert _fwd(_flagged(both)) == ss.SS_EINVAL
+    # the warp schedule refuses what it cannot run: N > 16, L % 8 != 0, the zero-order hold
+    assert _fwd(_flagged(ss.FLAG_SCHED_WARP, n=17)) == ss.SS_EINVAL
+    assert _fwd(_flagged(ss.FLAG_SCHED_WARP, L=12)) == ss.SS_EINVAL
+    assert _fwd(_flagged(ss.FLAG_SCHED_WARP | ss.FLAG_ZOH)) == ss.SS_EINVAL
+    # schedule flags belong to ss_scan_fwd only
+    assert _chunked(_flagged(ss.FLAG_SCHED_THREAD)) == ss.SS_EINVAL
+    assert _chunked(_flagged(ss.FLAG_SCHED_WARP)) == ss.SS_EINVAL
+    assert _bwd(_flagged(ss.FLAG_SCHED_WARP)) == ss.SS_EINVAL
+    # zero sizes stay no-ops under either flag
+    assert _fwd(_flagged(ss.FLAG_SCHED_WARP, b=0), u=None, delta=None, y=None) == ss.SS_OK
+    with pytest.raises(ValueError):
+        ss.scan_fwd(torch.zeros(1, 1, 8), torch.zeros(1, 1, 8), torch.zeros(1, 4), torch.zeros(1, 4, 8),
+                    torch.zeros(1, 4, 8), schedule="lanes")
 
 
 def test_chunked_validation():

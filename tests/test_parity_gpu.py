@@ -45,6 +45,8 @@ def run(p: I.Problem, impl: str, chunk_len=None):
     kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, softplus=p.softplus, return_last_state=True)
     if impl == "fwd":
         return ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, **kw)
+    if impl in ("fwd_thread", "fwd_warp"):
+        return ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, schedule=impl[4:], **kw)
     return ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, chunk_len=chunk_len, **kw)
 
 
@@ -115,14 +117,16 @@ def test_worked_examples(impl):
 
 # ------------------------------------------------------------ the workloads
 
-@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("chunked", 1), ("chunked", 7), ("chunked", 16), ("chunked", 64)])
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("fwd_thread", None), ("fwd_warp", None), ("chunked", 1),
+                                        ("chunked", 7), ("chunked", 16), ("chunked", 64)])
 def test_tiny_fp32(impl, chunk):
     p = I.workload("tiny_fp32", device=DEV, gen_device="cpu")
     y, hl = run(p, impl, chunk)
     compare(p, y, hl, f"tiny_fp32/{impl}{chunk or ''}")
 
 
-@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("chunked", 2048), ("chunked", 256), ("chunked", 100)])
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("fwd_thread", None), ("fwd_warp", None), ("chunked", 2048),
+                                        ("chunked", 256), ("chunked", 100)])
 def test_medium_fp32_gate(impl, chunk):
     p = I.workload("medium_fp32_gate", device=DEV, gen_device="cpu")
     y, hl = run(p, impl, chunk)
@@ -157,7 +161,7 @@ def test_medium_lti_closed_form():
     assert worst <= 1e-4, worst
 
 
-@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("chunked", 512)])
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("fwd_warp", None), ("chunked", 512)])
 def test_mamba130m_layer_bf16(impl, chunk):
     p = I.workload("mamba130m_layer_bf16", device=DEV, gen_device="cuda")
     y, hl = run(p, impl, chunk)
@@ -165,7 +169,7 @@ def test_mamba130m_layer_bf16(impl, chunk):
     compare(p, y, hl, f"mamba130m/{impl}{chunk or ''}", ds=ds)
 
 
-@pytest.mark.parametrize("impl,chunk", [("chunked", 2048), ("fwd", None)])
+@pytest.mark.parametrize("impl,chunk", [("chunked", 2048), ("fwd", None), ("fwd_thread", None)])
 def test_mamba2p8b_long_bf16(impl, chunk):
     p = I.workload("mamba2p8b_long_bf16", device=DEV, gen_device="cuda")
     y, hl = run(p, impl, chunk)
@@ -250,12 +254,50 @@ TMA_SHAPES = [
 
 
 @pytest.mark.parametrize("case", TMA_SHAPES, ids=[f"b{c[1]}d{c[2]}n{c[3]}L{c[4]}c{c[6]}" for c in TMA_SHAPES])
-@pytest.mark.parametrize("impl", ["fwd", "chunked"])
+@pytest.mark.parametrize("impl", ["fwd", "fwd_thread", "chunked"])
 def test_tma_shapes(case, impl):
     seed, batch, dim, N, L, dt, chunk = case
     p = custom(seed, batch, dim, N, L, dt)
     y, hl = run(p, impl, chunk)
     compare(p, y, hl, f"tma/{impl}")
+
+
+# Shapes for the one-warp-per-channel schedule (512-step segments, 16 steps per lane):
+# L = 8 (one lane busy), a last segment holding 8 steps, empty lanes in the last
+# segment, exact segment multiples, odd and small N, channel counts that leave the
+# last 12-warp block part-empty, and each optional input off.
+WARP_SHAPES = [
+    # seed, batch, dim, N, L, dtype, gate, with_D, with_bias, softplus
+    (61, 1, 5, 1, 8, torch.float32, True, True, True, True),
+    (62, 2, 13, 3, 24, torch.bfloat16, True, True, True, True),
+    (63, 1, 25, 16, 520, torch.float32, True, True, True, True),
+    (64, 3, 12, 8, 1536, torch.bfloat16, False, False, False, True),
+    (65, 1, 7, 16, 1032, torch.bfloat16, True, True, True, False),
+    (66, 2, 40, 5, 2000, torch.float32, True, False, True, True),
+    (67, 1, 3, 16, 4104, torch.bfloat16, True, True, True, True),
+]
+
+
+@pytest.mark.parametrize("case", WARP_SHAPES, ids=[f"b{c[1]}d{c[2]}n{c[3]}L{c[4]}{'bf' if c[5] == torch.bfloat16 else 'f'}"
+                                                   for c in WARP_SHAPES])
+def test_warp_schedule_shapes(case):
+    seed, batch, dim, N, L, dt, gate, wd, wb, sp = case
+    p = custom(seed, batch, dim, N, L, dt, gate, wd, wb, sp)
+    y, hl = run(p, "fwd_warp")
+    compare(p, y, hl, "warp")
+
+
+def test_warp_schedule_refuses_unaligned_rows():
+    p = custom(68, 1, 4, 16, 64, torch.bfloat16)
+    u = torch.empty(p.u.numel() + 1, dtype=p.u.dtype, device=DEV)[1:].view_as(p.u)
+    u.copy_(p.u)
+    with pytest.raises(ss.SSError) as ei:
+        ss.scan_fwd(u, p.delta, p.A, p.B, p.C, D=p.D, z=p.z, delta_bias=p.delta_bias, schedule="warp")
+    assert ei.value.status == ss.SS_EINVAL
+    # without the flag the library runs the thread schedule on the same arrays
+    kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, return_last_state=True)
+    y, hl = ss.scan_fwd(u, p.delta, p.A, p.B, p.C, **kw)
+    compare(p, y, hl, "unaligned u, default schedule")
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
@@ -412,7 +454,7 @@ def test_device_status_clean_after_runs():
     assert ss.device_status(clear=True) == ss.SS_OK
 
 
-@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("chunked", 64), ("chunked", 7)])
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("fwd_thread", None), ("chunked", 64), ("chunked", 7)])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 def test_initial_state(impl, chunk, dtype):
     """Scans started from a given state h0 against the oracle started from the same state."""
@@ -420,8 +462,8 @@ def test_initial_state(impl, chunk, dtype):
     g = torch.Generator().manual_seed(112)
     h0 = torch.randn((2, 90, 16), generator=g)
     kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, softplus=p.softplus, return_last_state=True, h0=h0.to(DEV))
-    if impl == "fwd":
-        y, hl = ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, **kw)
+    if impl.startswith("fwd"):
+        y, hl = ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, schedule=impl[4:] or None, **kw)
     else:
         y, hl = ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, chunk_len=chunk, **kw)
     yr, hr = oracle_scan(p.to("cpu"), h0=h0.double().numpy().reshape(180, 16))
