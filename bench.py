@@ -306,6 +306,10 @@ def run_ours(args):
     from selective_state_space_117_b300 import inputs as I
 
     pk = peaks()
+    if args.schedules_only:            # the ss_scan_fwd schedule comparison alone (for profiling it)
+        if rank == 0:
+            print(json.dumps({"fwd_schedules": bench_fwd_schedules(ss, I, torch)}), flush=True)
+        return 0
     p = I.workload(WORKLOAD, device="cuda", gen_device="cuda", dim=args.dim, seqlen=args.seqlen)
     Bt, Dm, N, L = p.batch, p.dim, p.dstate, p.seqlen
     if args.bwd_only:                  # the backward leg alone (for profiling it); one JSON line
@@ -505,17 +509,26 @@ def bench_fwd_layer(ss, I, torch, pk, reps=20):
 
 
 def bench_fwd_schedules(ss, I, torch, reps=50):
-    """ss_scan_fwd under both schedules on the medium workload (batch 2, D 256, N 16,
-    L 2048, fp32 inputs, gate): 512 channels, too few to fill the GPU one thread each."""
-    p = I.workload("medium_fp32_gate", device="cuda", gen_device="cuda")
-    elems = p.batch * p.dim * p.seqlen
-    out = {"workload": "medium_fp32_gate: batch=2, D=256, N=16, L=2048, fp32 inputs, gate",
-           "entry_point": "ss_scan_fwd", "note": "inputs 13 MB stay in L2 between repetitions",
-           "gpu_launches": 2 * reps}
-    for sched in ("warp", "thread"):
-        ms = time_scan_fwd(ss, torch, p, sched, reps)
-        out[f"ms_{sched}"] = round(ms, 4)
-        out[f"elem_per_s_{sched}"] = elems / (ms * 1e-3)
+    """ss_scan_fwd under both schedules (SS_FLAG_SCHED_WARP first, then _THREAD) on the
+    medium workload (batch 2, D 256, N 16, L 2048, fp32 inputs, gate: 512 channels, too
+    few to fill the GPU one thread each) and on the Mamba-130M-shaped layer (12288
+    channels, where one thread per channel wins).  Each schedule runs 3 untimed and
+    `reps` timed calls."""
+    out = {"entry_point": "ss_scan_fwd", "gpu_launches": 4 * reps}
+    for key, name, desc, note in (
+            ("medium", "medium_fp32_gate", "batch=2, D=256, N=16, L=2048, fp32 inputs, gate",
+             "inputs 13 MB stay in L2 between repetitions"),
+            ("mamba130m", "mamba130m_layer_bf16", "batch=8, D=1536, N=16, L=2048, bf16 inputs, gate",
+             "inputs 0.25 GB, about twice the L2")):
+        p = I.workload(name, device="cuda", gen_device="cuda")
+        elems = p.batch * p.dim * p.seqlen
+        r = {"workload": f"{name}: {desc}", "note": note}
+        for sched in ("warp", "thread"):
+            ms = time_scan_fwd(ss, torch, p, sched, reps)
+            r[f"ms_{sched}"] = round(ms, 4)
+            r[f"elem_per_s_{sched}"] = elems / (ms * 1e-3)
+        out[key] = r
+        del p
     return out
 
 
@@ -676,6 +689,8 @@ def main():
     ap.add_argument("--seqlen", type=int, default=65536, help="steps (65536 = the workload; shorter only for profiling)")
     ap.add_argument("--bwd-only", action="store_true",
                     help="time only the backward pass (ss_scan_bwd), --steps calls after 2 warm-ups")
+    ap.add_argument("--schedules-only", action="store_true",
+                    help="time only ss_scan_fwd under its two schedules (medium workload, then the 130M layer)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
