@@ -51,10 +51,10 @@ EX2_PER_CLK_PER_SM = 32          # MUFU.EX2 issue rate of sm_103 (31.85/clk/SM m
 # to the kernel sources with the hash below; after any change to those sources
 # they no longer describe the running kernels and the bench reports null.
 TRAFFIC = {
-    "sources": "f8e178b7f0512df0",
-    "local": 1359613000,     # local_tma_kernel: 1.347018 GB read + 0.012595 GB written
+    "sources": "f7e521cb34ececc7",
+    "local": 1360557000,     # local_tma_kernel: 1.347123 GB read + 0.013434 GB written
     "carry": 11485000,       # carry_kernel: 0.011485 GB read (writes stay in L2)
-    "fixup": 3345591000,     # scan_tma_kernel (fix-up): 2.034115 GB read + 1.311476 GB written
+    "fixup": 3346096000,     # scan_tma_kernel (fix-up): 2.033337 GB read + 1.312759 GB written
 }
 
 

@@ -309,6 +309,16 @@ int ss_last_cuda_error(void);
  */
 int ss_device_status(int clear);
 
+/*
+ * Diagnostic of the failure path above: launches one thread that waits, with
+ * the library's bounded mbarrier wait, on a barrier that nothing ever arrives
+ * on.  After the wait's limit (one second on the global timer) it gives up, records
+ * SS_ETIMEOUT in the device status word and returns; the device stays usable.
+ * Asynchronous on `stream`; read the result with ss_device_status.  Returns
+ * SS_ECUDA if the launch failed.  Nothing else is touched.
+ */
+int ss_selftest_wait_timeout(ss_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

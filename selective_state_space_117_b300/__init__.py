@@ -21,6 +21,7 @@ from typing import Optional
 import torch
 
 __all__ = ["scan_fwd", "scan_chunked", "scan_bwd", "bwd_workspace_bytes", "state_update", "causal_conv1d", "chunked_workspace_bytes", "device_status",
+           "selftest_wait_timeout",
            "SSError",
            "library_path",
            "F32", "BF16", "MAX_DSTATE", "LAUNCHES"]
@@ -89,6 +90,8 @@ def lib():
         L.ss_status_string.restype = ctypes.c_char_p
         L.ss_last_cuda_error.argtypes = []
         L.ss_last_cuda_error.restype = ctypes.c_int
+        L.ss_selftest_wait_timeout.argtypes = [vp]
+        L.ss_selftest_wait_timeout.restype = ctypes.c_int
         L.ss_causal_conv1d.argtypes = [dp, vp, vp, vp, ctypes.c_int, vp, vp]
         L.ss_causal_conv1d.restype = ctypes.c_int
         L.ss_scan_bwd_workspace_bytes.argtypes = [dp]
@@ -316,6 +319,14 @@ def device_status(clear: bool = False) -> int:
     if st not in (SS_OK, SS_ETIMEOUT):
         _check(st, "ss_device_status")
     return st
+
+
+def selftest_wait_timeout(device=None, stream=None):
+    """Launch the diagnostic bounded wait that runs out (ss_selftest_wait_timeout) on
+    ``device`` (default: the current CUDA device); read the outcome with device_status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib().ss_selftest_wait_timeout(_stream(dev, stream)), "ss_selftest_wait_timeout")
 
 
 def causal_conv1d(x, weight, bias=None, silu=True, *, out=None, stream=None):

@@ -422,6 +422,13 @@ const char* ss_status_string(int status) {
 
 int ss_last_cuda_error(void) { return g_last_cuda; }
 
+int ss_selftest_wait_timeout(ss_stream_t stream) {
+  int* word = device_status_word();
+  if (!word) return cuda_fail(cudaGetLastError());
+  ssk::launch_wait_timeout(word, reinterpret_cast<cudaStream_t>(stream));
+  return launched();
+}
+
 int ss_device_status(int clear) {
   int* word = device_status_word();
   if (!word) return cuda_fail(cudaGetLastError());

@@ -39,6 +39,9 @@ int bwd_main_ctiles(int64_t dim, int64_t dstate);
 bool warp_scan_available(const ScanArgs& a, bool bf16);
 int launch_scan_warp(const ScanArgs& a, bool bf16, bool has_z, cudaStream_t s);
 
+// Diagnostic: one bounded mbarrier wait that runs out and records the timeout in *err.
+int launch_wait_timeout(int* err, cudaStream_t s);
+
 // Causal depthwise conv1d (width 4) with optional SiLU; segments of a row per warp.
 int launch_conv1d(const ConvArgs& a, bool bf16, bool silu_on, cudaStream_t s);
 int64_t conv1d_segments(int64_t seqlen);

@@ -3,9 +3,9 @@
 // Bulk tensor copies move whole 2-D/3-D boxes between global and shared
 // memory without per-thread address work: one elected thread issues them, an
 // mbarrier counts the bytes of each load, and bulk-group fences track the
-// stores.  Every wait on an mbarrier is bounded: after kMaxSpins polls it
-// records an error in the caller's status word and gives up instead of
-// hanging the GPU.
+// stores.  Every wait on an mbarrier is bounded: after one second on the
+// global timer it records an error in the caller's status word and gives up
+// instead of hanging the GPU.
 #pragma once
 
 #include <cuda.h>
@@ -19,7 +19,18 @@ namespace ssk {
 constexpr int kDevOk = 0;
 constexpr int kDevTimeout = 1;
 
-constexpr int kMaxSpins = 1 << 22;
+// A wait gives up after kWaitNs of the global timer.  A poll of an incomplete
+// phase can itself suspend the thread for a few microseconds, so the limit is
+// kept in time, not in polls; kMaxSpins only backs it up should the timer not
+// advance.
+constexpr unsigned long long kWaitNs = 1000000000ull;
+constexpr int kMaxSpins = 1 << 26;
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
@@ -49,11 +60,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false
-// (and sets *err) if it did not complete within kMaxSpins polls.
+// (and sets *err) if it did not complete within kWaitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
   for (int i = 0; i < kMaxSpins; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (i > 64) __nanosleep(128);
+    if ((i & 255) == 255 && global_ns() - t0 > kWaitNs) break;
   }
   if (err) atomicExch(err, kDevTimeout);
   return false;
