@@ -86,12 +86,14 @@ typedef enum {
  *                         steps of a 512-step segment, and the lanes' (decay
  *                         product, state) pairs are combined by a warp-shuffle
  *                         scan under the associative operator of the recurrence
- *                         ("Parallel scan", azimuth.plus).  Needs the Euler
- *                         weight, 1 <= N <= 16, L a multiple of 8 and 16-byte
- *                         aligned u, delta, z, y, B and C; otherwise SS_EINVAL.
+ *                         ("Parallel scan", azimuth.plus).  Needs
+ *                         1 <= N <= 16, L a multiple of 8 and 16-byte aligned
+ *                         u, delta, z, y, B and C (either input weight);
+ *                         otherwise SS_EINVAL.
  * With neither flag the library picks: the warp schedule where it is available
- * and batch * dim < 9216 (too few channels to fill the GPU one thread each),
- * else the thread schedule.  Both flags together: SS_EINVAL.
+ * and batch * dim < 9216 (< 20480 with SS_FLAG_ZOH): too few channels to fill
+ * the GPU one thread each; else the thread schedule.  Both flags together:
+ * SS_EINVAL.
  */
 #define SS_FLAG_SCHED_THREAD 2
 #define SS_FLAG_SCHED_WARP 4

@@ -33,8 +33,11 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 constexpr int64_t kMaxGridX = 2147483647;
 constexpr int64_t kMaxGridY = 65535;
 constexpr size_t kWsAlign = 256;
-// ss_scan_fwd takes the one-warp-per-channel schedule below this many channels (batch * dim).
+// ss_scan_fwd takes the one-warp-per-channel schedule below this many channels (batch * dim):
+// Euler input weight, and the zero-order hold (whose weight slows the one-thread-per-channel
+// kernel about 2.9x but the warp kernel only about 1.4x).
 constexpr int64_t kWarpBelowChannels = 9216;
+constexpr int64_t kWarpBelowChannelsZoh = 20480;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -132,14 +135,16 @@ int scan_fwd_impl(const ss_dims* dims, const float* h0, const void* u, const voi
   const dim3 grid((unsigned)a.ctiles, (unsigned)d.batch);
   const bool bf = d.in_dtype == SS_BF16;
   // Schedule.  One thread per channel advances a channel by about one step per 110 ns
-  // while the GPU is far from full, and one warp per channel moves about 90 G
-  // elements/s (B300, N = 16): the two meet near 10 K channels, whatever L is.
+  // (Euler; 290 ns with the hold weight) while the GPU is far from full, and one warp per
+  // channel moves about 90 G elements/s (73 G with the hold weight; B300, N = 16): the two
+  // meet near 10 K channels (21 K with the hold weight), whatever L is.
   const bool warp_ok = ssk::warp_scan_available(a, bf);
   if (d.flags & SS_FLAG_SCHED_WARP) {
     if (!warp_ok) return SS_EINVAL;
   }
+  const int64_t below = a.zoh ? kWarpBelowChannelsZoh : kWarpBelowChannels;
   const bool use_warp = (d.flags & SS_FLAG_SCHED_WARP) ||
-                        (!(d.flags & SS_FLAG_SCHED_THREAD) && warp_ok && d.batch * d.dim < kWarpBelowChannels);
+                        (!(d.flags & SS_FLAG_SCHED_THREAD) && warp_ok && d.batch * d.dim < below);
   if (use_warp) {
     const int rc = ssk::launch_scan_warp(a, bf, z != nullptr, s);
     if (rc != 0) return cuda_fail((cudaError_t)rc);

@@ -34,7 +34,7 @@ int launch_bwd(const BwdArgs& a, bool bf16, bool has_z, cudaStream_t s);
 int bwd_main_ctiles(int64_t dim, int64_t dstate);
 
 // Full-sequence scan with one warp per channel (lanes split time): available for
-// Euler, N <= 16, seqlen % 8 == 0 and 16-byte aligned rows; returns 0 when launched,
+// N <= 16, seqlen % 8 == 0 and 16-byte aligned rows (either input weight); returns 0 when launched,
 // else the cudaError_t of the failed attribute call.
 bool warp_scan_available(const ScanArgs& a, bool bf16);
 int launch_scan_warp(const ScanArgs& a, bool bf16, bool has_z, cudaStream_t s);

@@ -17,8 +17,9 @@
 // channels, are copied into shared memory by cp.async one segment ahead and
 // widened to fp32 [pair][step] tiles once per block.
 //
-// Supported: Euler input weight, N <= 16, seqlen % 8 == 0, 16-byte aligned rows
-// (u, delta, z, y, B, C).  Other shapes use the one-thread-per-channel kernels.
+// Supported: the Euler or the zero-order-hold input weight, N <= 16, seqlen % 8 == 0,
+// 16-byte aligned rows (u, delta, z, y, B, C).  Other shapes use the
+// one-thread-per-channel kernels.
 #include "ss_device.cuh"
 #include "ss_kernels.cuh"
 #include "ss_launch.h"
@@ -33,8 +34,8 @@ constexpr int kWW = 12;                 // warps (channels) per block
 constexpr int kWRow = kWS + kWS / kWT;  // tile row in f2 units: one pad slot per lane's steps
 
 // Shared memory: B and C tiles (f2 [NP][kWRow] each), the raw B/C rows of the next
-// segment ([B, C][NT][kWS] input elements), and per warp A * log2(e) and the
-// carried state as pairs.
+// segment ([B, C][NT][kWS] input elements), and per warp A * log2(e), 1 / A (zero where
+// A = 0) and the carried state as pairs.
 template <int NT, bool BF>
 struct WarpLayout {
   static constexpr int NP = NT / 2;
@@ -44,7 +45,8 @@ struct WarpLayout {
   static constexpr int oRaw = 2 * kTile;
   static constexpr int kRaw = 2 * NT * kWS * ES;
   static constexpr int oA = oRaw + kRaw;
-  static constexpr int oH = oA + kWW * NP * 8;
+  static constexpr int oIA = oA + kWW * NP * 8;
+  static constexpr int oH = oIA + kWW * NP * 8;
   static constexpr int kBytes = oH + kWW * NP * 8;
 };
 
@@ -63,7 +65,7 @@ __device__ __forceinline__ float raw_elem(const unsigned char* p, int i) {
   else return reinterpret_cast<const float*>(p)[i];
 }
 
-template <int NT, bool BF, bool HAS_Z>
+template <int NT, bool BF, bool HAS_Z, bool ZOH>
 __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a) {
   using L = In<BF>;
   using Lay = WarpLayout<NT, BF>;
@@ -75,6 +77,7 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
   unsigned char* raw = sm + Lay::oRaw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   f2* sA = reinterpret_cast<f2*>(sm + Lay::oA) + warp * NP;
+  f2* sIA = reinterpret_cast<f2*>(sm + Lay::oIA) + warp * NP;
   f2* sH = reinterpret_cast<f2*>(sm + Lay::oH) + warp * NP;
 
   const int64_t b = blockIdx.y;
@@ -90,14 +93,15 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
     const int n0 = 2 * lane, n1 = 2 * lane + 1;
     float a0 = 0.f, a1 = 0.f, h0 = 0.f, h1 = 0.f;
     if (active) {
-      if (n0 < N) a0 = a.A[d * N + n0] * kLog2e;
-      if (n1 < N) a1 = a.A[d * N + n1] * kLog2e;
+      if (n0 < N) a0 = a.A[d * N + n0];
+      if (n1 < N) a1 = a.A[d * N + n1];
       if (a.h0) {
         if (n0 < N) h0 = a.h0[bd * N + n0];
         if (n1 < N) h1 = a.h0[bd * N + n1];
       }
     }
-    sA[lane] = pk(a0, a1);
+    sA[lane] = pk(a0 * kLog2e, a1 * kLog2e);
+    sIA[lane] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
     sH[lane] = pk(h0, h1);
   }
   const float bias = (a.delta_bias && active) ? a.delta_bias[d] : 0.f;
@@ -162,9 +166,9 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
         step_scalars<BF>(ru, rd, bias2, a.softplus, dtg, dug);
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-          dt2[4 * g + p] = dtg[p];
-          du2[4 * g + p] = dug[p];
           const f2 up = L::pair(ru, p);
+          dt2[4 * g + p] = dtg[p];
+          du2[4 * g + p] = ZOH ? up : dug[p];  // the hold weight multiplies u itself
           y2[8 * g + 2 * p] = pk(Dd * lo(up), 0.f);
           y2[8 * g + 2 * p + 1] = pk(Dd * hi(up), 0.f);
         }
@@ -183,19 +187,23 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
     for (int p = 1; p < kWT / 2; ++p) s2 = add2(s2, dt2[p]);
     const float sdt = lo(s2) + hi(s2);
 
+    // du2 holds dt * u (Euler) or u (zero-order hold).
     const f2* lB = tB + lane * (kWT + 1);
     const f2* lC = tC + lane * (kWT + 1);
 #pragma unroll 1
     for (int q = 0; q < NP; ++q) {
       const f2 A2 = sA[q];
+      const f2 iA = sIA[q];
       f2 e[kWT], bb[kWT];
       f2 agg = pk(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < kWT; ++i) {
         const float dt = (i & 1) ? hi(dt2[i >> 1]) : lo(dt2[i >> 1]);
         const float du = (i & 1) ? hi(du2[i >> 1]) : lo(du2[i >> 1]);
-        e[i] = ex2x2(mul2(pk(dt, dt), A2));
-        bb[i] = mul2(pk(du, du), lB[q * kWRow + i]);
+        const f2 arg = mul2(pk(dt, dt), A2);
+        e[i] = ex2x2(arg);
+        if constexpr (ZOH) bb[i] = mul2(hold2(arg, e[i], pk(dt, dt), iA), mul2(pk(du, du), lB[q * kWRow + i]));
+        else bb[i] = mul2(pk(du, du), lB[q * kWRow + i]);
         agg = fma2(e[i], agg, bb[i]);
       }
       // Inclusive scan over lanes of (decay product, zero-start end state).
@@ -255,10 +263,10 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
   }
 }
 
-template <int NT, bool BF, bool HAS_Z>
+template <int NT, bool BF, bool HAS_Z, bool ZOH>
 int go_warp(const ScanArgs& a, cudaStream_t s) {
   constexpr int bytes = WarpLayout<NT, BF>::kBytes;
-  auto k = scan_warp_kernel<NT, BF, HAS_Z>;
+  auto k = scan_warp_kernel<NT, BF, HAS_Z, ZOH>;
   const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return (int)e;
   const dim3 grid((unsigned)((a.dim + kWW - 1) / kWW), (unsigned)a.batch);
@@ -266,18 +274,23 @@ int go_warp(const ScanArgs& a, cudaStream_t s) {
   return 0;
 }
 
+template <bool BF, bool HAS_Z, bool ZOH>
+int dispatch_nt(const ScanArgs& a, cudaStream_t s) {
+  if (a.dstate <= 4) return go_warp<4, BF, HAS_Z, ZOH>(a, s);
+  if (a.dstate <= 8) return go_warp<8, BF, HAS_Z, ZOH>(a, s);
+  return go_warp<16, BF, HAS_Z, ZOH>(a, s);
+}
+
 template <bool BF, bool HAS_Z>
 int dispatch_warp(const ScanArgs& a, cudaStream_t s) {
-  if (a.dstate <= 4) return go_warp<4, BF, HAS_Z>(a, s);
-  if (a.dstate <= 8) return go_warp<8, BF, HAS_Z>(a, s);
-  return go_warp<16, BF, HAS_Z>(a, s);
+  return a.zoh ? dispatch_nt<BF, HAS_Z, true>(a, s) : dispatch_nt<BF, HAS_Z, false>(a, s);
 }
 
 }  // namespace
 
 bool warp_scan_available(const ScanArgs& a, bool bf16) {
   (void)bf16;
-  return !a.zoh && a.dstate >= 1 && a.dstate <= 16 && a.seqlen % 8 == 0 && a.vec && a.vec_bc;
+  return a.dstate >= 1 && a.dstate <= 16 && a.seqlen % 8 == 0 && a.vec && a.vec_bc;
 }
 
 int launch_scan_warp(const ScanArgs& a, bool bf16, bool has_z, cudaStream_t s) {

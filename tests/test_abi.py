@@ -91,10 +91,11 @@ def test_schedule_flags():
     # every case fails on the host before any launch
     both = ss.FLAG_SCHED_THREAD | ss.FLAG_SCHED_WARP
     assert _fwd(_flagged(both)) == ss.SS_EINVAL
-    # the warp schedule refuses what it cannot run: N > 16, L % 8 != 0, the zero-order hold
+    # the warp schedule refuses what it cannot run: N > 16, L % 8 != 0 (either input weight)
     assert _fwd(_flagged(ss.FLAG_SCHED_WARP, n=17)) == ss.SS_EINVAL
     assert _fwd(_flagged(ss.FLAG_SCHED_WARP, L=12)) == ss.SS_EINVAL
-    assert _fwd(_flagged(ss.FLAG_SCHED_WARP | ss.FLAG_ZOH)) == ss.SS_EINVAL
+    assert _fwd(_flagged(ss.FLAG_SCHED_WARP | ss.FLAG_ZOH, n=17)) == ss.SS_EINVAL
+    assert _fwd(_flagged(ss.FLAG_SCHED_WARP | ss.FLAG_ZOH, L=20)) == ss.SS_EINVAL
     # schedule flags belong to ss_scan_fwd only
     assert _chunked(_flagged(ss.FLAG_SCHED_THREAD)) == ss.SS_EINVAL
     assert _chunked(_flagged(ss.FLAG_SCHED_WARP)) == ss.SS_EINVAL

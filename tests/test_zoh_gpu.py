@@ -1,6 +1,7 @@
 """GPU parity of the zero-order-hold discretisation (SS_FLAG_ZOH) against the
-fp64 oracle, on every path: the TMA and ring forward scans, the chunked scan
-(TMA and ring local passes), and the decode step; plus Theorem 1 on the GPU."""
+fp64 oracle, on every path: the forward scan under both schedules (one thread per
+channel with TMA or ring staging, one warp per channel), the chunked scan (TMA and
+ring local passes), and the decode step; plus Theorem 1 on the GPU."""
 from __future__ import annotations
 
 import math
@@ -43,17 +44,24 @@ CASES = [
     (2, 1, 130, 16, 1024, torch.bfloat16, True),
     (3, 2, 40, 5, 77, torch.float32, False),      # ring path (L % 8 != 0)
     (4, 1, 64, 64, 96, torch.bfloat16, True),
+    (5, 1, 30, 5, 520, torch.float32, True),      # a last 512-step segment of 8 steps
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"s{c[0]}d{c[2]}n{c[3]}L{c[4]}" for c in CASES])
-@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("chunked", 64), ("chunked", 7)])
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("fwd_thread", None), ("fwd_warp", None), ("chunked", 64),
+                                        ("chunked", 7)])
 def test_zoh_scan_matches_oracle(case, impl, chunk):
     seed, batch, dim, N, L, dtype, spread = case
     p = problem(seed, batch, dim, N, L, dtype, spread)
     kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, return_last_state=True, zoh=True)
-    if impl == "fwd":
-        y, hl = ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, **kw)
+    if impl == "fwd_warp" and (L % 8 or N > 16):   # outside the warp schedule: refused on the host
+        with pytest.raises(ss.SSError) as ei:
+            ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, schedule="warp", **kw)
+        assert ei.value.status == ss.SS_EINVAL
+        return
+    if impl.startswith("fwd"):
+        y, hl = ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, schedule=impl[4:] or None, **kw)
     else:
         y, hl = ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, chunk_len=chunk, **kw)
     yr, hr = oracle_zoh(p.to("cpu"))
@@ -87,10 +95,11 @@ def test_zoh_theorem1_on_gpu():
     gate = torch.randn((1, dim, L), generator=g) * 2.0
     one = torch.ones((1, 1, L))
     A = -torch.ones((dim, 1))
-    for impl in ("fwd", "chunked"):
+    for impl in ("warp", "thread", "chunked"):
         kw = dict(return_last_state=True, zoh=True)
         args = (x.to(DEV), gate.to(DEV), A.to(DEV), one.to(DEV), one.to(DEV))
-        y, _ = ss.scan_fwd(*args, **kw) if impl == "fwd" else ss.scan_chunked(*args, chunk_len=64, **kw)
+        y, _ = ss.scan_chunked(*args, chunk_len=64, **kw) if impl == "chunked" else ss.scan_fwd(*args, schedule=impl,
+                                                                                               **kw)
         s = torch.sigmoid(gate.double())
         h = torch.zeros((1, dim), dtype=torch.float64)
         want = []
