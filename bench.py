@@ -472,10 +472,35 @@ def bench_e2e(ss, torch, p, y, hl, ws, world, elems, e2e_steps):
     a1.record(cur)
     torch.cuda.synchronize()
     e2e_ms = barrier_and_max(a0.elapsed_time(a1), world) / e2e_steps
+
+    # The host link alone: the same uploads and downloads on the same streams, no scan.
+    def copies(i):
+        b = i % 2
+        with torch.cuda.stream(s_up):
+            for k, v in hp.items():
+                dp[b][k].copy_(v, non_blocking=True)
+        with torch.cuda.stream(s_down):
+            hy[b].copy_(dy[b], non_blocking=True)
+            hh[b].copy_(dh[b], non_blocking=True)
+
+    copies(0)
+    torch.cuda.synchronize()
+    a0.record(cur)
+    for st in (s_up, s_down):
+        st.wait_event(a0)
+    for i in range(e2e_steps):
+        copies(i)
+    for st in (s_up, s_down):
+        cur.wait_stream(st)
+    a1.record(cur)
+    torch.cuda.synchronize()
+    link_ms = a0.elapsed_time(a1) / e2e_steps
     del dp, hp, hy, hh
     return {"value": elems * world / (e2e_ms * 1e-3), "unit": "elem/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
-            "pipelined": "upload / scan / download on three streams, two buffer sets"}
+            "pipelined": "upload / scan / download on three streams, two buffer sets",
+            "copies_only_ms_per_step": round(link_ms, 3),
+            "copies_only_gbs": round((h2d + d2h) / (link_ms * 1e-3) / 1e9, 1)}
 
 
 def time_scan_fwd(ss, torch, p, schedule, reps):
