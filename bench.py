@@ -15,12 +15,19 @@ whole job (every rank runs its own replica of the workload: the scan shards
 over independent channels and batch rows, with no collective on the data
 path).  The line also carries the roofline of the dominant kernel, the whole
 step's roofline, per-kernel times measured with CUDA events inside the timed
-region, the end-to-end figure through host buffers, clocks sampled during the
-timed region, a decode measurement, and the fp64 oracle timed on the host
-cores as a CPU baseline.
+region, the end-to-end figure through host buffers (and the same host copies
+timed without the scan), clocks sampled during the timed region, side
+measurements (decode, causal conv1d, the zero-order-hold step, ss_scan_fwd on
+the 130M-shaped layer and under both of its schedules, the backward pass), and
+the fp64 oracle timed on the host cores as a CPU baseline.
 
 `--impl reference` times the fp64 CPU oracle instead (the reference arm):
 same metric and workload, a bounded sample of channels per step.
+
+Profiling aids (one JSON object, no bench line): `--bwd-only` times only the
+backward pass, `--schedules-only` only ss_scan_fwd under its two schedules;
+`--dim` / `--seqlen` shrink the workload; `--no-decode`, `--no-e2e` and
+`--no-cpu-baseline` drop legs.
 """
 from __future__ import annotations
 
