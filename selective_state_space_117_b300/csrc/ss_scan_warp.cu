@@ -12,7 +12,7 @@
 //   3. runs the recurrence h = e h + b over its steps again from that state, with the
 //      decays still in registers, and accumulates the readout C_t h_t.
 // Each exp is computed once.  Segments follow one another in time; the state
-// leaving a segment (that of lane 31) enters the next one.  A block is kWW warps
+// leaving a segment (that of lane 31) enters the next one.  A block is up to kWW warps
 // (channels) of one batch row: the B and C rows of a segment, shared by those
 // channels, are copied into shared memory by cp.async one segment ahead and
 // widened to fp32 [pair][step] tiles once per block.
@@ -20,9 +20,12 @@
 // Supported: the Euler or the zero-order-hold input weight, N <= 16, seqlen % 8 == 0,
 // 16-byte aligned rows (u, delta, z, y, B, C).  Other shapes use the
 // one-thread-per-channel kernels.
+#include <algorithm>
+
 #include "ss_device.cuh"
 #include "ss_kernels.cuh"
 #include "ss_launch.h"
+#include "ss_occupancy.cuh"
 
 namespace ssk {
 
@@ -30,7 +33,7 @@ namespace {
 
 constexpr int kWT = 16;                 // steps per lane
 constexpr int kWS = 32 * kWT;           // steps per segment
-constexpr int kWW = 12;                 // warps (channels) per block
+constexpr int kWW = 12;                 // most warps (channels) per block
 constexpr int kWRow = kWS + kWS / kWT;  // tile row in f2 units: one pad slot per lane's steps
 
 // Shared memory: B and C tiles (f2 [NP][kWRow] each), the raw B/C rows of the next
@@ -81,7 +84,8 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
   f2* sH = reinterpret_cast<f2*>(sm + Lay::oH) + warp * NP;
 
   const int64_t b = blockIdx.y;
-  const int64_t d = (int64_t)blockIdx.x * kWW + warp;
+  const int ww = blockDim.x >> 5;        // warps (channels) in this block
+  const int64_t d = (int64_t)blockIdx.x * ww + warp;
   const bool active = d < a.dim;
   const int N = (int)a.dstate;
   const int64_t Lsq = a.seqlen;
@@ -114,7 +118,7 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
     constexpr int CPR = kWS * ES / 16;
     const int64_t t0 = (int64_t)sg * kWS;
     const int total = 2 * N * CPR;
-    for (int c = threadIdx.x; c < total; c += 32 * kWW) {
+    for (int c = threadIdx.x; c < total; c += blockDim.x) {
       const int which = c / (N * CPR);
       const int rem = c - which * N * CPR;
       const int n = rem / CPR, k = rem - n * CPR;
@@ -129,7 +133,7 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
   };
   // Widen the raw rows to the [pair][step] tiles; lane l's step i sits at l * (kWT + 1) + i.
   auto convert = [&]() {
-    for (int u = threadIdx.x; u < NP * kWS; u += 32 * kWW) {
+    for (int u = threadIdx.x; u < NP * kWS; u += blockDim.x) {
       const int q = u / kWS, t = u - q * kWS;
       const int n0 = 2 * q, n1 = 2 * q + 1;
       const unsigned char* rB = raw;
@@ -269,8 +273,14 @@ int go_warp(const ScanArgs& a, cudaStream_t s) {
   auto k = scan_warp_kernel<NT, BF, HAS_Z, ZOH>;
   const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return (int)e;
-  const dim3 grid((unsigned)((a.dim + kWW - 1) / kWW), (unsigned)a.batch);
-  k<<<grid, 32 * kWW, bytes, s>>>(a);
+  // Warps per block: 12, or fewer when there are too few channels to give every SM a
+  // block, so that the channels spread over all SMs instead of sharing a few.
+  DevInfo di;
+  const int64_t sms = device_info(&di) && di.sms > 0 ? di.sms : 148;
+  const int64_t ch = a.batch * a.dim;
+  const int ww = (int)std::min<int64_t>(kWW, std::max<int64_t>(1, (ch + sms - 1) / sms));
+  const dim3 grid((unsigned)((a.dim + ww - 1) / ww), (unsigned)a.batch);
+  k<<<grid, 32 * ww, bytes, s>>>(a);
   return 0;
 }
 
