@@ -37,8 +37,9 @@ constexpr int kWW = 12;                 // most warps (channels) per block
 constexpr int kWRow = kWS + kWS / kWT;  // tile row in f2 units: one pad slot per lane's steps
 
 // Shared memory: B and C tiles (f2 [NP][kWRow] each), the raw B/C rows of the next
-// segment ([B, C][NT][kWS] input elements), and per warp A * log2(e), 1 / A (zero where
-// A = 0) and the carried state as pairs.
+// segment ([B, C][NT][kWS] input elements), per warp A * log2(e), 1 / A (zero where
+// A = 0) and the carried state as pairs, and per warp its channel's u, delta and z
+// rows of a segment ([u, delta, z][kWS] input elements).
 template <int NT, bool BF>
 struct WarpLayout {
   static constexpr int NP = NT / 2;
@@ -50,7 +51,9 @@ struct WarpLayout {
   static constexpr int oA = oRaw + kRaw;
   static constexpr int oIA = oA + kWW * NP * 8;
   static constexpr int oH = oIA + kWW * NP * 8;
-  static constexpr int kBytes = oH + kWW * NP * 8;
+  static constexpr int oIn = oH + kWW * NP * 8;
+  static constexpr int kIn = 3 * kWS * ES;
+  static constexpr int kBytes = oIn + kWW * kIn;
 };
 
 // 16-byte asynchronous copy that reads src_bytes (16 or 0) and zero-fills the rest.
@@ -82,6 +85,7 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
   f2* sA = reinterpret_cast<f2*>(sm + Lay::oA) + warp * NP;
   f2* sIA = reinterpret_cast<f2*>(sm + Lay::oIA) + warp * NP;
   f2* sH = reinterpret_cast<f2*>(sm + Lay::oH) + warp * NP;
+  unsigned char* sIn = sm + Lay::oIn + warp * Lay::kIn;   // [u, delta, z][kWS] of this warp's channel
 
   const int64_t b = blockIdx.y;
   const int ww = blockDim.x >> 5;        // warps (channels) in this block
@@ -131,6 +135,22 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
     }
     cp_async_commit();
   };
+  // This warp's rows of arrays [first, first + count) (u, delta, z) for segment sg, by
+  // its own lanes; chunks past seqlen are zero-filled.
+  auto issue_in = [&](int sg, int first, int count) {
+    constexpr int CPR = kWS * ES / 16;
+    const int64_t t0 = (int64_t)sg * kWS;
+    for (int arr = first; arr < first + count; ++arr) {
+      const unsigned char* src =
+          static_cast<const unsigned char*>(arr == 0 ? a.u : arr == 1 ? a.delta : a.z) + row * ES;
+      for (int k = lane; k < CPR; k += 32) {
+        const int64_t t = t0 + (int64_t)k * (16 / ES);
+        const bool ok = t < Lsq;
+        cp_async16_fill(smem_addr(sIn + arr * kWS * ES + k * 16), ok ? src + t * ES : src, ok ? 16 : 0);
+      }
+    }
+    cp_async_commit();
+  };
   // Widen the raw rows to the [pair][step] tiles; lane l's step i sits at l * (kWT + 1) + i.
   auto convert = [&]() {
     for (int u = threadIdx.x; u < NP * kWS; u += blockDim.x) {
@@ -148,10 +168,13 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
     }
   };
 
-  if (nseg > 0) issue(0);
+  if (nseg > 0) {
+    issue(0);
+    if (active) issue_in(0, 0, HAS_Z ? 3 : 2);
+  }
   for (int sg = 0; sg < nseg; ++sg) {
     cp_async_wait<0>();
-    __syncthreads();  // raw rows of sg visible; every warp is done with the tiles of sg - 1
+    __syncthreads();  // rows of sg visible (B, C and each warp's inputs); tiles of sg - 1 done
     convert();
     __syncthreads();  // tiles of sg ready; the raw buffer is free
     if (sg + 1 < nseg) issue(sg + 1);
@@ -164,8 +187,9 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
 #pragma unroll
     for (int g = 0; g < kWT / 8; ++g) {
       if (8 * g < nv) {
-        const typename L::Raw8 ru = L::load8(a.u, row + tb + 8 * g);
-        const typename L::Raw8 rd = L::load8(a.delta, row + tb + 8 * g);
+        const unsigned off = (unsigned)((lane * kWT + 8 * g) * ES);
+        const typename L::Raw8 ru = L::from_smem(smem_addr(sIn + off), 16);
+        const typename L::Raw8 rd = L::from_smem(smem_addr(sIn + kWS * ES + off), 16);
         f2 dtg[4], dug[4];
         step_scalars<BF>(ru, rd, bias2, a.softplus, dtg, dug);
 #pragma unroll
@@ -186,6 +210,8 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
         }
       }
     }
+    __syncwarp();  // every lane has read u and delta of sg: refill them with sg + 1
+    if (sg + 1 < nseg) issue_in(sg + 1, 0, 2);
     f2 s2 = dt2[0];
 #pragma unroll
     for (int p = 1; p < kWT / 2; ++p) s2 = add2(s2, dt2[p]);
@@ -242,7 +268,8 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
     for (int g = 0; g < kWT / 8; ++g) {
       if (8 * g < nv) {
         if constexpr (HAS_Z) {
-          const typename L::Raw8 rz = L::load8(a.z, row + tb + 8 * g);
+          const typename L::Raw8 rz =
+              L::from_smem(smem_addr(sIn + 2 * kWS * ES + (unsigned)((lane * kWT + 8 * g) * ES)), 16);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             const f2 s = silu2(L::pair(rz, p));
@@ -254,6 +281,10 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
         yp[0] = make_float4(yo[8 * g], yo[8 * g + 1], yo[8 * g + 2], yo[8 * g + 3]);
         yp[1] = make_float4(yo[8 * g + 4], yo[8 * g + 5], yo[8 * g + 6], yo[8 * g + 7]);
       }
+    }
+    if constexpr (HAS_Z) {
+      __syncwarp();  // every lane has read z of sg
+      if (sg + 1 < nseg) issue_in(sg + 1, 2, 1);
     }
   }
 
