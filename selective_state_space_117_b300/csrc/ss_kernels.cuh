@@ -127,7 +127,12 @@ __device__ __forceinline__ f2 step_pair(f2 h, f2 A2, f2 iA2, f2 dtp, f2 dup, f2 
   return fma2(e, h, mul2(dup, Bp));
 }
 
-template <int NT, bool BF, bool HAS_Z, bool ZOH>
+// The readout sum over state pairs runs as one chain of fused multiply-adds, or with
+// TWO_CHAINS as two (even and odd pairs) added at the end: one more instruction per
+// step, half the chain's latency.  Two chains pay where few warps share an SM (the
+// full-sequence scan of a layer with few channels per SM), one where many do (the
+// chunked fix-up pass).
+template <int NT, bool BF, bool HAS_Z, bool ZOH, bool TWO_CHAINS = false>
 __device__ __forceinline__ void scan_group(const typename In<BF>::Raw8& cu, const typename In<BF>::Raw8& rd,
                                            const typename In<BF>::Raw8& cz, f2 bias2, f2 D2, int softplus,
                                            const f2 (&A2)[NT / 2], const f2 (&iA2)[NT / 2], f2 (&h)[NT / 2],
@@ -150,7 +155,7 @@ __device__ __forceinline__ void scan_group(const typename In<BF>::Raw8& cu, cons
     const f2 dtp = pk(dt, dt), dup = pk(du, du);
     const float* rb = cB + j * NT;
     const float* rc = cC + j * NT;
-    f2 acc;
+    f2 acc, acc1;
 #pragma unroll
     for (int q = 0; q < NP; q += 2) {
       const float4 bv = *reinterpret_cast<const float4*>(rb + 2 * q);
@@ -158,8 +163,10 @@ __device__ __forceinline__ void scan_group(const typename In<BF>::Raw8& cu, cons
       h[q] = step_pair<ZOH>(h[q], A2[q], iA2[q], dtp, dup, upp, pk(bv.x, bv.y));
       acc = q == 0 ? mul2(pk(cv.x, cv.y), h[q]) : fma2(pk(cv.x, cv.y), h[q], acc);
       h[q + 1] = step_pair<ZOH>(h[q + 1], A2[q + 1], iA2[q + 1], dtp, dup, upp, pk(bv.z, bv.w));
-      acc = fma2(pk(cv.z, cv.w), h[q + 1], acc);
+      if constexpr (TWO_CHAINS) acc1 = q == 0 ? mul2(pk(cv.z, cv.w), h[q + 1]) : fma2(pk(cv.z, cv.w), h[q + 1], acc1);
+      else acc = fma2(pk(cv.z, cv.w), h[q + 1], acc);
     }
+    if constexpr (TWO_CHAINS) acc = add2(acc, acc1);
     yo[j] = lo(acc) + hi(acc);
   }
 #pragma unroll
@@ -256,8 +263,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(c
           typename L::Raw8 cz{};
           if (HAS_Z) cz = ring.get(gi, NA - 1);
           f2 y2[4];
-          scan_group<NT, BF, HAS_Z, ZOH>(cu, rd, cz, bias2, D2, a.softplus, A2, iA2, h, cB + g * NT, cC + g * NT,
-                                         y2);
+          scan_group<NT, BF, HAS_Z, ZOH, MODE == kFull>(cu, rd, cz, bias2, D2, a.softplus, A2, iA2, h, cB + g * NT,
+                                                        cC + g * NT, y2);
           float4* qy = reinterpret_cast<float4*>(a.y + w.row + t);
           qy[0] = make_float4(lo(y2[0]), hi(y2[0]), lo(y2[1]), hi(y2[1]));
           qy[1] = make_float4(lo(y2[2]), hi(y2[2]), lo(y2[3]), hi(y2[3]));

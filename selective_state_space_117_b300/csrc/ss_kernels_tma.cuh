@@ -169,8 +169,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
         typename L::Raw8 cz{};
         if (HAS_Z) cz = tile_row8<BF, Lay::RB>(slot + 2 * Lay::kIn, tid, g);
         f2 y2[4];
-        scan_group<NT, BF, HAS_Z, ZOH>(cu, rd, cz, bias2, D2, a.softplus, A2, iA2, h, cB + g * kGroup * NT,
-                                       cC + g * kGroup * NT, y2);
+        scan_group<NT, BF, HAS_Z, ZOH, MODE == kFull>(cu, rd, cz, bias2, D2, a.softplus, A2, iA2, h,
+                                                      cB + g * kGroup * NT, cC + g * kGroup * NT, y2);
         sts16(ybase + swz<Lay::YB>(tid, 2 * g), make_float4(lo(y2[0]), hi(y2[0]), lo(y2[1]), hi(y2[1])));
         sts16(ybase + swz<Lay::YB>(tid, 2 * g + 1), make_float4(lo(y2[2]), hi(y2[2]), lo(y2[3]), hi(y2[3])));
       }
