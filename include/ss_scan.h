@@ -112,8 +112,8 @@ typedef struct {
  * "The same layer has two faces", multigrid.ai, section "Why a linear
  * recurrence can be trained in parallel").  One pass over L per channel with
  * the state kept on chip; the (batch, L, dim, N) expanded state is never
- * written ("never materializing the large expanded state", ai-trend.me,
- * "How it works"; "Kernel fusion", azimuth.plus).
+ * written to device memory (ai-trend.me, "How it works"; azimuth.plus,
+ * "Kernel fusion").
  *   u, delta, B, C, A, y   required (unless the corresponding size is 0)
  *   D, z, delta_bias       optional (NULL = absent: D = 0, no gate, bias 0)
  *   softplus_flag          nonzero: dt = softplus(delta + bias); zero: dt = delta + bias
@@ -187,10 +187,10 @@ int ss_scan_chunked_h0(const ss_dims* dims, const float* h0, const void* u, cons
                        size_t workspace_bytes, ss_stream_t stream);
 
 /*
- * One decode step on a persistent state (the recurrence face: "each new token
- * only updates a fixed-size state", mernstackdev.com, FAQ; the state of
- * shape (batch, dim, N) is the fixed-size memory of "The state, in bytes",
- * multigrid.ai).  dims->seqlen is ignored.
+ * One decode step on a persistent state (the recurrence face: a token costs
+ * one update of a state whose size does not grow with the sequence;
+ * mernstackdev.com, FAQ, and multigrid.ai, "The state, in bytes", which sizes
+ * that (batch, dim, N) state).  dims->seqlen is ignored.
  *   state   (batch, dim, dstate) fp32, read and updated in place
  *   u, delta, z, y : (batch, dim)      B, C : (batch, dstate)
  * Other arguments as ss_scan_fwd.  Running L steps from a zero state gives
