@@ -287,6 +287,35 @@ def test_warp_schedule_shapes(case):
     compare(p, y, hl, "warp")
 
 
+def _random_warp_cases(n=12, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        cases.append((300 + i, int(rng.integers(1, 4)), int(rng.integers(1, 41)), int(rng.integers(1, 17)),
+                      8 * int(rng.integers(1, 201)), torch.bfloat16 if rng.random() < 0.5 else torch.float32,
+                      bool(rng.random() < 0.7), bool(rng.random() < 0.7), bool(rng.random() < 0.7),
+                      bool(rng.random() < 0.8)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_warp_cases(), ids=lambda c: f"s{c[0]}b{c[1]}d{c[2]}n{c[3]}L{c[4]}")
+def test_warp_schedule_random_shapes(case):
+    """Seeded random shapes (batch 1-3, D 1-40, N 1-16, L a multiple of 8 up to 1600, either
+    dtype, each optional input on or off) under the warp schedule, with and without h0."""
+    seed, batch, dim, N, L, dt, gate, wd, wb, sp = case
+    p = custom(seed, batch, dim, N, L, dt, gate, wd, wb, sp)
+    y, hl = run(p, "fwd_warp")
+    compare(p, y, hl, "warp/random")
+    g = torch.Generator().manual_seed(seed + 7)
+    h0 = torch.randn((batch, dim, N), generator=g)
+    y, hl = ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, D=p.D, z=p.z, delta_bias=p.delta_bias, softplus=p.softplus,
+                        return_last_state=True, h0=h0.to(DEV), schedule="warp")
+    yr, hr = oracle_scan(p.to("cpu"), h0=h0.double().numpy().reshape(batch * dim, N))
+    bf = dt == torch.bfloat16
+    check(host(y).reshape(batch * dim, L), yr, bf, "warp/random h0 y")
+    check(host(hl).reshape(batch * dim, N), hr, bf, "warp/random h0 last_state")
+
+
 def test_warp_schedule_refuses_unaligned_rows():
     p = custom(68, 1, 4, 16, 64, torch.bfloat16)
     u = torch.empty(p.u.numel() + 1, dtype=p.u.dtype, device=DEV)[1:].view_as(p.u)

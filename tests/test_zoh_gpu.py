@@ -70,6 +70,22 @@ def test_zoh_scan_matches_oracle(case, impl, chunk):
     check(host(hl).reshape(batch * dim, N), hr, bf, f"zoh/{impl} state")
 
 
+@pytest.mark.parametrize("impl", ["warp", "thread", "chunked"])
+def test_zoh_initial_state(impl):
+    """The zero-order hold started from a given state h0, on every forward path."""
+    p = problem(31, 2, 24, 16, 264, torch.bfloat16, spread=True)
+    g = torch.Generator().manual_seed(32)
+    h0 = torch.randn((2, 24, 16), generator=g)
+    kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, return_last_state=True, zoh=True, h0=h0.to(DEV))
+    if impl == "chunked":
+        y, hl = ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, chunk_len=48, **kw)
+    else:
+        y, hl = ss.scan_fwd(p.u, p.delta, p.A, p.B, p.C, schedule=impl, **kw)
+    yr, hr = oracle_zoh(p.to("cpu"), h0=h0.double().numpy().reshape(48, 16))
+    check(host(y).reshape(48, 264), yr, True, f"zoh h0/{impl} y")
+    check(host(hl).reshape(48, 16), hr, True, f"zoh h0/{impl} state")
+
+
 @pytest.mark.parametrize("N", [1, 8, 16, 40])
 def test_zoh_decode_matches_oracle(N):
     p = problem(20 + N, 3, 70, N, 12, torch.float32, spread=N > 1)
