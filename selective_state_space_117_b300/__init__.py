@@ -21,7 +21,7 @@ from typing import Optional
 import torch
 
 __all__ = ["scan_fwd", "scan_chunked", "scan_bwd", "bwd_workspace_bytes", "state_update", "causal_conv1d", "chunked_workspace_bytes", "device_status",
-           "selftest_wait_timeout",
+           "selftest_wait_timeout", "selective_scan",
            "SSError",
            "library_path",
            "F32", "BF16", "MAX_DSTATE", "LAUNCHES"]
@@ -279,6 +279,50 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, 
                            _ptr(workspace), workspace.numel(), _stream(dev, stream))
     _check(st, "ss_scan_bwd")
     return out
+
+
+class _SelectiveScan(torch.autograd.Function):
+    """Forward: ss_scan_fwd (or ss_scan_chunked when chunk_len is given); backward:
+    ss_scan_bwd with the cotangents of y and of the final state.  Gradients come back
+    in fp32 from the library and are cast to each input's dtype."""
+
+    @staticmethod
+    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, softplus, zoh, chunk_len):
+        kw = dict(D=D, z=z, delta_bias=delta_bias, softplus=softplus, zoh=zoh, return_last_state=True)
+        if chunk_len is None:
+            y, last = scan_fwd(u, delta, A, B, C, **kw)
+        else:
+            y, last = scan_chunked(u, delta, A, B, C, chunk_len=chunk_len, **kw)
+        ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias)
+        ctx.softplus, ctx.zoh = softplus, zoh
+        ctx.set_materialize_grads(False)
+        return y, last
+
+    @staticmethod
+    def backward(ctx, dy, dlast):
+        u, delta, A, B, C, D, z, delta_bias = ctx.saved_tensors
+        if dy is None:
+            dy = torch.zeros(u.shape, dtype=torch.float32, device=u.device)
+        dy = dy.to(torch.float32).contiguous()
+        if dlast is not None:
+            dlast = dlast.to(torch.float32).contiguous()
+        need = ctx.needs_input_grad
+        g = scan_bwd(u, delta, A, B, C, D, z, delta_bias, ctx.softplus, dy=dy, dlast=dlast,
+                     want_dD=D is not None and need[5], want_dbias=delta_bias is not None and need[7],
+                     want_dh0=False, zoh=ctx.zoh)
+        cast = lambda t, like: None if t is None else t.to(like.dtype)
+        return (cast(g["du"], u), cast(g["ddelta"], delta), g["dA"], cast(g["dB"], B), cast(g["dC"], C),
+                g["dD"] if D is not None else None, cast(g["dz"], z) if z is not None else None,
+                g["ddelta_bias"] if delta_bias is not None else None, None, None, None)
+
+
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, zoh=False,
+                   chunk_len=None):
+    """Differentiable selective scan: returns (y, last_state) like ``scan_fwd(...,
+    return_last_state=True)`` (or ``scan_chunked`` with ``chunk_len``), and back-propagates
+    through ``scan_bwd`` into every input that requires grad.  Inputs as ``scan_fwd``;
+    they must be contiguous CUDA tensors."""
+    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, bool(softplus), bool(zoh), chunk_len)
 
 
 def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, y=None,
