@@ -80,3 +80,20 @@ def test_branch_a_conv_then_scan():
                          delta_bias=w_(p.delta_bias), dtype="bf16")
     check(host(y).reshape(batch * dim, L), yr, True, "branch A y")
     check(host(hl).reshape(batch * dim, N), hr, True, "branch A state")
+
+
+def test_conv1d_full_size_sampled():
+    """The benchmark's shape (batch 1, D 5120, L 65536, bf16 in and out, bias, SiLU) in its
+    launch configuration; sampled rows against the oracle."""
+    g = torch.Generator(device=DEV).manual_seed(5)
+    x = torch.randn((1, 5120, 65536), generator=g, device=DEV).to(torch.bfloat16)
+    w = torch.randn((5120, 4), generator=g, device=DEV) * 0.5
+    b = torch.randn((5120,), generator=g, device=DEV) * 0.1
+    out = ss.causal_conv1d(x, w, b)
+    ds = torch.tensor(list(range(13, 5120, 397)) + [5119], device=DEV)
+    xs = x.index_select(1, ds).cpu()
+    ref = oracle.conv1d(I.to_wire(xs), I.to_wire(w.index_select(0, ds).cpu()), I.to_wire(b.index_select(0, ds).cpu()),
+                        silu=True, dtype="bf16")
+    check_bf16_out(host(out.index_select(1, ds)), ref, "conv1d full size")
+    del x, out
+    torch.cuda.empty_cache()
