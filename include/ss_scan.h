@@ -243,7 +243,7 @@ int ss_scan_chunked_static(const ss_dims* dims, const void* u, const void* delta
  *   out[b,d,t] = silu(bias[d] + sum_{k=0..3} weight[d,k] * x[b,d,t-3+k])   (x = 0 before t = 0)
  *
  * weight[d,3] weighs the current step.  Its output is the scan's input u.
- *   dims         batch, dim, seqlen and in_dtype (dstate is ignored)
+ *   dims         batch, dim, seqlen and in_dtype (dstate is ignored; flags must be 0)
  *   x, out       (batch, dim, seqlen) of in_dtype (bf16 output is rounded to nearest even)
  *   weight       (dim, 4) fp32, 16-byte aligned;  bias (dim) fp32 or NULL
  *   silu_flag    nonzero: apply SiLU;  zero: the plain convolution

@@ -305,6 +305,7 @@ int ss_causal_conv1d(const ss_dims* dims, const void* x, const float* weight, co
   const ss_dims& d = *dims;
   if (d.in_dtype != SS_F32 && d.in_dtype != SS_BF16) return SS_EDTYPE;
   if (d.batch < 0 || d.dim < 0 || d.seqlen < 0) return SS_EINVAL;
+  if (d.flags != 0) return SS_EINVAL;   // no input weight or schedule to choose
   if (d.batch == 0 || d.dim == 0 || d.seqlen == 0) return SS_OK;
   if (!x || !weight || !out) return SS_EINVAL;
   const size_t es = in_size(d.in_dtype);

@@ -107,6 +107,22 @@ def test_schedule_flags():
                     torch.zeros(1, 4, 8), schedule="lanes")
 
 
+def _conv(dims, x=P, w=P, bias=None, out=P):
+    return ss.lib().ss_causal_conv1d(ctypes.byref(dims), x, w, bias, 1, out, None)
+
+
+def test_conv_validation():
+    # every case fails (or returns) on the host before any launch
+    assert _conv(_dims(dt=9)) == ss.SS_EDTYPE
+    assert _conv(_dims(L=-1)) == ss.SS_EINVAL
+    assert _conv(_flagged(ss.FLAG_ZOH)) == ss.SS_EINVAL          # no input weight to choose
+    assert _conv(_flagged(ss.FLAG_SCHED_WARP)) == ss.SS_EINVAL
+    assert _conv(_dims(), x=None) == ss.SS_EINVAL
+    assert _conv(_dims(), w=P + 4) == ss.SS_EALIGN               # taps must be 16-byte aligned
+    assert _conv(_dims(dt=ss.BF16), x=P + 1) == ss.SS_EALIGN
+    assert _conv(_dims(L=0), x=None, w=None, out=None) == ss.SS_OK
+
+
 def test_chunked_validation():
     assert _chunked(_dims(), chunk=0) == ss.SS_EINVAL
     assert _chunked(_dims(), ws=None) == ss.SS_EWORKSPACE

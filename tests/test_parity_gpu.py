@@ -383,6 +383,32 @@ def test_empty_and_degenerate(impl):
     compare(q, y, hl, f"N=0/{impl}")
 
 
+def test_degenerate_sizes_decode_conv_bwd():
+    """Zero batch rows, channels or steps on the decode step, the convolution and the backward
+    pass: no error, empty outputs, and the backward pass's gradients of an empty sum are zero."""
+    # decode: batch 0 or dim 0
+    for bsz, dim in ((0, 8), (3, 0)):
+        st = torch.empty((bsz, dim, 4), device=DEV)
+        v = torch.empty((bsz, dim), device=DEV)
+        bc = torch.empty((bsz, 4), device=DEV)
+        y = ss.state_update(st, v, v, torch.empty((dim, 4), device=DEV), bc, bc)
+        assert y.shape == (bsz, dim)
+    # convolution: L = 0 and dim = 0
+    for shape in ((2, 8, 0), (2, 0, 64)):
+        x = torch.empty(shape, device=DEV, dtype=torch.bfloat16)
+        out = ss.causal_conv1d(x, torch.zeros((shape[1], 4), device=DEV))
+        assert out.shape == shape
+    # backward with dim = 0: dB and dC (sums over channels) are exactly zero
+    bsz, N, L = 2, 4, 16
+    u = torch.empty((bsz, 0, L), device=DEV)
+    BC = torch.randn((bsz, N, L), device=DEV)
+    g = ss.scan_bwd(u, u, torch.empty((0, N), device=DEV), BC, BC, dy=torch.empty((bsz, 0, L), device=DEV))
+    torch.cuda.synchronize()
+    assert g["dB"].shape == (bsz, N, L) and torch.count_nonzero(g["dB"]).item() == 0
+    assert g["dC"].shape == (bsz, N, L) and torch.count_nonzero(g["dC"]).item() == 0
+    assert ss.device_status() == ss.SS_OK
+
+
 def test_two_faces_agree():
     """L decode steps from a zero state == scan_fwd == scan_chunked at several chunk lengths."""
     p = custom(51, 2, 70, 16, 129, torch.float32)
