@@ -287,42 +287,44 @@ class _SelectiveScan(torch.autograd.Function):
     in fp32 from the library and are cast to each input's dtype."""
 
     @staticmethod
-    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, softplus, zoh, chunk_len):
-        kw = dict(D=D, z=z, delta_bias=delta_bias, softplus=softplus, zoh=zoh, return_last_state=True)
+    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, h0, softplus, zoh, chunk_len):
+        kw = dict(D=D, z=z, delta_bias=delta_bias, softplus=softplus, zoh=zoh, return_last_state=True, h0=h0)
         if chunk_len is None:
             y, last = scan_fwd(u, delta, A, B, C, **kw)
         else:
             y, last = scan_chunked(u, delta, A, B, C, chunk_len=chunk_len, **kw)
-        ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias)
+        ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias, h0)
         ctx.softplus, ctx.zoh = softplus, zoh
         ctx.set_materialize_grads(False)
         return y, last
 
     @staticmethod
     def backward(ctx, dy, dlast):
-        u, delta, A, B, C, D, z, delta_bias = ctx.saved_tensors
+        u, delta, A, B, C, D, z, delta_bias, h0 = ctx.saved_tensors
         if dy is None:
             dy = torch.zeros(u.shape, dtype=torch.float32, device=u.device)
         dy = dy.to(torch.float32).contiguous()
         if dlast is not None:
             dlast = dlast.to(torch.float32).contiguous()
         need = ctx.needs_input_grad
-        g = scan_bwd(u, delta, A, B, C, D, z, delta_bias, ctx.softplus, dy=dy, dlast=dlast,
+        g = scan_bwd(u, delta, A, B, C, D, z, delta_bias, ctx.softplus, dy=dy, dlast=dlast, h0=h0,
                      want_dD=D is not None and need[5], want_dbias=delta_bias is not None and need[7],
-                     want_dh0=False, zoh=ctx.zoh)
+                     want_dh0=h0 is not None and need[8], zoh=ctx.zoh)
         cast = lambda t, like: None if t is None else t.to(like.dtype)
         return (cast(g["du"], u), cast(g["ddelta"], delta), g["dA"], cast(g["dB"], B), cast(g["dC"], C),
                 g["dD"] if D is not None else None, cast(g["dz"], z) if z is not None else None,
-                g["ddelta_bias"] if delta_bias is not None else None, None, None, None)
+                g["ddelta_bias"] if delta_bias is not None else None, g["dh0"] if h0 is not None else None,
+                None, None, None)
 
 
-def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, zoh=False,
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, h0=None, zoh=False,
                    chunk_len=None):
     """Differentiable selective scan: returns (y, last_state) like ``scan_fwd(...,
-    return_last_state=True)`` (or ``scan_chunked`` with ``chunk_len``), and back-propagates
-    through ``scan_bwd`` into every input that requires grad.  Inputs as ``scan_fwd``;
-    they must be contiguous CUDA tensors."""
-    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, bool(softplus), bool(zoh), chunk_len)
+    return_last_state=True)`` (or ``scan_chunked`` with ``chunk_len``), starting from ``h0``
+    (fp32 (batch, dim, N)) when given, and back-propagates through ``scan_bwd`` into every
+    input that requires grad, h0 included.  Inputs as ``scan_fwd``; they must be contiguous
+    CUDA tensors."""
+    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, h0, bool(softplus), bool(zoh), chunk_len)
 
 
 def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *, y=None,

@@ -249,16 +249,17 @@ def test_bwd_long_sequence_zoh_sampled():
 @pytest.mark.parametrize("chunk", [None, 64], ids=["fwd", "chunked64"])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 def test_selective_scan_autograd(chunk, dtype):
-    """ss.selective_scan through torch.autograd: the leaves' .grad of sum(dy y) + sum(dlast h_last)
-    against the oracle's adjoint.  Gradients of bf16 inputs come back rounded to bf16, so they are
+    """ss.selective_scan through torch.autograd, from an initial state h0: the leaves' .grad (h0's
+    included) of sum(dy y) + sum(dlast h_last) against the oracle's adjoint.  Gradients of bf16 inputs come back rounded to bf16, so they are
     held to twice bf16's rounding bound, 2^-8 of max(|ref|, rms(ref)); fp32 ones to TOL_GRAD."""
-    p, ct = make(501, 2, 40, 16, 136, dtype, h0=False)
+    p, ct = make(501, 2, 40, 16, 136, dtype, h0=True)
     names = ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")
     leaf = {k: getattr(p, k).detach().clone().requires_grad_(True) for k in names}
-    y, h = ss.selective_scan(*(leaf[k] for k in names), softplus=p.softplus, chunk_len=chunk)
+    leaf["h0"] = ct.h0.detach().clone().requires_grad_(True)
+    y, h = ss.selective_scan(*(leaf[k] for k in names), softplus=p.softplus, h0=leaf["h0"], chunk_len=chunk)
     ((y * ct.dy).sum() + (h * ct.dlast).sum()).backward()
     r = oracle_grads(p, ct)
-    for k, key in zip(names, ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")):
+    for k, key in zip(names + ("h0",), ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias", "dh0")):
         got = leaf[k].grad
         assert got is not None and got.dtype == leaf[k].dtype, k
         tol = 2.0 ** -8 if got.dtype == torch.bfloat16 else TOL_GRAD
