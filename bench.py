@@ -18,16 +18,19 @@ step's roofline, per-kernel times measured with CUDA events inside the timed
 region, the end-to-end figure through host buffers (and the same host copies
 timed without the scan), clocks sampled during the timed region, side
 measurements (decode, causal conv1d, the zero-order-hold step, ss_scan_fwd on
-the 130M-shaped layer and under both of its schedules, the backward pass), and
-the fp64 oracle timed on the host cores as a CPU baseline.
+the 130M-shaped layer and under both of its schedules, the backward pass), the
+ex2 throughput of the running GPU (the SFU peak that the exponential roofline
+divides by, `sfu`), and the fp64 oracle timed on the host cores as a CPU
+baseline, whose sample channels are also compared with the bench's own outputs
+(`cpu_baseline.parity_sample`).
 
 `--impl reference` times the fp64 CPU oracle instead (the reference arm):
 same metric and workload, a bounded sample of channels per step.
 
 Profiling aids (one JSON object, no bench line): `--bwd-only` times only the
 backward pass, `--schedules-only` only ss_scan_fwd under its two schedules;
-`--dim` / `--seqlen` shrink the workload; `--no-decode`, `--no-e2e` and
-`--no-cpu-baseline` drop legs.
+`--dim` / `--seqlen` shrink the workload; `--no-decode`, `--no-e2e`,
+`--no-sfu` and `--no-cpu-baseline` drop legs.
 """
 from __future__ import annotations
 
@@ -47,7 +50,10 @@ WORKLOAD = "mamba2p8b_long_bf16"
 CHUNK = 2048
 SMS = 148
 SM_MAX_MHZ = 2032.0
-EX2_PER_CLK_PER_SM = 32          # MUFU.EX2 issue rate of sm_103 (31.85/clk/SM measured on this machine's B300)
+# Fallback only, used when the ex2 throughput leg below cannot run: 32 MUFU.EX2 lanes per
+# clock per SM, the rate ncu's pipe_xu utilisation implies for the scan kernels.  The bench
+# line's SFU peak is normally the rate that leg measures on the running GPU.
+EX2_PER_CLK_PER_SM_FALLBACK = 32
 
 
 # ----------------------------------------------------------------- measured DRAM traffic
@@ -103,15 +109,52 @@ def workload_counts(batch, dim, dstate, seqlen, in_bytes=2, gate=True):
     return elems, byts, exps
 
 
-def peaks():
+def peaks(sfu=None):
+    """HBM peak from MEASURED_PEAKS.json; the SFU (ex2) peak from the throughput leg when it
+    ran (`sfu`), else the fallback rate at the maximum SM clock."""
     path = os.path.join(HERE, "MEASURED_PEAKS.json")
     hbm, src = 6400.0, "fallback"
     if os.path.exists(path):
         with open(path) as f:
             pk = json.load(f)
         hbm, src = float(pk.get("hbm_gbs", hbm)), "measured"
-    sfu = SMS * EX2_PER_CLK_PER_SM * SM_MAX_MHZ * 1e6 / 1e12     # Texp/s at the maximum SM clock
-    return {"hbm_gbs": hbm, "hbm_src": src, "sfu_texps": sfu}
+    if sfu and sfu.get("texps"):
+        return {"hbm_gbs": hbm, "hbm_src": src, "sfu_texps": sfu["texps"],
+                "sfu_src": "measured: ex2.approx.ftz.f32 throughput loop (ss_measure_ex2), best of "
+                           f"{sfu['launches']} launches at {sfu['sm_mhz']} MHz"}
+    texps = SMS * EX2_PER_CLK_PER_SM_FALLBACK * SM_MAX_MHZ * 1e6 / 1e12
+    return {"hbm_gbs": hbm, "hbm_src": src, "sfu_texps": texps,
+            "sfu_src": f"fallback: {SMS} SMs x {EX2_PER_CLK_PER_SM_FALLBACK}/clk/SM x {SM_MAX_MHZ:.0f} MHz"}
+
+
+def measure_sfu(ss, torch, launches=20, iters=4096):
+    """The ex2.approx.ftz.f32 throughput of the running GPU (ss_measure_ex2): 8 blocks of 256
+    threads per SM, each thread 8 independent chains; every launch timed with CUDA events on
+    the current stream; the best launch gives the peak.  Clocks are sampled meanwhile so the
+    rate can also be stated per clock and per SM."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    blocks = 8 * sms
+    sink = torch.empty((blocks,), dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        n = ss.measure_ex2(blocks, iters, sink=sink)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    with ClockSampler(device_index_for_smi(torch)) as clk:
+        time.sleep(0.2)
+        for e0, e1 in ev:
+            e0.record()
+            ss.measure_ex2(blocks, iters, sink=sink)
+            e1.record()
+        torch.cuda.synchronize()
+    ms = sorted(e0.elapsed_time(e1) for e0, e1 in ev)
+    best, med = ms[0], ms[len(ms) // 2]
+    c = clk.summary()
+    mhz = c["sm_mhz"] or SM_MAX_MHZ
+    texps = n / (best * 1e-3) / 1e12
+    return {"texps": round(texps, 4), "texps_median": round(n / (med * 1e-3) / 1e12, 4),
+            "per_clk_per_sm": round(texps * 1e12 / (sms * mhz * 1e6), 3), "sm_mhz": mhz, "sms": sms,
+            "ex2_per_launch": n, "ms_best": round(best, 4), "launches": launches,
+            "clock_reasons": c["reasons"], "gpu_launches": launches + 3}
 
 
 def roofline_terms(byts, exps, ms, pk):
@@ -232,16 +275,38 @@ def oracle_sample(p, nchan):
                 B=I.to_wire(p.B), C=I.to_wire(p.C))
 
 
-def time_oracle(sample, threads):
+def time_oracle(sample, threads, out=None):
+    """Seconds the oracle takes on the sample; its (y, last_state) go into `out` when given."""
     import oracle
     t0 = time.perf_counter()
-    oracle.scan(sample["u"], sample["delta"], sample["A"], sample["B"], sample["C"], D=sample["D"], z=sample["z"],
-                delta_bias=sample["delta_bias"], softplus=True, dtype="bf16", nthreads=threads)
-    return time.perf_counter() - t0
+    r = oracle.scan(sample["u"], sample["delta"], sample["A"], sample["B"], sample["C"], D=sample["D"],
+                    z=sample["z"], delta_bias=sample["delta_bias"], softplus=True, dtype="bf16", nthreads=threads)
+    dt = time.perf_counter() - t0
+    if out is not None:
+        out["y"], out["h"] = r
+    return dt
 
 
-def cpu_baseline(p, budget_s=20.0):
-    """The oracle on the host cores over a bounded channel sample (about `budget_s` of wall time)."""
+def parity_of_sample(res, y, hl, nchan):
+    """The bench's own outputs on the oracle's sample channels (batch row 0), under the bf16 rule
+    max |err| <= 2e-3 rms(ref), with the unfloored relative error over |ref| >= 1e-2 rms."""
+    import numpy as np
+    out = {"channels": nchan, "rule": "max|err|/rms(ref) <= 2e-3 (bf16 inputs)"}
+    for key, got, ref in (("y", y[0, :nchan].float().cpu().numpy(), res["y"]),
+                          ("last_state", hl[0, :nchan].float().cpu().numpy(), res["h"])):
+        ref = np.asarray(ref, dtype=np.float64).reshape(got.shape)
+        err = np.abs(got.astype(np.float64) - ref)
+        r = float(np.sqrt(np.mean(ref * ref)))
+        keep = np.abs(ref) >= 1e-2 * r
+        out[key] = {"max_abs_err": float(err.max()), "rms_ref": r, "max_err_over_rms": float(err.max() / r),
+                    "rel_unfloored": float(np.max(err[keep] / np.abs(ref[keep]))) if keep.any() else 0.0}
+    return out
+
+
+def cpu_baseline(p, budget_s=20.0, y=None, hl=None):
+    """The oracle on the host cores over a bounded channel sample (about `budget_s` of wall time).
+    With the GPU's y and final state of the same workload, the sample's outputs are also compared
+    with them (`parity_sample`)."""
     import oracle
     oracle.build()
     threads = host_threads()
@@ -251,7 +316,8 @@ def cpu_baseline(p, budget_s=20.0):
     nchan = int(min(p.dim, max(threads, budget_s / max(per_chan, 1e-9))))
     nchan = min(p.dim, max(threads, (nchan // threads) * threads))
     sample = oracle_sample(p, nchan)
-    dt = time_oracle(sample, threads)
+    res = {}
+    dt = time_oracle(sample, threads, res)
     elems = p.batch * nchan * L
     # one core, on a few channels; per-channel work is the same for every channel, so the
     # whole workload's single-core time is this scaled linearly
@@ -262,7 +328,8 @@ def cpu_baseline(p, budget_s=20.0):
             "sample": f"{nchan} of {p.dim} channels x L={L} (fp64 C oracle, OpenMP over channels), {dt:.1f} s",
             "single_core": {"value": one, "unit": "elem/s", "sample": f"{n1} channels x L={L} on 1 thread, {t1:.2f} s",
                             "scaled_workload_s": round(p.batch * p.dim * L / one, 1),
-                            "note": "scaled linearly from the sample to all channels"}}
+                            "note": "scaled linearly from the sample to all channels"},
+            **({"parity_sample": parity_of_sample(res, y, hl, nchan)} if y is not None else {})}
 
 
 # ----------------------------------------------------------------- the reference arm
@@ -312,7 +379,13 @@ def run_ours(args):
     import selective_state_space_117_b300 as ss
     from selective_state_space_117_b300 import inputs as I
 
-    pk = peaks()
+    sfu = None
+    if not args.no_sfu:
+        try:
+            sfu = measure_sfu(ss, torch)
+        except Exception as e:   # the line then states the fallback peak it used
+            sfu = {"error": str(e)}
+    pk = peaks(sfu)
     if args.schedules_only:            # the ss_scan_fwd schedule comparison alone (for profiling it)
         if rank == 0:
             print(json.dumps({"fwd_schedules": bench_fwd_schedules(ss, I, torch)}), flush=True)
@@ -367,8 +440,7 @@ def run_ours(args):
                     for n, v in per_kernel.items()}
     roof_dom = roofline_terms(byts, exps, per_kernel[dominant], pk)
     roof_dom.update({"kernel": f"{dominant} pass", "traffic": traffic_for(dominant, L),
-                     "peak_src": ("derived: 148 SMs x 32 MUFU.EX2/clk/SM x 2032 MHz" if roof_dom["bound"] == "alu"
-                                  else pk["hbm_src"])})
+                     "peak_src": pk["sfu_src"] if roof_dom["bound"] == "alu" else pk["hbm_src"]})
     roof_step = roofline_terms(byts, exps, ms, pk)
 
     e2e = None if args.no_e2e else bench_e2e(ss, torch, p, y, hl, ws, world, elems, min(8, args.steps))
@@ -400,6 +472,7 @@ def run_ours(args):
         "gpu_launches": args.steps * len(phases),
         "clocks": clk.summary(),
         "peaks": pk,
+        "sfu": sfu,
     }
     if dec is not None:
         line["decode"] = dec
@@ -407,7 +480,9 @@ def run_ours(args):
         line["conv1d"] = conv
     line.update(side)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(p)
+        step()                       # y and the final state of the workload again (the side legs reused them)
+        torch.cuda.synchronize()
+        line["cpu_baseline"] = cpu_baseline(p, y=y, hl=hl)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -717,6 +792,7 @@ def main():
                     help="skip the side measurements (decode, conv1d, ZOH step, single-pass layer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sfu", action="store_true", help="skip the ex2 throughput leg (the SFU peak then falls back)")
     ap.add_argument("--dim", type=int, default=5120, help="channels (5120 = the workload; smaller only for profiling)")
     ap.add_argument("--seqlen", type=int, default=65536, help="steps (65536 = the workload; shorter only for profiling)")
     ap.add_argument("--bwd-only", action="store_true",

@@ -216,9 +216,12 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
  *     ss_scan_chunked_workspace_bytes(dims, chunk_len) exceeds
  *     SS_STATIC_WORKSPACE_BYTES (16 MiB: for example batch 1, dim 5120, N 16,
  *     L 65536 with chunk 2048 needs 11.2 MB).
- *   - The first call on a device looks up the array's device address with
- *     cudaGetSymbolAddress (under a lock, with that device current) and keeps
- *     it; make that first call before capturing any stream on that device.
+ *   - Every call made outside a stream capture looks up the array's device
+ *     address with cudaGetSymbolAddress (under a lock, with that device
+ *     current); a call made while its stream is being captured uses the address
+ *     of the last lookup on that device.  So make one call on a device before
+ *     capturing a stream there, and again after a cudaDeviceReset, which ends
+ *     the context the address belonged to.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
  *   - Every call, on every stream, uses the same array, which keeps the last
  *     call's contents (nothing in it needs clearing: each call writes every
@@ -320,6 +323,27 @@ int ss_device_status(int clear);
  * SS_ECUDA if the launch failed.  Nothing else is touched.
  */
 int ss_selftest_wait_timeout(ss_stream_t stream);
+
+/*
+ * Measurement of the exponential throughput that bounds the scan: every decay
+ * exp(dt * A) is one ex2.approx.ftz.f32 (MUFU.EX2) after A is scaled by log2(e),
+ * so the roofline's exponential term divides by this instruction's rate.  The
+ * pages state the method's exponential count, not the hardware's rate, so this
+ * call has no counterpart there; it measures the denominator on the GPU that
+ * runs the scan.
+ *
+ * Launches one kernel of `blocks` blocks on `stream`.  Each thread runs several
+ * independent chains of `iters` links x <- ex2(x) * (-1/2) (one MUFU.EX2 and one
+ * multiply per link), enough exponentials in flight that the MUFU pipe, not
+ * latency, bounds the loop.  *ex2_count (host pointer) receives the number of
+ * exponentials the launch computes; time the launch with events on `stream`
+ * and divide.  `sink` is a device float array of `blocks` entries that the
+ * kernel never actually writes (it keeps the chains live).  Use at least a few
+ * blocks per SM (for example 8 x the SM count) so that every SM is busy.
+ * Returns SS_EINVAL for blocks < 1, iters < 1 or a NULL pointer, SS_ECUDA if
+ * the launch failed.  Asynchronous.
+ */
+int ss_measure_ex2(int64_t blocks, int iters, float* sink, uint64_t* ex2_count, ss_stream_t stream);
 
 #ifdef __cplusplus
 }

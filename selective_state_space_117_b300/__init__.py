@@ -21,7 +21,7 @@ from typing import Optional
 import torch
 
 __all__ = ["scan_fwd", "scan_chunked", "scan_bwd", "bwd_workspace_bytes", "state_update", "causal_conv1d", "chunked_workspace_bytes", "device_status",
-           "selftest_wait_timeout", "selective_scan",
+           "selftest_wait_timeout", "selective_scan", "measure_ex2",
            "SSError",
            "library_path",
            "F32", "BF16", "MAX_DSTATE", "LAUNCHES"]
@@ -101,6 +101,8 @@ def lib():
         L.ss_scan_bwd.restype = ctypes.c_int
         L.ss_device_status.argtypes = [ctypes.c_int]
         L.ss_device_status.restype = ctypes.c_int
+        L.ss_measure_ex2.argtypes = [i64, ctypes.c_int, vp, ctypes.POINTER(ctypes.c_uint64), vp]
+        L.ss_measure_ex2.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -373,6 +375,19 @@ def selftest_wait_timeout(device=None, stream=None):
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(dev):
         _check(lib().ss_selftest_wait_timeout(_stream(dev, stream)), "ss_selftest_wait_timeout")
+
+
+def measure_ex2(blocks: int, iters: int, *, sink=None, stream=None) -> int:
+    """Launch the exp2 throughput kernel (ss_measure_ex2) on the current device and
+    stream; returns the number of ex2.approx.ftz.f32 it computes.  Time the launch with
+    CUDA events on the same stream."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if sink is None:
+        sink = torch.empty((blocks,), dtype=torch.float32, device=dev)
+    n = ctypes.c_uint64(0)
+    _check(lib().ss_measure_ex2(int(blocks), int(iters), sink.data_ptr(), ctypes.byref(n), _stream(dev, stream)),
+           "ss_measure_ex2")
+    return int(n.value)
 
 
 def causal_conv1d(x, weight, bias=None, silu=True, *, out=None, stream=None):

@@ -41,24 +41,49 @@ constexpr int64_t kWarpBelowChannelsZoh = 20480;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// The device status word: kernels whose bounded waits give up record it here
-// (one word per device, looked up once per device with cudaGetSymbolAddress).
-__device__ int g_dev_status;
+// Device address of one of this library's __device__ variables on the current device.
+// The address belongs to the device's current context: after cudaDeviceReset the next
+// context loads the module afresh, possibly elsewhere, so a cached address may be stale.
+// The address is therefore looked up again (a host-side table query) on every call whose
+// stream is not being captured, and the last address seen on each device is kept for
+// calls made during a capture, where a lookup that had to load the module would not be
+// allowed.  Returns nullptr (and the CUDA error in *err) when the lookup fails.
+constexpr int kMaxDevices = 256;
 
-constexpr int kMaxStatusDevices = 256;
-std::mutex g_status_mu;
-int* g_status_ptr[kMaxStatusDevices];
+struct SymbolCache {
+  std::mutex mu;
+  void* ptr[kMaxDevices] = {};
+};
 
-int* device_status_word() {
+void* symbol_on_device(SymbolCache& c, const void* symbol, cudaStream_t s, cudaError_t* err) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxStatusDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_status_mu);
-  if (g_status_ptr[dev] == nullptr) {
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { *err = e; return nullptr; }
+  if (dev < 0 || dev >= kMaxDevices) { *err = cudaErrorInvalidDevice; return nullptr; }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const bool capturing = cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone;
+  if (capturing) (void)cudaGetLastError();   // a refused query leaves a (non-sticky) error behind
+  std::lock_guard<std::mutex> lock(c.mu);
+  if (!capturing || c.ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dev_status) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<int*>(p);
+    e = cudaGetSymbolAddress(&p, symbol);
+    if (e != cudaSuccess) { *err = e; return nullptr; }
+    c.ptr[dev] = p;
   }
-  return g_status_ptr[dev];
+  return c.ptr[dev];
+}
+
+// The device status word: kernels whose bounded waits give up record it here.
+__device__ int g_dev_status;
+SymbolCache g_status_cache;
+
+// The word's address for the kernels about to be launched on stream s, or nullptr (the
+// kernels then skip recording a timeout; the CUDA error is left in *err when given).
+int* device_status_word(cudaStream_t s, cudaError_t* err = nullptr) {
+  cudaError_t e = cudaSuccess;
+  void* p = symbol_on_device(g_status_cache, (const void*)&g_dev_status, s, &e);
+  if (err) *err = e;
+  return static_cast<int*>(p);
 }
 
 // Shape, dtype and pointer checks shared by the two full-sequence entry points.
@@ -86,7 +111,8 @@ int check_scan(const ss_dims* dims, const void* u, const void* delta, const floa
 
 ssk::ScanArgs make_scan_args(const ss_dims& d, const void* u, const void* delta, const float* A, const void* B,
                              const void* C, const float* D, const void* z, const float* delta_bias,
-                             int softplus_flag, float* y, float* last_state, int64_t chunk_len) {
+                             int softplus_flag, float* y, float* last_state, int64_t chunk_len,
+                             cudaStream_t s) {
   ssk::ScanArgs a{};
   a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias;
   a.y = y; a.last_state = last_state;
@@ -103,7 +129,7 @@ ssk::ScanArgs make_scan_args(const ss_dims& d, const void* u, const void* delta,
   // B/C rows are staged in 8-step segments from tile starts that are multiples of 8 steps.
   const bool bc16 = (d.seqlen * (int64_t)es) % 16 == 0 && aligned(B, 16) && aligned(C, 16);
   a.vec_bc = (bc16 && chunk_len % ssk::kGroup == 0) ? 1 : 0;
-  a.err = device_status_word();
+  a.err = device_status_word(s);
   a.zoh = (d.flags & SS_FLAG_ZOH) ? 1 : 0;
   return a;
 }
@@ -130,7 +156,7 @@ int scan_fwd_impl(const ss_dims* dims, const float* h0, const void* u, const voi
   if (d.batch == 0 || d.dim == 0) return SS_OK;
   if (d.seqlen == 0) return initial_state(d, h0, last_state, s);
   ssk::ScanArgs a = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
-                                   d.seqlen);
+                                   d.seqlen, s);
   a.h0 = h0;
   const dim3 grid((unsigned)a.ctiles, (unsigned)d.batch);
   const bool bf = d.in_dtype == SS_BF16;
@@ -202,7 +228,7 @@ int chunked_phase_impl(int phase, const ss_dims* dims, const float* h0, const vo
   const size_t need = ss_scan_chunked_workspace_bytes(dims, chunk_len);
   if (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes < need) return SS_EWORKSPACE;
   ssk::ScanArgs a = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state,
-                                   chunk_len);
+                                   chunk_len, s);
   a.h0 = h0;
   if ((int64_t)a.ctiles * a.nchunks > kMaxGridX) return SS_EINVAL;
   a.ws_S = static_cast<float*>(workspace);
@@ -288,13 +314,13 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
   a.batch = d.batch; a.dim = d.dim; a.dstate = d.dstate;
   a.softplus = softplus_flag ? 1 : 0;
   a.zoh = (d.flags & SS_FLAG_ZOH) ? 1 : 0;
-  a.err = device_status_word();
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  a.err = device_status_word(s);
   const uintptr_t bc_align = d.in_dtype == SS_BF16 ? 8 : 16;
   a.vec = (d.dstate % 4 == 0 && aligned(state, 16) && aligned(A, 16) && aligned(B, bc_align) && aligned(C, bc_align))
               ? 1 : 0;
   if (d.dim > (int64_t)INT32_MAX / 16) return SS_EINVAL;   // (channel, lane) index of a batch row fits int
   const dim3 grid(1);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (ssk::launch_decode(a, d.in_dtype == SS_BF16, z != nullptr, grid, s) != 0) return SS_EINVAL;
   return launched();
 }
@@ -377,7 +403,7 @@ int ss_scan_bwd(const ss_dims* dims, const float* h0, const void* u, const void*
 
   // The state entering every chunk: the forward local pass and carry at the backward's chunk length.
   ssk::ScanArgs f = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, nullptr, nullptr,
-                                   ssk::kBwdChunk);
+                                   ssk::kBwdChunk, s);
   f.h0 = h0;
   const int64_t K = f.nchunks;
   char* ws = static_cast<char*>(workspace);
@@ -429,16 +455,26 @@ const char* ss_status_string(int status) {
 int ss_last_cuda_error(void) { return g_last_cuda; }
 
 int ss_selftest_wait_timeout(ss_stream_t stream) {
-  int* word = device_status_word();
-  if (!word) return cuda_fail(cudaGetLastError());
+  cudaError_t e = cudaSuccess;
+  int* word = device_status_word(reinterpret_cast<cudaStream_t>(stream), &e);
+  if (!word) return cuda_fail(e);
   ssk::launch_wait_timeout(word, reinterpret_cast<cudaStream_t>(stream));
   return launched();
 }
 
+int ss_measure_ex2(int64_t blocks, int iters, float* sink, uint64_t* ex2_count, ss_stream_t stream) {
+  if (blocks < 1 || blocks > kMaxGridX || iters < 1 || !sink || !ex2_count) return SS_EINVAL;
+  if (!aligned(sink, 4)) return SS_EALIGN;
+  *ex2_count = (uint64_t)blocks * ssk::kEx2Threads * ssk::kEx2Chains * (uint64_t)iters;
+  ssk::launch_ex2_rate(blocks, iters, sink, reinterpret_cast<cudaStream_t>(stream));
+  return launched();
+}
+
 int ss_device_status(int clear) {
-  int* word = device_status_word();
-  if (!word) return cuda_fail(cudaGetLastError());
-  cudaError_t e = cudaDeviceSynchronize();
+  cudaError_t e = cudaSuccess;
+  int* word = device_status_word(nullptr, &e);
+  if (!word) return cuda_fail(e);
+  e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e);
   int v = 0;
   e = cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost);
@@ -458,31 +494,13 @@ int ss_device_status(int clear) {
 // The workspace is one file-scope __device__ array of SS_STATIC_WORKSPACE_BYTES.
 // In host code the name g_static_ws is only a host-side handle for the symbol,
 // not a device address, so it is never passed to a kernel; its device address
-// is looked up once per device with cudaGetSymbolAddress (with that device
-// current) and cached.
+// is looked up with cudaGetSymbolAddress (with the device current) by
+// symbol_on_device above: on every call made outside a stream capture, and
+// from the last lookup on that device during a capture.
 namespace {
 
 __device__ __align__(256) unsigned char g_static_ws[SS_STATIC_WORKSPACE_BYTES];
-
-constexpr int kMaxStaticDevices = 256;
-std::mutex g_static_mu;
-void* g_static_ptr[kMaxStaticDevices];
-
-int static_workspace(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= kMaxStaticDevices) return SS_EINVAL;
-  std::lock_guard<std::mutex> lock(g_static_mu);
-  if (g_static_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_ws);
-    if (e != cudaSuccess) return cuda_fail(e);
-    g_static_ptr[dev] = p;
-  }
-  *out = g_static_ptr[dev];
-  return SS_OK;
-}
+SymbolCache g_static_cache;
 
 }  // namespace
 
@@ -493,9 +511,9 @@ extern "C" int ss_scan_chunked_static(const ss_dims* dims, const void* u, const 
   if (!dims || chunk_len < 1) return SS_EINVAL;
   // Reject problems whose workspace does not fit before touching the device.
   if (ss_scan_chunked_workspace_bytes(dims, chunk_len) > (size_t)SS_STATIC_WORKSPACE_BYTES) return SS_EWORKSPACE;
-  void* ws = nullptr;
-  const int st = static_workspace(&ws);
-  if (st != SS_OK) return st;
+  cudaError_t e = cudaSuccess;
+  void* ws = symbol_on_device(g_static_cache, (const void*)&g_static_ws, reinterpret_cast<cudaStream_t>(stream), &e);
+  if (!ws) return cuda_fail(e);
   // The chunked phases write every workspace entry before reading it, so the
   // previous call's contents need no clearing.
   return ss_scan_chunked(dims, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, chunk_len, ws,

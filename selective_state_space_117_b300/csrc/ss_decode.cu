@@ -168,7 +168,8 @@ __device__ __forceinline__ void bulk_store_hint(void* dst, const void* src, unsi
 // range back.  Measured 38.2 us against 43.8 us per 256 x 5120 x 16 step (eager
 // launches): the state moves with a few large copies instead of 16-byte loads and
 // stores from every thread.  The wait on the mbarrier is bounded (mbar_wait records
-// a timeout in the device status word; the state is then left unchanged).
+// a timeout in the device status word); if any thread's wait gives up, the whole block
+// skips the step, so the state is left unchanged and y is not written.
 template <int NT, bool BF, bool HAS_Z, bool ZOH>
 __global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const DecodeArgs a) {
   using L = In<BF>;
@@ -227,7 +228,13 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const Decod
       Cv[k] = c4.x; Cv[k + 1] = c4.y; Cv[k + 2] = c4.z; Cv[k + 3] = c4.w;
     }
   }
-  const bool ok = mbar_wait(&bar, 0, a.err);
+  // Every thread waits for the state's copy itself; the block then agrees on the outcome,
+  // so that after a wait that gave up no thread computes and nothing is written back.
+  const bool ok = __syncthreads_and(mbar_wait(&bar, 0, a.err));
+  if (!ok) {
+    if (tid == 0) mbar_wait(&bar, 0, nullptr);   // the copy may still be in flight: wait (bounded) before exiting
+    return;
+  }
   float* st = sst + cl * N + n0;
 #pragma unroll
   for (int k = 0; k < SPL; k += 4) {
@@ -256,7 +263,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const Decod
     acc = fma2(pk(Cv[2 * q], Cv[2 * q + 1]), hn, acc);
   }
   float y = lo(acc) + hi(acc);
-  if (active && ok) {
+  if (active) {
 #pragma unroll
     for (int k = 0; k < SPL; k += 4)
       if (n0 + k < N) *reinterpret_cast<float4*>(st + k) = make_float4(hv[k], hv[k + 1], hv[k + 2], hv[k + 3]);
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const Decod
   fence_async_smem();
   __syncthreads();
   if (tid == 0) {
-    if (ok) bulk_store_hint(gst, sst, bytes, keep);
+    bulk_store_hint(gst, sst, bytes, keep);
     bulk_commit();
     bulk_wait<0>();
   }

@@ -148,18 +148,24 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
 
   float* bcf = reinterpret_cast<float*>(sm + Lay::oBCf);  // [buffer][B, C][TS * NT]
   constexpr int BCF = Lay::kBCf / 4;
+  // Every thread waits on the tile's barrier itself; the block then agrees on the
+  // outcome at the barrier that follows (__syncthreads_and), so that once any wait
+  // has given up no thread computes on the tile and thread 0 starts no further
+  // load or store.  Loads already in flight are then waited for (bounded) below.
   bool ok = mbar_wait(&bar[0], 0, a.err);
   tma_convert_bc<NT, BF, HAS_Z>(sm, N, bcf, bcf + BCF, tid);
-  __syncthreads();
+  ok = __syncthreads_and(ok);
+  int pending = 0;                 // on a failure: the first tile whose load may still be in flight
+  int issued = min(S, ntiles);     // tiles whose loads thread 0 has issued
 
-  for (int k = 0; k < ntiles; ++k) {
+  for (int k = 0; ok && k < ntiles; ++k) {
     const int s = k % S;
     const unsigned slot = smem_addr(sm + s * Lay::kSlot);
     unsigned char* yt = sm + Lay::oY + (k & 1) * Lay::kY;
     const float* cB = bcf + (k & 1) * 2 * BCF;
     const float* cC = cB + BCF;
     const int64_t t0 = w.t_begin + (int64_t)k * TS;
-    if (w.active && ok) {
+    if (w.active) {
       const unsigned ybase = smem_addr(yt);
 #pragma unroll
       for (int g = 0; g < TS / kGroup; ++g) {
@@ -178,21 +184,34 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
     fence_async_smem();
     if (k + 1 < ntiles) {
       const int s1 = (k + 1) % S;
-      if (ok) ok = mbar_wait(&bar[s1], ((k + 1) / S) & 1, a.err);
+      ok = mbar_wait(&bar[s1], ((k + 1) / S) & 1, a.err);
       float* nb = bcf + ((k + 1) & 1) * 2 * BCF;
       tma_convert_bc<NT, BF, HAS_Z>(sm + s1 * Lay::kSlot, N, nb, nb + BCF, tid);
     }
     if (tid == 0) bulk_wait_read<0>();  // the previous tile's y store has left the other buffer
-    __syncthreads();
+    ok = __syncthreads_and(ok);
+    if (!ok) {
+      pending = k + 1;
+      break;
+    }
     if (tid == 0) {
       tma_store_3d(&m.y, yt, (int)t0, y0, zb);
       bulk_commit();
-      if (k + S < ntiles) tma_issue<NT, BF, HAS_Z>(m, sm, bar, k + S, w.t_begin, y0, zb, N);
+      if (k + S < ntiles) {
+        tma_issue<NT, BF, HAS_Z>(m, sm, bar, k + S, w.t_begin, y0, zb, N);
+        issued = k + S + 1;
+      }
     }
   }
-  if (tid == 0) bulk_wait<0>();
+  if (tid == 0) {
+    // After a failure, tiles pending .. issued - 1 were issued and not all seen to land: wait
+    // for each (bounded; a completed phase returns at once) before the block exits.
+    if (!ok)
+      for (int j = pending; j < issued; ++j) mbar_wait(&bar[j % S], (j / S) & 1, nullptr);
+    bulk_wait<0>();
+  }
 
-  if (MODE == kFull && w.active && a.last_state) {
+  if (MODE == kFull && w.active && ok && a.last_state) {
     float* out = a.last_state + w.bd * N;
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
@@ -213,7 +232,7 @@ struct LocalTmaLayout {
   static constexpr int kBf = kTmaSteps * NT * 4;
   static constexpr int oBf = kTmaSlots * kSlot;
   static constexpr int oBar = oBf + 2 * kBf;
-  static constexpr int kBytes = oBar + kTmaSlots * 8;
+  static constexpr int kBytes = oBar + kTmaSlots * 8 + 8;   // barriers, then the failure flag
   static constexpr int kAlloc = kBytes + 1024;
 };
 
@@ -273,6 +292,7 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
   };
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+    *reinterpret_cast<int*>(sm + Lay::oBar + kTmaSlots * 8) = 0;
     mbar_init_fence();
   }
   __syncthreads();
@@ -281,19 +301,27 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
 
   float* bf = reinterpret_cast<float*>(sm + Lay::oBf);
   constexpr int BF_ = Lay::kBf / 4;
+  // A wait that gives up raises s_fail before the tile's barrier; after the barrier
+  // every thread sees it, the block stops, and thread 0 waits (bounded) for the loads
+  // still in flight before the block exits, as on an early stop.
+  int* s_fail = reinterpret_cast<int*>(sm + Lay::oBar + kTmaSlots * 8);
   bool ok = mbar_wait(&bar[0], 0, a.err);
   {
     float* const d0[1] = {bf};
     tma_convert_rows<NT, BF, 1>(sm + 2 * Lay::kIn, N, d0, tid);
   }
+  if (!ok) *s_fail = 1;
   __syncthreads();
+  ok = *s_fail == 0;
+  int pending = ok ? ntiles : 0;   // the first tile whose load may still be in flight
+  int issued = min(S, ntiles);     // tiles whose loads thread 0 has issued
 
-  for (int k = 0; k < ntiles; ++k) {
+  for (int k = 0; ok && k < ntiles; ++k) {
     const int s = k % S;
     const unsigned slot = smem_addr(sm + s * Lay::kSlot);
     const float* cB = bf + (k & 1) * BF_;
     const int64_t t0 = w.t_begin + (int64_t)(ntiles - 1 - k) * TS;
-    if (w.active && ok) {
+    if (w.active) {
 #pragma unroll
       for (int g = TS / kGroup - 1; g >= 0; --g) {
         if (t0 + g * kGroup >= w.t_end) continue;
@@ -319,23 +347,32 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
     }
     if (k + 1 < ntiles) {
       const int s1 = (k + 1) % S;
-      if (ok) ok = mbar_wait(&bar[s1], ((k + 1) / S) & 1, a.err);
+      if (!mbar_wait(&bar[s1], ((k + 1) / S) & 1, a.err)) *s_fail = 1;
       float* const d1[1] = {bf + ((k + 1) & 1) * BF_};
       tma_convert_rows<NT, BF, 1>(sm + s1 * Lay::kSlot + 2 * Lay::kIn, N, d1, tid);
     }
     // Every weight left in this chunk underflows for every channel of the block: stop,
     // after the loads already issued (tiles k + 2 .. k + S - 1) have landed.
     const bool dead = !w.active || (may_stop && amax * R < kDead);
-    if (__syncthreads_and(dead)) {
-      if (tid == 0)
-        for (int j = k + 2; j < k + S && j < ntiles; ++j)
-          if (ok) ok = mbar_wait(&bar[j % S], (j / S) & 1, a.err);
+    const bool all_dead = __syncthreads_and(dead);
+    if (*s_fail) {
+      ok = false;
+      pending = k + 1;
       break;
     }
-    if (tid == 0 && k + S < ntiles) issue(k + S);
+    if (all_dead) {
+      pending = k + 2;
+      break;
+    }
+    if (k + S < ntiles) {
+      if (tid == 0) issue(k + S);
+      issued = k + S + 1;
+    }
   }
+  if (tid == 0)   // tiles pending .. issued - 1 may still be in flight (none after a full walk)
+    for (int j = pending; j < issued; ++j) mbar_wait(&bar[j % S], (j / S) & 1, nullptr);
 
-  if (!w.active) return;
+  if (!w.active || !ok) return;
   a.ws_S[w.k * a.batch * a.dim + w.bd] = R;
   float* H = a.ws_H + (w.k * a.batch * a.dim + w.bd) * N;
 #pragma unroll

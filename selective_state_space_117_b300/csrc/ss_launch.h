@@ -42,6 +42,12 @@ int launch_scan_warp(const ScanArgs& a, bool bf16, bool has_z, cudaStream_t s);
 // Diagnostic: one bounded mbarrier wait that runs out and records the timeout in *err.
 int launch_wait_timeout(int* err, cudaStream_t s);
 
+// Measurement: `blocks` blocks of kEx2Threads threads, each thread running kEx2Chains
+// chains of `iters` ex2.approx.ftz.f32 links (ss_peak.cu); sink is written never.
+constexpr int kEx2Threads = 256;
+constexpr int kEx2Chains = 8;
+int launch_ex2_rate(int64_t blocks, int iters, float* sink, cudaStream_t s);
+
 // Causal depthwise conv1d (width 4) with optional SiLU; segments of a row per warp.
 int launch_conv1d(const ConvArgs& a, bool bf16, bool silu_on, cudaStream_t s);
 int64_t conv1d_segments(int64_t seqlen);

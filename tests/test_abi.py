@@ -189,6 +189,16 @@ def test_state_update_validation():
     assert call(_dims(b=0)) == ss.SS_OK
 
 
+def test_measure_ex2_validation():
+    n = ctypes.c_uint64(0)
+    f = ss.lib().ss_measure_ex2
+    assert f(0, 16, P, ctypes.byref(n), None) == ss.SS_EINVAL
+    assert f(4, 0, P, ctypes.byref(n), None) == ss.SS_EINVAL
+    assert f(4, 16, None, ctypes.byref(n), None) == ss.SS_EINVAL
+    assert f(4, 16, P, None, None) == ss.SS_EINVAL
+    assert f(4, 16, P + 2, ctypes.byref(n), None) == ss.SS_EALIGN
+
+
 def test_status_strings():
     for code in (0, -1, -2, -3, -4, -5, -6):
         s = ss.lib().ss_status_string(code).decode()

@@ -10,9 +10,9 @@ a MUFU.EX2 with ~2^-22 relative error, and dA, dD, ddelta_bias, dB, dC are fp32
 sums of up to L or dim terms.  The errors measured on B300 stay below 4e-6.
 
 At the long-sequence size (batch 1, dim 5120, N 16, L 65536, bf16) the oracle
-computes sampled channels one by one; dB, dC and du over all channels are
-checked by Euler's identity for functions homogeneous of degree one: y and
-h_last are linear in B, in C and in u (with h0 = 0), so
+computes every channel, in blocks of 512, and every gradient is compared; dB,
+dC and du are also checked by Euler's identity for functions homogeneous of
+degree one: y and h_last are linear in B, in C and in u (with h0 = 0), so
     sum dB B = sum dC C = sum dy (y - D u silu(z)) + sum dlast h_last   (dC: without dlast)
     sum du u = sum dy y + sum dlast h_last.
 """
@@ -27,7 +27,8 @@ import torch
 import oracle
 import selective_state_space_117_b300 as ss
 from selective_state_space_117_b300 import inputs as I
-from parity import host, rms
+from parity import StreamCheck, host, log_result, rms
+from fullsize import wire_problem
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -167,25 +168,54 @@ def test_bwd_repeated_calls_agree():
         assert grad_err(host(g1[k]), host(g2[k])) <= 1e-5, k
 
 
-def test_bwd_long_sequence_sampled_and_identities():
-    """Batch 1, dim 5120, N 16, L 65536 (bf16, gate): the size and call the benchmark times."""
+def full_size_grads_vs_oracle(p, ct, label):
+    """Every gradient of a batch-1 problem against the oracle's adjoint, the oracle running over
+    blocks of 512 channels: du, ddelta, dz element by element (streamed), dA, dD, ddelta_bias per
+    channel, and dB, dC as the sums of every block's share.  Returns the GPU gradients."""
+    assert p.batch == 1
+    g = gpu_grads(p, ct)
+    torch.cuda.synchronize()
+    wp = wire_problem(p)
+    N, L = p.dstate, p.seqlen
+    dy = host(ct.dy).reshape(p.dim, L)
+    dl = host(ct.dlast).reshape(p.dim, N)
+    zoh = p.extra.get("zoh", False)
+    chk = {k: StreamCheck(f"{label} {k}", False, tol=TOL_GRAD) for k in ("du", "ddelta", "dz")}
+    dB = np.zeros((1, N, L))
+    dC = np.zeros((1, N, L))
+    dA = np.zeros((p.dim, N))
+    dD = np.zeros(p.dim)
+    db = np.zeros(p.dim)
+    for d0 in range(0, p.dim, 512):
+        d1 = min(p.dim, d0 + 512)
+        chans = np.arange(d0, d1, dtype=np.int64)
+        r = oracle.scan_bwd(wp["u"], wp["delta"], wp["A"], wp["B"], wp["C"], D=wp["D"], z=wp["z"],
+                            delta_bias=wp["delta_bias"], softplus=p.softplus, dtype=wp["dtype"], dy=dy[d0:d1],
+                            dlast=dl[d0:d1], chans=chans, want_BC=True, zoh=zoh)
+        for k in chk:
+            chk[k].add(host(g[k][0, d0:d1]), r[k])
+        dB += r["dB"]
+        dC += r["dC"]
+        dA[d0:d1], dD[d0:d1], db[d0:d1] = r["dA_part"], r["dD_part"], r["dbias_part"]
+    for k in chk:
+        chk[k].finish()
+    for k, ref in (("dA", dA), ("dD", dD), ("ddelta_bias", db), ("dB", dB), ("dC", dC)):
+        e = grad_err(host(g[k]).reshape(ref.shape), ref)
+        log_result(f"{label} {k}", n=int(ref.size), judged=e, rule="max err/max(|ref|,rms)", tol=TOL_GRAD)
+        assert e <= TOL_GRAD, f"{label} {k}: {e:.3e}"
+    return g
+
+
+def test_bwd_long_sequence_full_and_identities():
+    """Batch 1, dim 5120, N 16, L 65536 (bf16, gate): the size and call the benchmark times.
+    Every gradient against the oracle (all channels), then Euler's identity for dB, dC and du."""
     p = I.workload("mamba2p8b_long_bf16", device=DEV, gen_device="cuda")
     ct = I.cotangents(seed=103, batch=1, dim=p.dim, dstate=p.dstate, seqlen=p.seqlen, with_h0=False, device=DEV,
                       gen_device="cuda")
-    g = gpu_grads(p, ct)
+    g = full_size_grads_vs_oracle(p, ct, "bwd mamba2p8b_long")
     y, hl = ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, D=p.D, z=p.z, delta_bias=p.delta_bias, chunk_len=2048,
                             return_last_state=True)
     torch.cuda.synchronize()
-    # sampled channels against the oracle
-    chans = np.array([0, 1, 63, 64, 2047, 3001, 5119])
-    r = oracle_grads(p.to("cpu"), ct, chans=chans)
-    dy_rows = lambda t: host(t).reshape(p.dim, p.seqlen)[chans]
-    for k in ("du", "ddelta", "dz"):
-        e = grad_err(dy_rows(g[k]), r[k])
-        assert e <= TOL_GRAD, f"{k}: {e:.3e}"
-    assert grad_err(host(g["dA"])[chans], r["dA_part"]) <= TOL_GRAD
-    assert grad_err(host(g["dD"])[chans], r["dD_part"]) <= TOL_GRAD
-    assert grad_err(host(g["ddelta_bias"])[chans], r["dbias_part"]) <= TOL_GRAD
     # Euler's identity for dB, dC, du over every channel (float64 sums on the GPU)
     f = lambda t: t.double()
     ds_u = f(p.D)[None, :, None] * f(p.u) * torch.nn.functional.silu(f(p.z))
@@ -226,24 +256,14 @@ def _offset_copy(t):
     return out
 
 
-def test_bwd_long_sequence_zoh_sampled():
+def test_bwd_long_sequence_zoh_full():
     """The zero-order-hold backward pass at batch 1, dim 5120, N 16, L 65536 (bf16, gate):
-    sampled channels against the oracle."""
+    every gradient against the oracle (all channels)."""
     p = I.workload("mamba2p8b_long_bf16", device=DEV, gen_device="cuda")
     p.extra["zoh"] = True
     ct = I.cotangents(seed=104, batch=1, dim=p.dim, dstate=p.dstate, seqlen=p.seqlen, with_h0=False, device=DEV,
                       gen_device="cuda")
-    g = gpu_grads(p, ct)
-    torch.cuda.synchronize()
-    chans = np.array([2, 100, 2500, 5118])
-    r = oracle_grads(p.to("cpu"), ct, chans=chans)
-    rows = lambda t: host(t).reshape(p.dim, p.seqlen)[chans]
-    for k in ("du", "ddelta", "dz"):
-        e = grad_err(rows(g[k]), r[k])
-        assert e <= TOL_GRAD, f"{k}: {e:.3e}"
-    assert grad_err(host(g["dA"])[chans], r["dA_part"]) <= TOL_GRAD
-    assert grad_err(host(g["dD"])[chans], r["dD_part"]) <= TOL_GRAD
-    assert grad_err(host(g["ddelta_bias"])[chans], r["dbias_part"]) <= TOL_GRAD
+    full_size_grads_vs_oracle(p, ct, "zoh bwd mamba2p8b_long")
 
 
 @pytest.mark.parametrize("chunk", [None, 64], ids=["fwd", "chunked64"])

@@ -4,7 +4,8 @@ Every case draws seeded inputs from selective_state_space_117_b300.inputs,
 runs the library on the GPU, runs the oracle on the host on the same bytes,
 and compares element by element under the tolerances of tests/parity.py.
 Large workloads run at full size on the GPU in the launch configuration the
-benchmark times; the oracle then computes a sample of channels one by one.
+benchmark times; the oracle then computes every channel, block by block
+(tests/fullsize.py), and every output element is compared.
 """
 from __future__ import annotations
 
@@ -17,7 +18,8 @@ import torch
 import oracle
 import selective_state_space_117_b300 as ss
 from selective_state_space_117_b300 import inputs as I
-from parity import check, host
+from parity import StreamCheck, check, host
+from fullsize import compare_scans
 from pins import read_golden
 
 pytestmark = pytest.mark.gpu
@@ -32,15 +34,6 @@ def oracle_scan(p: I.Problem, h0=None):
                        softplus=p.softplus, dtype="bf16" if p.in_dtype == I.BF16 else "f32", h0=h0)
 
 
-def subproblem(p: I.Problem, ds) -> I.Problem:
-    """The same problem restricted to channels ds (channels are independent)."""
-    ds = torch.as_tensor(ds, device=p.u.device)
-    pick = lambda t: None if t is None else t.index_select(1, ds).contiguous()
-    pick0 = lambda t: None if t is None else t.index_select(0, ds).contiguous()
-    return I.Problem(p.name + "_sub", pick(p.u), pick(p.delta), pick0(p.A), p.B, p.C, pick0(p.D), pick(p.z),
-                     pick0(p.delta_bias), p.softplus, p.chunk_len)
-
-
 def run(p: I.Problem, impl: str, chunk_len=None):
     kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, softplus=p.softplus, return_last_state=True)
     if impl == "fwd":
@@ -50,15 +43,11 @@ def run(p: I.Problem, impl: str, chunk_len=None):
     return ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, chunk_len=chunk_len, **kw)
 
 
-def compare(p: I.Problem, y, hl, what, ds=None):
+def compare(p: I.Problem, y, hl, what):
     bf = p.in_dtype == I.BF16
-    ref_p = p if ds is None else subproblem(p, ds)
-    yr, hr = oracle_scan(ref_p.to("cpu"))
-    if ds is not None:
-        y = y[:, ds]
-        hl = hl[:, ds]
-    B, Dm, L = ref_p.u.shape
-    N = ref_p.A.shape[1]
+    yr, hr = oracle_scan(p.to("cpu"))
+    B, Dm, L = p.u.shape
+    N = p.A.shape[1]
     ey = check(host(y).reshape(B * Dm, L), yr, bf, what + " y")
     eh = check(host(hl).reshape(B * Dm, N), hr, bf, what + " last_state")
     return ey, eh
@@ -161,55 +150,52 @@ def test_medium_lti_closed_form():
     assert worst <= 1e-4, worst
 
 
-@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("fwd_warp", None), ("chunked", 512)])
+@pytest.mark.parametrize("impl,chunk", [("fwd", None), ("fwd_warp", None), ("chunked", 512), ("chunked", 2048)])
 def test_mamba130m_layer_bf16(impl, chunk):
+    """The Mamba-130M-shaped layer (8 x 1536 x 16 x 2048, bf16): every element of y and every
+    final state against the oracle."""
     p = I.workload("mamba130m_layer_bf16", device=DEV, gen_device="cuda")
     y, hl = run(p, impl, chunk)
-    ds = list(range(0, 1536, 37)) + [1535]
-    compare(p, y, hl, f"mamba130m/{impl}{chunk or ''}", ds=ds)
+    compare_scans(p, {f"{impl}{chunk or ''}": (y, hl)}, "mamba130m")
 
 
-@pytest.mark.parametrize("impl,chunk", [("chunked", 2048), ("fwd", None), ("fwd_thread", None)])
-def test_mamba2p8b_long_bf16(impl, chunk):
+def test_mamba2p8b_long_bf16():
+    """The Mamba-2.8B-shaped long sequence (1 x 5120 x 16 x 65536, bf16) through the chunked
+    scan at chunk 2048 (the launch configuration the benchmark times) and through ss_scan_fwd
+    under its default and thread schedules: every element of y (335.5 M per run) and every
+    final state against the oracle, which computes each channel block once for all runs."""
     p = I.workload("mamba2p8b_long_bf16", device=DEV, gen_device="cuda")
-    y, hl = run(p, impl, chunk)
-    ds = list(range(3, 5120, 331)) + [5119]
-    compare(p, y, hl, f"mamba2p8b_long/{impl}{chunk or ''}", ds=ds)
-    del y, hl, p
+    outs = {name: run(p, impl, chunk) for name, impl, chunk in
+            (("chunked2048", "chunked", 2048), ("fwd", "fwd", None), ("fwd_thread", "fwd_thread", None))}
+    torch.cuda.synchronize()
+    compare_scans(p, outs, "mamba2p8b_long")
+    del outs, p
     torch.cuda.empty_cache()
 
 
 def test_decode_stream_256x5120():
-    """1024 sequential decode steps on a (256, 5120, 16) fp32 state; sampled channels of every
-    step's y and the final state against the oracle's recurrence."""
+    """1024 sequential decode steps on a (256, 5120, 16) fp32 state: every step's y over all
+    256 x 5120 channels and the whole final state against the oracle's recurrence, which
+    advances its own fp64 state through the same 1024 steps."""
     cfg = I.DECODE
     st_in = I.decode_stream(seed=cfg["seed"], batch=cfg["batch"], dim=cfg["dim"], dstate=cfg["dstate"],
                             steps=cfg["steps"], device=DEV, gen_device="cuda")
-    state = torch.zeros((cfg["batch"], cfg["dim"], cfg["dstate"]), device=DEV)
-    bs = torch.tensor([0, 173], device=DEV)
-    ds = torch.arange(5, 5120, 80, device=DEV)
-    ys = []
-    y = torch.empty((cfg["batch"], cfg["dim"]), device=DEV)
+    nb, nd, N = cfg["batch"], cfg["dim"], cfg["dstate"]
+    state = torch.zeros((nb, nd, N), device=DEV)
+    y = torch.empty((nb, nd), device=DEV)
+    w = I.to_wire
+    A, Dv, bias = w(st_in.A), w(st_in.D), w(st_in.delta_bias)
+    sref = np.zeros((nb * nd, N))
+    cy = StreamCheck("decode_256x5120 y (all steps, all channels)", True)
     for t in range(cfg["steps"]):
         ss.state_update(state, st_in.u[t], st_in.delta[t], st_in.A, st_in.B[t], st_in.C[t], D=st_in.D, z=st_in.z[t],
                         delta_bias=st_in.delta_bias, y=y)
-        ys.append(y.index_select(0, bs).index_select(1, ds).clone())
-    yg = torch.stack(ys).cpu().numpy()                         # (steps, 2, nd)
-    sg = state.index_select(0, bs).index_select(1, ds).cpu().numpy().reshape(-1, cfg["dstate"])
-    # oracle: the same sub-problem, one step at a time
-    w = I.to_wire
-    A = st_in.A.index_select(0, ds).cpu().numpy()
-    Dv = st_in.D.index_select(0, ds).cpu().numpy()
-    bias = st_in.delta_bias.index_select(0, ds).cpu().numpy()
-    sub = lambda x: w(x.index_select(1, bs).index_select(2, ds))
-    u, dl, z = sub(st_in.u), sub(st_in.delta), sub(st_in.z)
-    Bw, Cw = w(st_in.B.index_select(1, bs)), w(st_in.C.index_select(1, bs))
-    sref = np.zeros((2 * len(ds), cfg["dstate"]))
-    yref = np.empty((cfg["steps"], 2 * len(ds)))
-    for t in range(cfg["steps"]):
-        yref[t] = oracle.state_update(sref, u[t], dl[t], A, Bw[t], Cw[t], D=Dv, z=z[t], delta_bias=bias, dtype="bf16")
-    check(yg.reshape(cfg["steps"], -1), yref, True, "decode y (all steps)")
-    check(sg, sref, True, "decode final state")
+        yg = host(y).reshape(-1)
+        yr = oracle.state_update(sref, w(st_in.u[t]), w(st_in.delta[t]), A, w(st_in.B[t]), w(st_in.C[t]), D=Dv,
+                                 z=w(st_in.z[t]), delta_bias=bias, dtype="bf16")
+        cy.add(yg, yr)
+    cy.finish()
+    check(host(state).reshape(nb * nd, N), sref, True, "decode_256x5120 final state (all channels)")
     del st_in, state
     torch.cuda.empty_cache()
 

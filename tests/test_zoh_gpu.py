@@ -13,7 +13,8 @@ import torch
 import oracle
 import selective_state_space_117_b300 as ss
 from selective_state_space_117_b300 import inputs as I
-from parity import check, host
+from parity import StreamCheck, check, host
+from fullsize import compare_scans
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -140,56 +141,39 @@ def test_zoh_two_faces_agree():
     check(host(st), host(hf), False, "zoh decode state vs fwd")
 
 
-def test_zoh_long_sequence_sampled():
+def test_zoh_long_sequence_full():
     """The long-sequence workload (batch 1, D 5120, N 16, L 65536, bf16) with the hold weight
-    through the chunked scan at chunk 2048, the benchmark's launch configuration; sampled
-    channels against the oracle's ZOH scan."""
+    through the chunked scan at chunk 2048, the benchmark's launch configuration: every
+    element of y and every final state against the oracle's ZOH scan."""
     p = I.workload("mamba2p8b_long_bf16", device=DEV, gen_device="cuda")
     y, hl = ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, D=p.D, z=p.z, delta_bias=p.delta_bias, chunk_len=2048,
                             return_last_state=True, zoh=True)
-    ds = torch.tensor(list(range(7, 5120, 409)) + [5119], device=DEV)
-    pick = lambda t: t.index_select(1, ds).contiguous()
-    sub = I.Problem("zoh_long_sub", pick(p.u), pick(p.delta), p.A.index_select(0, ds).contiguous(), p.B, p.C,
-                    p.D.index_select(0, ds).contiguous(), pick(p.z), p.delta_bias.index_select(0, ds).contiguous(),
-                    p.softplus, p.chunk_len)
-    yr, hr = oracle_zoh(sub.to("cpu"))
-    n = len(ds)
-    check(host(y.index_select(1, ds)).reshape(n, -1), yr, True, "zoh long y")
-    check(host(hl.index_select(1, ds)).reshape(n, 16), hr, True, "zoh long state")
+    torch.cuda.synchronize()
+    compare_scans(p, {"chunked2048": (y, hl)}, "zoh mamba2p8b_long", zoh=True)
     del y, hl, p
     torch.cuda.empty_cache()
 
 
 def test_zoh_decode_stream_full_size():
     """256 sequential decode steps with the hold weight on the (256, 5120, 16) state of the
-    decode workload; sampled channels of every step's y and of the final state against the
+    decode workload: every step's y over all channels and the whole final state against the
     oracle's ZOH recurrence."""
     steps = 256
     st_in = I.decode_stream(seed=4, batch=256, dim=5120, dstate=16, steps=steps, device=DEV, gen_device="cuda")
     state = torch.zeros((256, 5120, 16), device=DEV)
-    bs = torch.tensor([3, 200], device=DEV)
-    ds = torch.arange(11, 5120, 97, device=DEV)
     y = torch.empty((256, 5120), device=DEV)
-    ys = []
+    w = I.to_wire
+    A, Dv, bias = w(st_in.A), w(st_in.D), w(st_in.delta_bias)
+    sref = np.zeros((256 * 5120, 16))
+    cy = StreamCheck("zoh decode_256x5120 y (256 steps, all channels)", True)
     for t in range(steps):
         ss.state_update(state, st_in.u[t], st_in.delta[t], st_in.A, st_in.B[t], st_in.C[t], D=st_in.D,
                         z=st_in.z[t], delta_bias=st_in.delta_bias, y=y, zoh=True)
-        ys.append(y.index_select(0, bs).index_select(1, ds).clone())
-    yg = torch.stack(ys).cpu().numpy()
-    sg = state.index_select(0, bs).index_select(1, ds).cpu().numpy().reshape(-1, 16)
-    w = I.to_wire
-    A = st_in.A.index_select(0, ds).cpu().numpy()
-    Dv = st_in.D.index_select(0, ds).cpu().numpy()
-    bias = st_in.delta_bias.index_select(0, ds).cpu().numpy()
-    sub = lambda x: w(x.index_select(1, bs).index_select(2, ds))
-    u, dl, z = sub(st_in.u), sub(st_in.delta), sub(st_in.z)
-    Bw, Cw = w(st_in.B.index_select(1, bs)), w(st_in.C.index_select(1, bs))
-    sref = np.zeros((2 * len(ds), 16))
-    yref = np.empty((steps, 2 * len(ds)))
-    for t in range(steps):
-        yref[t] = oracle.state_update(sref, u[t], dl[t], A, Bw[t], Cw[t], D=Dv, z=z[t], delta_bias=bias,
-                                      dtype="bf16", zoh=True)
-    check(yg.reshape(steps, -1), yref, True, "zoh decode y (all steps)")
-    check(sg, sref, True, "zoh decode final state")
+        yg = host(y).reshape(-1)
+        yr = oracle.state_update(sref, w(st_in.u[t]), w(st_in.delta[t]), A, w(st_in.B[t]), w(st_in.C[t]), D=Dv,
+                                 z=w(st_in.z[t]), delta_bias=bias, dtype="bf16", zoh=True)
+        cy.add(yg, yr)
+    cy.finish()
+    check(host(state).reshape(-1, 16), sref, True, "zoh decode_256x5120 final state (all channels)")
     del st_in, state
     torch.cuda.empty_cache()

@@ -7,10 +7,12 @@ ss_scan_chunked_static, which takes no workspace argument and uses a fixed
 device array inside the library instead (SS_STATIC_WORKSPACE_BYTES).
 
 The GPU test calls it through the C ABI twice in a row, on two problems of
-different shapes and dtypes, and checks each result against ss_scan_chunked with
-a caller-provided workspace, under the parity tolerances of tests/parity.py.
-Because every call shares the array, anything the first call left behind that
-the second call wrongly read would show up as a mismatch.  The host test checks
+different shapes and dtypes.  Each result must equal, bit for bit, what
+ss_scan_chunked computes with a caller-provided workspace (the same kernels in
+the same launch configuration), and must match the fp64 oracle under the parity
+tolerances of tests/parity.py.  Because every call shares the array, anything
+the first call left behind that the second call wrongly read would show up as a
+mismatch.  The host test checks
 that a problem too large for the array is refused before the device is touched.
 """
 import ctypes
@@ -18,6 +20,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import selective_state_space_117_b300 as ss
 from selective_state_space_117_b300 import inputs as I
 from parity import check, host
@@ -64,10 +67,15 @@ def test_static_workspace_matches_caller_workspace_on_two_calls():
         st = _call_static(p, chunk, y, hl)
         assert st == 0, ss.lib().ss_status_string(st).decode()
         torch.cuda.synchronize()
+        assert torch.equal(y, y_ref), f"{p.name}: y differs from ss_scan_chunked's"
+        assert torch.equal(hl, h_ref), f"{p.name}: last_state differs from ss_scan_chunked's"
         bf = p.in_dtype == I.BF16
         n = p.batch * p.dim
-        check(host(y).reshape(n, p.seqlen), host(y_ref).reshape(n, p.seqlen), bf, f"{p.name} y")
-        check(host(hl).reshape(n, p.dstate), host(h_ref).reshape(n, p.dstate), bf, f"{p.name} last_state")
+        w = I.to_wire
+        yr, hr = oracle.scan(w(p.u), w(p.delta), w(p.A), w(p.B), w(p.C), D=w(p.D), z=w(p.z),
+                             delta_bias=w(p.delta_bias), dtype="bf16" if bf else "f32")
+        check(host(y).reshape(n, p.seqlen), yr, bf, f"{p.name} static y vs oracle")
+        check(host(hl).reshape(n, p.dstate), hr, bf, f"{p.name} static last_state vs oracle")
 
 
 def test_static_workspace_refuses_oversized_problem():
