@@ -73,7 +73,8 @@ TRAFFIC = {
 
 # The files that define the chunked step's three kernels and how they are launched.
 STEP_SOURCES = ("ss_device.cuh", "ss_kernels.cuh", "ss_kernels_tma.cuh", "ss_tma.cuh", "ss_tma_launch.cuh",
-                "ss_scan_tma.cu", "ss_scan_local.cu", "ss_occupancy.cuh", "ss_types.h", "ss_dispatch.cuh")
+                "ss_scan_tma.cu", "ss_scan_local.cu", "ss_occupancy.cuh", "ss_types.h", "ss_dispatch.cuh",
+                "ss_local_sorted.cu")
 
 
 def kernel_sources_hash():
@@ -140,7 +141,6 @@ def measure_sfu(ss, torch, launches=20, iters=4096):
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
     with ClockSampler(device_index_for_smi(torch)) as clk:
-        time.sleep(0.2)
         for e0, e1 in ev:
             e0.record()
             ss.measure_ex2(blocks, iters, sink=sink)
@@ -174,7 +174,9 @@ def roofline_terms(byts, exps, ms, pk):
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples (every 50 ms) while the timed region runs."""
+    """nvidia-smi samples (every 50 ms) while the timed region runs.  Entering waits (up to
+    10 s) for the first sample, so that the sampler's start-up, which can hold up the
+    process's own CUDA calls for a moment, falls before the timed region."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
@@ -183,8 +185,11 @@ class ClockSampler:
         self.proc = None
         self.idx = device_index
         self.out = ""
+        self.lines = []
+        self.reader = None
 
     def __enter__(self):
+        import threading
         cmd = ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "50"]
         if self.idx is not None:
             cmd += ["-i", str(self.idx)]
@@ -192,6 +197,19 @@ class ClockSampler:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        first = threading.Event()
+
+        def pump():
+            for line in self.proc.stdout:
+                self.lines.append(line)
+                first.set()
+            first.set()
+
+        self.reader = threading.Thread(target=pump, daemon=True)
+        self.reader.start()
+        first.wait(timeout=10.0)
+        time.sleep(0.2)
         return self
 
     def __exit__(self, *exc):
@@ -199,10 +217,13 @@ class ClockSampler:
             time.sleep(0.1)
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                self.proc.wait()
+            if self.reader is not None:
+                self.reader.join(timeout=5)
+            self.out = "".join(self.lines)
 
     def summary(self):
         rows = []
@@ -415,7 +436,6 @@ def run_ours(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(device_index_for_smi(torch)) as clk:
-        time.sleep(0.3)                  # let the sampler start before the timed region
         barrier(world)
         torch.cuda.synchronize()
         t0.record()
@@ -469,7 +489,7 @@ def run_ours(args):
         "kernels": line_kernels,
         "kernel_sources": kernel_sources_hash(),
         "e2e": e2e,
-        "gpu_launches": args.steps * len(phases),
+        "gpu_launches": args.steps * (len(phases) + 1),   # the local phase orders the channels first
         "clocks": clk.summary(),
         "peaks": pk,
         "sfu": sfu,
@@ -602,17 +622,45 @@ def time_scan_fwd(ss, torch, p, schedule, reps):
     return e0.elapsed_time(e1) / reps
 
 
+def time_scan_chunked(ss, torch, p, chunk, reps):
+    """Average ms of ss_scan_chunked at `chunk` over reps calls (CUDA events around the loop)."""
+    y = torch.empty((p.batch, p.dim, p.seqlen), device="cuda")
+    hl = torch.empty((p.batch, p.dim, p.dstate), device="cuda")
+    ws = torch.empty((ss.chunked_workspace_bytes(p.batch, p.dim, p.dstate, p.seqlen, chunk),), dtype=torch.uint8,
+                     device="cuda")
+    kw = dict(D=p.D, z=p.z, delta_bias=p.delta_bias, softplus=p.softplus, y=y, last_state=hl, chunk_len=chunk,
+              workspace=ws)
+    for _ in range(3):
+        ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, **kw)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ss.scan_chunked(p.u, p.delta, p.A, p.B, p.C, **kw)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def bench_fwd_layer(ss, I, torch, pk, reps=20):
-    """ss_scan_fwd on the Mamba-130M-shaped layer (batch 8, D 1536, N 16, L 2048, bf16
-    inputs, gate), the single-pass entry point's own workload."""
+    """The Mamba-130M-shaped layer (batch 8, D 1536, N 16, L 2048, bf16 inputs, gate):
+    ss_scan_fwd (one pass; 12288 channels at one thread each fill 2.6 warps per SM) and
+    ss_scan_chunked at chunks of 256, 512 and 1024 steps (4 to 8 times the threads, plus a
+    local pass and a carry); the roofline is stated for the faster entry point."""
     p = I.workload("mamba130m_layer_bf16", device="cuda", gen_device="cuda")
     elems, byts, exps = workload_counts(p.batch, p.dim, p.dstate, p.seqlen)
     ms = time_scan_fwd(ss, torch, p, None, reps)
-    roof = roofline_terms(byts, exps, ms, pk)
+    chunked = {c: time_scan_chunked(ss, torch, p, c, reps) for c in (256, 512, 1024)}
+    best_c = min(chunked, key=chunked.get)
+    best = ("ss_scan_fwd", ms) if ms <= chunked[best_c] else (f"ss_scan_chunked (chunk {best_c})", chunked[best_c])
+    roof = roofline_terms(byts, exps, best[1], pk)
     return {"workload": "mamba130m_layer_bf16: batch=8, D=1536, N=16, L=2048, bf16 inputs, gate",
             "entry_point": "ss_scan_fwd", "schedule": "thread (12288 channels)", "ms": round(ms, 4),
-            "elem_per_s": elems / (ms * 1e-3), "roofline": roof,
-            "note": "inputs 0.25 GB, about twice the L2: no flush between repetitions", "gpu_launches": reps}
+            "chunked_ms": {str(c): round(v, 4) for c, v in chunked.items()},
+            "best": best[0], "best_ms": round(best[1], 4), "elem_per_s": elems / (best[1] * 1e-3), "roofline": roof,
+            "roofline_fwd": roofline_terms(byts, exps, ms, pk),
+            "note": "inputs 0.25 GB, about twice the L2: no flush between repetitions",
+            "gpu_launches": reps * (1 + 3 * 4) + 9 * 4 + 3}
 
 
 def bench_fwd_schedules(ss, I, torch, reps=50):

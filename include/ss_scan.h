@@ -132,17 +132,23 @@ size_t ss_scan_chunked_workspace_bytes(const ss_dims* dims, int64_t chunk_len);
 
 /*
  * Chunked scan for long sequences: the same result as ss_scan_fwd, computed
- * as (1) a local zero-start scan of every chunk of chunk_len steps, giving the
- * chunk's end state and its decay product, (2) an exclusive scan across chunks
- * of the (decay product, state) pairs under the associative operator
- * (a1,b1) o (a2,b2) = (a1*a2, a2*b1 + b2), which gives each chunk its true
- * starting state, and (3) a fix-up pass that runs every chunk from that state
- * and writes y.  The recurrence is associative ("Parallel scan", azimuth.plus),
- * which is what makes chunks independent.
+ * as (1) a local zero-start scan of every chunk of chunk_len steps but the
+ * last, giving the chunk's end state and its decay product, (2) an exclusive
+ * scan across chunks of the (decay product, state) pairs under the associative
+ * operator (a1,b1) o (a2,b2) = (a1*a2, a2*b1 + b2), which gives each chunk its
+ * true starting state, and (3) a fix-up pass that runs every chunk from that
+ * state, writes y, and writes last_state from the last chunk.  The recurrence
+ * is associative ("Parallel scan", azimuth.plus), which is what makes chunks
+ * independent.  The local scan only needs each chunk's end state: walking a
+ * chunk backward from its end, a state's remaining terms are exact zeros once
+ * its weight exp(A R) underflows in fp32, and (with the softplus on) they are
+ * left out, with the channels grouped by decay speed so that whole warps
+ * stop together; the results are those of the full walk.
  *   chunk_len        >= 1
  *   workspace        device memory of at least ss_scan_chunked_workspace_bytes,
  *                    256-byte aligned; its contents on entry are ignored
- * Other arguments as ss_scan_fwd.  Three kernels are launched on `stream`.
+ * Other arguments as ss_scan_fwd.  Three to four kernels are launched on
+ * `stream` (none for the local scan when there is a single chunk).
  */
 int ss_scan_chunked(const ss_dims* dims, const void* u, const void* delta, const float* A,
                     const void* B, const void* C, const float* D, const void* z,
@@ -155,8 +161,9 @@ int ss_scan_chunked(const ss_dims* dims, const void* u, const void* delta, const
  * themselves (for example to time them, or to run other work between them).
  * Calling phases SS_PHASE_LOCAL, SS_PHASE_CARRY and SS_PHASE_FIXUP in this
  * order on one stream, with the same arguments and workspace, is exactly
- * ss_scan_chunked.  Each phase launches one kernel.  The carry phase writes
- * last_state; the fix-up phase writes y.
+ * ss_scan_chunked.  The local phase launches up to two kernels (the channel
+ * order, then the local scan), the others one each.  The fix-up phase writes
+ * y and last_state (the carry phase writes last_state only when L = 0).
  */
 typedef enum { SS_PHASE_LOCAL = 1, SS_PHASE_CARRY = 2, SS_PHASE_FIXUP = 3 } ss_phase;
 
@@ -215,7 +222,7 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
  *   - Returns SS_EWORKSPACE, without touching the device, when
  *     ss_scan_chunked_workspace_bytes(dims, chunk_len) exceeds
  *     SS_STATIC_WORKSPACE_BYTES (16 MiB: for example batch 1, dim 5120, N 16,
- *     L 65536 with chunk 2048 needs 11.2 MB).
+ *     L 65536 with chunk 2048 needs 11.3 MB).
  *   - Every call made outside a stream capture looks up the array's device
  *     address with cudaGetSymbolAddress (under a lock, with that device
  *     current); a call made while its stream is being captured uses the address

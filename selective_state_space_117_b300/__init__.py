@@ -32,8 +32,9 @@ _lib = None
 
 F32, BF16 = 0, 1
 MAX_DSTATE = 64
-# Kernels launched per call (for launch accounting): chunked = local + carry + fix-up.
-LAUNCHES = {"scan_fwd": 1, "scan_chunked": 3, "state_update": 1, "scan_bwd": 5}
+# Kernels launched per call (for launch accounting): chunked = channel order + local + carry + fix-up
+# (the first two only when there is more than one chunk).
+LAUNCHES = {"scan_fwd": 1, "scan_chunked": 4, "state_update": 1, "scan_bwd": 5}
 
 SS_OK, SS_EINVAL, SS_EALIGN, SS_EDTYPE, SS_EWORKSPACE, SS_ECUDA, SS_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 

@@ -200,13 +200,26 @@ int ss_scan_fwd_h0(const ss_dims* dims, const float* h0, const void* u, const vo
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+// The chunked workspace: S (K, batch, dim) fp32, then H (K, batch, dim, N) fp32, then the
+// channel order of the grouped local pass (dim) int32, each part 256-byte aligned.
+struct ChunkedWs {
+  size_t s_off, h_off, perm_off, bytes;
+};
+
+ChunkedWs chunked_ws_layout(const ss_dims& d, int64_t chunk_len) {
+  const int64_t K = ceil_div(d.seqlen, chunk_len);
+  ChunkedWs w;
+  w.s_off = 0;
+  w.h_off = align_up((size_t)(d.batch * d.dim * K) * sizeof(float), kWsAlign);
+  w.perm_off = w.h_off + align_up((size_t)(d.batch * d.dim * K * d.dstate) * sizeof(float), kWsAlign);
+  w.bytes = w.perm_off + (size_t)d.dim * sizeof(int);
+  return w;
+}
+
 size_t ss_scan_chunked_workspace_bytes(const ss_dims* dims, int64_t chunk_len) {
   if (!dims || chunk_len < 1 || dims->batch < 0 || dims->dim < 0 || dims->dstate < 0 || dims->seqlen < 0)
     return 0;
-  const int64_t K = ceil_div(dims->seqlen, chunk_len);
-  const size_t s_bytes = (size_t)(dims->batch * dims->dim * K) * sizeof(float);
-  const size_t h_bytes = (size_t)(dims->batch * dims->dim * K * dims->dstate) * sizeof(float);
-  return align_up(s_bytes, kWsAlign) + h_bytes;
+  return chunked_ws_layout(*dims, chunk_len).bytes;
 }
 
 }  // extern "C"
@@ -231,15 +244,26 @@ int chunked_phase_impl(int phase, const ss_dims* dims, const float* h0, const vo
                                    chunk_len, s);
   a.h0 = h0;
   if ((int64_t)a.ctiles * a.nchunks > kMaxGridX) return SS_EINVAL;
-  a.ws_S = static_cast<float*>(workspace);
-  a.ws_H = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                    align_up((size_t)(d.batch * d.dim * a.nchunks) * sizeof(float), kWsAlign));
+  const ChunkedWs lay = chunked_ws_layout(d, chunk_len);
+  char* ws = static_cast<char*>(workspace);
+  a.ws_S = reinterpret_cast<float*>(ws + lay.s_off);
+  a.ws_H = reinterpret_cast<float*>(ws + lay.h_off);
+  a.perm = reinterpret_cast<int*>(ws + lay.perm_off);
+  // The local pass leaves out the last chunk: only the carry into each chunk is needed from it,
+  // and the final state comes out of the last chunk's fix-up.
+  a.local_chunks = a.nchunks - 1;
   const dim3 grid((unsigned)(a.ctiles * a.nchunks), (unsigned)d.batch);
   const bool bf = d.in_dtype == SS_BF16;
   int rc = 0;
   if (phase == SS_PHASE_LOCAL) {
-    if (!(ssk::tma_available(a, bf, ssk::kLocal) && ssk::launch_local_tma(a, bf, grid, s) == 0))
-      rc = ssk::launch_scan_local(a, bf, grid, s);
+    const dim3 lgrid((unsigned)(a.ctiles * a.local_chunks), (unsigned)d.batch);
+    if (a.local_chunks == 0) {
+      rc = 0;
+    } else if (softplus_flag && ssk::local_sorted_available(a, bf)) {
+      rc = ssk::launch_local_sorted(a, bf, s);
+    } else if (!(ssk::tma_available(a, bf, ssk::kLocal) && ssk::launch_local_tma(a, bf, lgrid, s) == 0)) {
+      rc = ssk::launch_scan_local(a, bf, lgrid, s);
+    }
   } else if (phase == SS_PHASE_CARRY) {
     rc = ssk::launch_carry(a, s);
   } else if (!(ssk::tma_available(a, bf, ssk::kFixup) &&
@@ -406,6 +430,7 @@ int ss_scan_bwd(const ss_dims* dims, const float* h0, const void* u, const void*
                                    ssk::kBwdChunk, s);
   f.h0 = h0;
   const int64_t K = f.nchunks;
+  f.local_chunks = K;   // the adjoint carry also needs the last chunk's dt sum
   char* ws = static_cast<char*>(workspace);
   const size_t s_bytes = align_up((size_t)(d.batch * d.dim * K) * sizeof(float), kWsAlign);
   const size_t h_bytes = align_up((size_t)(d.batch * d.dim * K * d.dstate) * sizeof(float), kWsAlign);

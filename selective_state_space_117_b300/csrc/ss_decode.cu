@@ -228,13 +228,10 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const Decod
       Cv[k] = c4.x; Cv[k + 1] = c4.y; Cv[k + 2] = c4.z; Cv[k + 3] = c4.w;
     }
   }
-  // Every thread waits for the state's copy itself; the block then agrees on the outcome,
-  // so that after a wait that gave up no thread computes and nothing is written back.
-  const bool ok = __syncthreads_and(mbar_wait(&bar, 0, a.err));
-  if (!ok) {
-    if (tid == 0) mbar_wait(&bar, 0, nullptr);   // the copy may still be in flight: wait (bounded) before exiting
-    return;
-  }
+  // Every thread waits for the state's copy itself.  A thread whose wait gave up writes
+  // nothing (neither its y nor its states); the block agrees at its last barrier, and the
+  // state goes back to memory only if every wait succeeded.
+  const bool ok = mbar_wait(&bar, 0, a.err);
   float* st = sst + cl * N + n0;
 #pragma unroll
   for (int k = 0; k < SPL; k += 4) {
@@ -263,7 +260,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const Decod
     acc = fma2(pk(Cv[2 * q], Cv[2 * q + 1]), hn, acc);
   }
   float y = lo(acc) + hi(acc);
-  if (active) {
+  if (active && ok) {
 #pragma unroll
     for (int k = 0; k < SPL; k += 4)
       if (n0 + k < N) *reinterpret_cast<float4*>(st + k) = make_float4(hv[k], hv[k + 1], hv[k + 2], hv[k + 3]);
@@ -274,17 +271,23 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const Decod
 #pragma unroll
     for (int off = G / 2; off > 0; off >>= 1) y += __shfl_xor_sync(gmask, y, off);
   }
-  if (active && l == 0) {
+  // y sums the partial readouts of a channel's lanes: written only if every lane of the warp saw its data.
+  const bool warp_ok = __all_sync(0xffffffffu, ok);
+  if (active && l == 0 && warp_ok) {
     float yv = fmaf(Dd, uu, y);
     if (HAS_Z) yv *= silu(zz);
     a.y[c] = yv;
   }
   fence_async_smem();
-  __syncthreads();
+  const bool all_ok = __syncthreads_and(ok);
   if (tid == 0) {
-    bulk_store_hint(gst, sst, bytes, keep);
-    bulk_commit();
-    bulk_wait<0>();
+    if (all_ok) {
+      bulk_store_hint(gst, sst, bytes, keep);
+      bulk_commit();
+      bulk_wait_read<0>();   // the source tile has been read: the block may exit while the write completes
+    } else {
+      mbar_wait(&bar, 0, nullptr);   // the copy may still be in flight: wait (bounded) before exiting
+    }
   }
 }
 

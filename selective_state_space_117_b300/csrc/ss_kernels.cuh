@@ -17,8 +17,9 @@
 // and one fma (the readout C*h), where A' = A*log2(e).
 //
 // scan_kernel modes:
-//   kFull   start from h = 0, write y and (optionally) the final state
-//   kFixup  start from the carried-in state in the workspace, write y
+//   kFull   start from h = 0 (or h0), write y and (optionally) the final state
+//   kFixup  start from the carried-in state in the workspace, write y, and the final
+//           state from the last chunk
 // local_kernel is the first phase of the chunked scan (see its comment).
 #pragma once
 
@@ -303,7 +304,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(c
   }
 
   cp_async_wait<0>();
-  if (MODE == kFull && w.active && a.last_state) {
+  // The final state: after the whole sequence, or after the last chunk of the chunked scan.
+  if ((MODE == kFull || w.k == a.nchunks - 1) && w.active && a.last_state) {
     float* out = a.last_state + w.bd * N;
 #pragma unroll
     for (int q = 0; q < NP; ++q) {

@@ -208,10 +208,11 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
     // for each (bounded; a completed phase returns at once) before the block exits.
     if (!ok)
       for (int j = pending; j < issued; ++j) mbar_wait(&bar[j % S], (j / S) & 1, nullptr);
-    bulk_wait<0>();
+    bulk_wait_read<0>();   // the y tiles have been read out of shared memory; their writes complete on their own
   }
 
-  if (MODE == kFull && w.active && ok && a.last_state) {
+  // The final state: after the whole sequence, or after the last chunk of the chunked scan.
+  if ((MODE == kFull || w.k == a.nchunks - 1) && w.active && ok && a.last_state) {
     float* out = a.last_state + w.bd * N;
 #pragma unroll
     for (int q = 0; q < NP; ++q) {

@@ -25,6 +25,13 @@ inline int launch_scan_local(const ScanArgs& a, bool bf16, dim3 grid, cudaStream
   return a.zoh ? launch_scan_local_t<true>(a, bf16, grid, s) : launch_scan_local_t<false>(a, bf16, grid, s);
 }
 int launch_carry(const ScanArgs& a, cudaStream_t s);
+
+// The local pass over channels grouped by decay speed (ss_local_sorted.cu): one warp per
+// (32 channels, batch row, chunk) for chunks 0 .. local_chunks - 1, states dropped once their
+// weights underflow.  Needs N <= 16, 16-byte aligned rows (vec, vec_bc), whole 16-step tiles
+// per chunk and a.perm; returns 0 when launched.
+bool local_sorted_available(const ScanArgs& a, bool bf16);
+int launch_local_sorted(const ScanArgs& a, bool bf16, cudaStream_t s);
 int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
 
 // Backward pass after the forward local pass and carry: adjoint local pass, adjoint carry, main

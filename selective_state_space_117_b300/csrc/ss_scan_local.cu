@@ -7,9 +7,11 @@ namespace ssk {
 // Exclusive scan over chunks of the pairs (P_k, H_k) = (exp(A * S_k), chunk end state) under
 // (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2), one thread per (b, d, n):
 //   carry_0 = h0 (zeros without one),   carry_{k+1} = P_k * carry_k + H_k.
-// Overwrites the workspace's H_k with carry_k (the true state entering chunk k) and writes the
-// final state after the last chunk.  The dependent chain is latency-bound: loads run in
-// batches of 8 chunks, and the next batch is requested before the current one is consumed.
+// Overwrites the workspace's H_k with carry_k (the true state entering chunk k) for every chunk.
+// Only the chunks the local pass covered (0 .. local_chunks - 1) are combined: the forward scan
+// leaves out its last chunk, whose end state is the final state that its fix-up pass writes.
+// The dependent chain is latency-bound: loads run in batches of 8 chunks, and the next batch is
+// requested before the current one is consumed.
 __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t N = a.dstate;
@@ -36,7 +38,7 @@ __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
     for (int u = 0; u < 8; ++u) {
       if (k0 + u < K) {
         H[(k0 + u) * BD * N] = c;
-        c = fmaf(ex2(A2 * sk[u]), c, he[u]);
+        if (k0 + u < a.local_chunks) c = fmaf(ex2(A2 * sk[u]), c, he[u]);
       }
     }
 #pragma unroll
@@ -45,7 +47,6 @@ __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
       sk[u] = sn[u];
     }
   }
-  if (a.last_state) a.last_state[bd * N + n] = c;
 }
 
 int launch_carry(const ScanArgs& a, cudaStream_t s) {

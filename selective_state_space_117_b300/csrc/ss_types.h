@@ -32,6 +32,8 @@ struct ScanArgs {
   int vec_bc;        // 1: every 8-step segment of a B or C row is 16-byte aligned
   int* err;          // device status word (bounded waits record a timeout here), may be null
   int zoh;           // 1: zero-order-hold input weight (exp(dt A) - 1) / A instead of dt
+  int64_t local_chunks;  // the local pass covers chunks 0 .. local_chunks - 1
+  int* perm;         // (dim) workspace for the channel order of the grouped local pass, or null
 };
 
 // Backward pass.  Chunks of kBwdChunk steps; the workspace holds, per (chunk k, b, d),

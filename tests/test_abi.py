@@ -133,12 +133,13 @@ def test_chunked_validation():
 
 
 def test_workspace_bytes():
-    # S: batch*dim*K floats padded to 256 B, then H: batch*dim*K*N floats
-    assert ss.chunked_workspace_bytes(1, 4, 4, 16, 8) == 256 + 1 * 4 * 2 * 4 * 4
+    # S: batch*dim*K floats, then H: batch*dim*K*N floats, each padded to 256 B, then the
+    # channel order of the local pass: dim int32
+    assert ss.chunked_workspace_bytes(1, 4, 4, 16, 8) == 256 + 256 + 4 * 4
     K = 65536 // 2048
-    assert ss.chunked_workspace_bytes(1, 5120, 16, 65536, 2048) == 5120 * K * 4 + 5120 * K * 16 * 4
+    assert ss.chunked_workspace_bytes(1, 5120, 16, 65536, 2048) == 5120 * K * 4 + 5120 * K * 16 * 4 + 5120 * 4
     assert ss.chunked_workspace_bytes(1, 4, 4, 16, 0) == 0
-    assert ss.chunked_workspace_bytes(2, 3, 5, 7, 3) == 256 + 2 * 3 * 3 * 5 * 4
+    assert ss.chunked_workspace_bytes(2, 3, 5, 7, 3) == 256 + 512 + 3 * 4   # H: 360 B padded to 512
 
 
 def _bwd(dims, ws=P, ws_bytes=1 << 40, **over):
