@@ -19,28 +19,34 @@
 // The order only changes which channels share a warp, never a channel's own arithmetic.  Slow
 // groups come first in the grid, so the long items start first and the fast ones fill in behind.
 //
-// Data movement: a warp is its own block (no block barriers).  Each lane copies its channel's u and
-// delta rows of a tile, and one 16-byte piece of the tile's B rows, with cp.async into a ring of
-// kLsSlots tiles; bf16 B rows are widened once per tile into an fp32 [state][step] tile that
-// every lane reads as broadcast 16-byte loads.  Per state and pair of steps: one packed multiply
-// for the exponent, two MUFU.EX2, one packed multiply for the input term, one packed fma.
+// Data movement: a warp is its own block (no block barriers).  Its 32 channels are rows scattered
+// over the (batch * dim, L) arrays, so one lane gathers each 16-step tile of their u and delta rows
+// with tensor-memory-accelerator gathers (cp.async.bulk.tensor ... tile::gather4: four rows by
+// index per instruction, eight per array) and the tile's B rows with one 3-D tensor load, all
+// completing on the slot's mbarrier; a ring of kLsSlots tiles keeps the copies ahead.  (Per-lane
+// 16-byte copies from 32 different rows cost 32 L1 requests per instruction, and the memory
+// instruction queue, not the arithmetic, then bounded the pass.)  bf16 B rows are widened once
+// per tile into an fp32 [state][step] tile that every lane reads as broadcast 16-byte loads.  Per
+// state and pair of steps: one packed multiply for the exponent, two MUFU.EX2, one packed multiply
+// for the input term, one packed fma.  Every wait on an mbarrier is bounded; a wait that gives up
+// stops the warp (no further copy is issued) after the copies in flight have landed.
 #include <type_traits>
 
 #include "ss_kernels.cuh"
 #include "ss_launch.h"
+#include "ss_tma.cuh"
+#include "ss_tma_launch.cuh"
 
 namespace ssk {
 
 namespace {
 
-#ifndef SS_LS_SLOTS
-#define SS_LS_SLOTS 4
-#endif
-#ifndef SS_LS_MINBLOCKS
-#define SS_LS_MINBLOCKS 12
-#endif
 constexpr int kLsSteps = 16;           // steps per tile
-constexpr int kLsSlots = SS_LS_SLOTS;  // tiles in flight per warp
+constexpr int kLsSlots = 4;            // tiles in flight per warp
+// Warps per SM the register budget is set for (1-warp blocks).  Measured on the long sequence:
+// 12 ran the pass in 0.775 ms, 16 in 0.80 (fewer registers), 8 and 10 no faster than 12; ring
+// depths of 3 to 8 tiles and 32-step tiles changed nothing.
+constexpr int kLsMinBlocks = 12;
 constexpr int kBuckets = 64;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kDeadArg = -127.f;     // ex2 of anything below is under 2^-127: 0 after flushing
@@ -79,27 +85,47 @@ __global__ void __launch_bounds__(1024) order_channels_kernel(const ScanArgs a, 
   for (int64_t d = tid; d < a.dim; d += blockDim.x) perm[atomicAdd(&cnt[speed_bucket(a, d)], 1)] = (int)d;
 }
 
+// Tensor maps of one call: u and delta as 2-D (L, batch * dim) arrays gathered by row, B as the
+// 3-D (L, N, batch) array of the other TMA kernels.
+struct LsMaps {
+  CUtensorMap u, delta, B;
+};
+
+constexpr int align128(int x) { return (x + 127) / 128 * 128; }
+
 template <int NT, bool BF>
 struct LsLayout {
   static constexpr int ES = In<BF>::kBytes;
   static constexpr int RB = kLsSteps * ES;     // bytes of one row of a tile: 32 (bf16) or 64 (fp32)
-  static constexpr int CH = RB / 16;           // 16-byte pieces per row
-  static constexpr int kIn = 32 * RB;          // u or delta rows of the warp's 32 channels, piece-major
+  static constexpr int kIn = 32 * RB;          // u or delta rows of the warp's 32 channels, [lane][RB]
   static constexpr int kB = NT * RB;           // the tile's raw B rows, [state][step]
-  static constexpr int kSlot = 2 * kIn + kB;
+  static constexpr int kSlot = align128(2 * kIn + kB);
   static constexpr int kBf = BF ? NT * kLsSteps * 4 : 0;   // B widened to fp32 (bf16 inputs)
-  static constexpr int kBytes = kLsSlots * kSlot + kBf;
-  static constexpr int kBPieces = NT * CH;     // 16-byte pieces of raw B per tile
+  static constexpr int oBf = kLsSlots * kSlot;
+  static constexpr int oRows = oBf + kBf;      // the warp's 32 row indices (b * dim + d)
+  static constexpr int oBar = oRows + 128;
+  static constexpr int kBytes = oBar + kLsSlots * 8;
+  static constexpr int kBPieces = NT * (RB / 16);   // 16-byte pieces of raw B per tile
 };
 
-// A lane's row of a tile (16 steps) as 8 pairs of steps: its 16-byte pieces are stored
-// piece-major ([piece][lane]), so the 32 lanes' reads of one piece are 512 contiguous bytes.
+// Gather of the 16-byte-aligned (x, rows r.x .. r.w) box of a 2-D tensor map: four rows of the
+// map's box width land one after the other at dst, completing on bar.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int4 r) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r.x), "r"(r.y), "r"(r.z), "r"(r.w), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// A lane's row of a tile (kLsSteps steps, RB bytes at lane * RB) as pairs of steps.
 template <bool BF>
 __device__ __forceinline__ void row_pairs(const unsigned char* arr, int lane, f2 (&v)[kLsSteps / 2]) {
+  const unsigned char* row = arr + lane * kLsSteps * In<BF>::kBytes;
   if constexpr (BF) {
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint4 r = *reinterpret_cast<const uint4*>(arr + c * 512 + lane * 16);
+    for (int c = 0; c < kLsSteps / 8; ++c) {
+      const uint4 r = *reinterpret_cast<const uint4*>(row + c * 16);
       v[4 * c] = bf16x2(r.x);
       v[4 * c + 1] = bf16x2(r.y);
       v[4 * c + 2] = bf16x2(r.z);
@@ -107,8 +133,8 @@ __device__ __forceinline__ void row_pairs(const unsigned char* arr, int lane, f2
     }
   } else {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float4 r = *reinterpret_cast<const float4*>(arr + c * 512 + lane * 16);
+    for (int c = 0; c < kLsSteps / 4; ++c) {
+      const float4 r = *reinterpret_cast<const float4*>(row + c * 16);
       v[2 * c] = pk(r.x, r.y);
       v[2 * c + 1] = pk(r.z, r.w);
     }
@@ -122,13 +148,15 @@ __device__ __forceinline__ void row_pairs(const unsigned char* arr, int lane, f2
 constexpr int kLsGroup = 4;
 
 template <int NT, bool BF, bool ZOH>
-__global__ void __launch_bounds__(32, SS_LS_MINBLOCKS) local_sorted_kernel(const ScanArgs a, const int* __restrict__ perm,
-                                                          int64_t kchunks) {
-  using L = In<BF>;
+__global__ void __launch_bounds__(32, kLsMinBlocks)
+    local_sorted_kernel(const ScanArgs a, const int* __restrict__ perm, int64_t kchunks,
+                        const __grid_constant__ LsMaps m) {
   using Lay = LsLayout<NT, BF>;
   constexpr int S = kLsSlots;
   constexpr int NPAIR = kLsSteps / 2;
   __shared__ __align__(128) unsigned char sm[Lay::kBytes];
+  int* rows = reinterpret_cast<int*>(sm + Lay::oRows);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
 
   const int lane = threadIdx.x;
   const int64_t items_per_group = a.batch * kchunks;
@@ -146,7 +174,6 @@ __global__ void __launch_bounds__(32, SS_LS_MINBLOCKS) local_sorted_kernel(const
   // and each group's slowest A' (the last of its states to die).
   constexpr int NG = (NT + kLsGroup - 1) / kLsGroup;
   float Ap[NT], iAs[NT], gmax[NG];
-  float amax = -INFINITY;
 #pragma unroll
   for (int gi = 0; gi < NG; ++gi) gmax[gi] = -INFINITY;
 #pragma unroll
@@ -154,65 +181,81 @@ __global__ void __launch_bounds__(32, SS_LS_MINBLOCKS) local_sorted_kernel(const
     const float an = (n < N) ? a.A[d * N + n] : 0.f;
     Ap[n] = an * kLog2e;
     iAs[n] = an != 0.f ? 1.f / an : 0.f;
-    if (n < N) {
-      amax = fmaxf(amax, Ap[n]);
-      gmax[n / kLsGroup] = fmaxf(gmax[n / kLsGroup], Ap[n]);
-    }
+    if (n < N) gmax[n / kLsGroup] = fmaxf(gmax[n / kLsGroup], Ap[n]);
   }
   const float bias = a.delta_bias ? a.delta_bias[d] : 0.f;
   const f2 bias2 = pk(bias, bias);
   const bool may_stop = a.softplus != 0;
 
-  // Copies of time tile (ntiles - 1 - i) into ring slot i % S (the walk goes backward).
-  const char* urow = static_cast<const char*>(a.u) + (bd * a.seqlen + t_begin) * Lay::ES;
-  const char* drow = static_cast<const char*>(a.delta) + (bd * a.seqlen + t_begin) * Lay::ES;
-  const char* bbase = static_cast<const char*>(a.B) + (b * N * a.seqlen + t_begin) * Lay::ES;
-  auto issue = [&](int i) {
-    unsigned char* s = sm + (i % S) * Lay::kSlot;
-    const int64_t off = (int64_t)(ntiles - 1 - i) * Lay::RB;
-#pragma unroll
-    for (int c = 0; c < Lay::CH; ++c) {
-      cp_async16(smem_addr(s + c * 512 + lane * 16), urow + off + c * 16);
-      cp_async16(smem_addr(s + Lay::kIn + c * 512 + lane * 16), drow + off + c * 16);
-    }
-#pragma unroll
-    for (int q0 = 0; q0 < Lay::kBPieces; q0 += 32) {
-      const int q = q0 + lane, n = q / Lay::CH, c = q % Lay::CH;
-      if (q < Lay::kBPieces && n < N)
-        cp_async16(smem_addr(s + 2 * Lay::kIn + q * 16), bbase + (int64_t)n * a.seqlen * Lay::ES + off + c * 16);
-    }
-  };
-  // Raw B rows of padding states stay zero in every slot.
+  // Raw B rows of padding states stay zero in every slot; the warp's row indices; the barriers.
 #pragma unroll
   for (int q0 = 0; q0 < Lay::kBPieces; q0 += 32) {
     const int q = q0 + lane;
-    if (q < Lay::kBPieces && q / Lay::CH >= N)
+    if (q < Lay::kBPieces && q / (Lay::RB / 16) >= N)
       for (int s = 0; s < S; ++s)
         *reinterpret_cast<uint4*>(sm + s * Lay::kSlot + 2 * Lay::kIn + q * 16) = make_uint4(0, 0, 0, 0);
   }
+  rows[lane] = (int)bd;
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+
+  // Lane 0: copies of time tile (ntiles - 1 - i) into ring slot i % S (the walk goes backward).
+  auto issue = [&](int i) {
+    unsigned char* s = sm + (i % S) * Lay::kSlot;
+    uint64_t* br = &bar[i % S];
+    mbar_expect_tx(br, 2 * Lay::kIn + N * Lay::RB);
+    const int x = (int)(t_begin + (int64_t)(ntiles - 1 - i) * kLsSteps);
 #pragma unroll
-  for (int i = 0; i < S - 1; ++i) {
-    if (i < ntiles) issue(i);
-    cp_async_commit();
+    for (int j = 0; j < 8; ++j) {
+      const int4 r4 = *reinterpret_cast<const int4*>(rows + 4 * j);
+      tma_gather4(s + j * 4 * Lay::RB, &m.u, br, x, r4);
+      tma_gather4(s + Lay::kIn + j * 4 * Lay::RB, &m.delta, br, x, r4);
+    }
+    tma_load_3d(s + 2 * Lay::kIn, &m.B, br, x, 0, (int)b);
+  };
+  int issued = 0;   // tiles whose copies lane 0 has issued
+  if (lane == 0) {
+    prefetch_tensormap(&m.u);
+    prefetch_tensormap(&m.delta);
+    prefetch_tensormap(&m.B);
+  }
+  for (int i = 0; i < S - 1 && i < ntiles; ++i) {
+    if (lane == 0) issue(i);
+    issued = i + 1;
   }
 
   f2 acc[NT];
 #pragma unroll
   for (int n = 0; n < NT; ++n) acc[n] = pk(0.f, 0.f);
   float R = 0.f;   // sum of dt after the current tile
+  bool ok = true;
+  int i = 0;
 
-  for (int i = 0; i < ntiles; ++i) {
-    // Every state of every channel of the warp has underflowed: the rest of the chunk adds zeros.
-    if (may_stop && !__any_sync(kFull, active && amax * R >= kDeadArg)) break;
-    if (i + S - 1 < ntiles) issue(i + S - 1);
-    cp_async_commit();
-    cp_async_wait<S - 1>();
-    __syncwarp();
+  for (; i < ntiles; ++i) {
+    // The groups with a state whose weights have not underflowed in some channel of the warp
+    // (all votes first: they depend only on R, not on this tile's data).  None left: the rest
+    // of the chunk adds zeros.
+    const float R_in = R;
+    unsigned live = 0;
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi)
+      if (gi * kLsGroup < N && (!may_stop || __any_sync(kFull, active && gmax[gi] * R_in >= kDeadArg)))
+        live |= 1u << gi;
+    if (live == 0) break;
+    if (i + S - 1 < ntiles) {   // into the slot of tile i - 1, which every lane has finished with
+      if (lane == 0) issue(i + S - 1);
+      issued = i + S;
+    }
+    ok = __all_sync(kFull, mbar_wait(&bar[i % S], (i / S) & 1, a.err));
+    if (!ok) break;
     const unsigned char* s = sm + (i % S) * Lay::kSlot;
     const float* Bt;
     if constexpr (BF) {
-      // Widen the tile's B rows to fp32: lane q converts piece q (state q / 2, steps 8 (q % 2) ..).
-      float* bf = reinterpret_cast<float*>(sm + S * Lay::kSlot);
+      // Widen the tile's B rows to fp32: lane q converts piece q (8 steps of one state).
+      float* bf = reinterpret_cast<float*>(sm + Lay::oBf);
 #pragma unroll
       for (int q0 = 0; q0 < Lay::kBPieces; q0 += 32) {
         const int q = q0 + lane;
@@ -243,22 +286,14 @@ __global__ void __launch_bounds__(32, SS_LS_MINBLOCKS) local_sorted_kernel(const
         w2[p] = ZOH ? ur[p] : mul2(dt2[p], ur[p]);
       }
     }
-    // Suffix sums over the tile's 8 pairs as a 3-level tree (instead of a chain of 16 adds):
-    // after[p] = sum of dt over pairs p+1 .. 7.
-    const float R_in = R;
+    // after[p] = sum of dt over the pairs after p in the tile (sums of pairs first, then a chain).
     {
       float ps[NPAIR], after[NPAIR];
 #pragma unroll
       for (int p = 0; p < NPAIR; ++p) ps[p] = lo(dt2[p]) + hi(dt2[p]);
-      const float s67 = ps[6] + ps[7], s45 = ps[4] + ps[5], s23 = ps[2] + ps[3], s4567 = s45 + s67;
-      after[7] = 0.f;
-      after[6] = ps[7];
-      after[5] = s67;
-      after[4] = ps[5] + s67;
-      after[3] = s4567;
-      after[2] = ps[3] + s4567;
-      after[1] = s23 + s4567;
-      after[0] = (ps[1] + s23) + s4567;
+      after[NPAIR - 1] = 0.f;
+#pragma unroll
+      for (int p = NPAIR - 2; p >= 0; --p) after[p] = after[p + 1] + ps[p + 1];
 #pragma unroll
       for (int p = 0; p < NPAIR; ++p) {
         const float r_hi = R_in + after[p];
@@ -269,8 +304,7 @@ __global__ void __launch_bounds__(32, SS_LS_MINBLOCKS) local_sorted_kernel(const
 
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
-      if (gi * kLsGroup >= N) break;
-      if (may_stop && !__any_sync(kFull, active && gmax[gi] * R_in >= kDeadArg)) continue;
+      if (!((live >> gi) & 1u)) continue;
 #pragma unroll
       for (int n = gi * kLsGroup; n < (gi + 1) * kLsGroup && n < NT; ++n) {
         if (n >= N) break;
@@ -278,8 +312,8 @@ __global__ void __launch_bounds__(32, SS_LS_MINBLOCKS) local_sorted_kernel(const
         const f2 A2 = pk(Ap[n], Ap[n]);
         f2 sum = acc[n];
         if constexpr (ZOH) {
-          // Weights at the 17 points R_{-1} = R (before the tile), R_0, ..., R_15: the hold weight
-          // of step s is (w(R_{s-1}) - w(R_s)) / A with w(R) = exp(A R).
+          // Weights at the points R_{-1} = R (before the tile), R_0, ..., R_{kLsSteps-1}: the hold
+          // weight of step s is (w(R_{s-1}) - w(R_s)) / A with w(R) = exp(A R).
           const f2 iA2 = pk(iAs[n], iAs[n]);
           float w_prev = ex2(Ap[n] * R);   // w(R_{-1})
 #pragma unroll
@@ -305,9 +339,13 @@ __global__ void __launch_bounds__(32, SS_LS_MINBLOCKS) local_sorted_kernel(const
     }
     __syncwarp();   // every lane is done with this slot and the fp32 B tile before they are refilled
   }
-  cp_async_wait<0>();   // no copy may still be landing in shared memory when the warp exits
+  // Tiles i .. issued - 1 were issued and not waited for (after an early stop, or the tile whose
+  // wait gave up): wait for each (bounded; a completed phase returns at once) before exiting.
+  if (lane == 0)
+    for (int j = i; j < issued; ++j) mbar_wait(&bar[j % S], (j / S) & 1, nullptr);
+  __syncwarp();
 
-  if (!active) return;
+  if (!active || !ok) return;
   const int64_t BD = a.batch * a.dim;
   a.ws_S[k * BD + bd] = R;
   float* H = a.ws_H + (k * BD + bd) * N;
@@ -316,12 +354,32 @@ __global__ void __launch_bounds__(32, SS_LS_MINBLOCKS) local_sorted_kernel(const
     if (n < N) H[n] = lo(acc[n]) + hi(acc[n]);
 }
 
+// (L, rows) row-major array as a 2-D tensor map gathered one row at a time (box: kLsSteps x 1).
+inline bool encode_rows(CUtensorMap* mp, bool bf16, const void* base, int64_t L, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int64_t es = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)L, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(L * es)};
+  cuuint32_t box[2] = {(cuuint32_t)kLsSteps, 1};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(mp, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int NT, bool BF, bool ZOH>
 int go_local_sorted(const ScanArgs& a, int64_t kchunks, cudaStream_t s) {
+  LsMaps m;
+  const int64_t rows = a.batch * a.dim;
+  if (!encode_rows(&m.u, BF, a.u, a.seqlen, rows) || !encode_rows(&m.delta, BF, a.delta, a.seqlen, rows) ||
+      !encode3d(&m.B, BF, false, a.B, a.seqlen, a.dstate, a.batch, kLsSteps, (unsigned)a.dstate,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    return 1;
   const int64_t groups = (a.dim + 31) / 32;
   const int64_t items = groups * a.batch * kchunks;
   order_channels_kernel<<<1, 1024, 0, s>>>(a, a.perm);
-  local_sorted_kernel<NT, BF, ZOH><<<(unsigned)items, 32, 0, s>>>(a, a.perm, kchunks);
+  local_sorted_kernel<NT, BF, ZOH><<<(unsigned)items, 32, 0, s>>>(a, a.perm, kchunks, m);
   return 0;
 }
 
@@ -330,9 +388,9 @@ int go_local_sorted(const ScanArgs& a, int64_t kchunks, cudaStream_t s) {
 bool local_sorted_available(const ScanArgs& a, bool bf16) {
   (void)bf16;
   const int64_t kchunks = a.local_chunks;
-  if (kchunks < 1 || !a.perm) return false;
+  if (kchunks < 1 || !a.perm || !encode_fn()) return false;
   if (a.dstate < 1 || a.dstate > 16 || !a.vec || !a.vec_bc || a.chunk_len % kLsSteps != 0) return false;
-  if (a.dim > (int64_t)INT32_MAX) return false;
+  if (a.batch * a.dim > (int64_t)INT32_MAX || a.seqlen > (int64_t)INT32_MAX) return false;
   const int64_t items = (a.dim + 31) / 32 * a.batch * kchunks;
   return items <= (int64_t)INT32_MAX;
 }
