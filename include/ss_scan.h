@@ -59,7 +59,8 @@ typedef enum {
     SS_EDTYPE = -3,      /* in_dtype is neither SS_F32 nor SS_BF16 */
     SS_EWORKSPACE = -4,  /* chunked workspace missing, too small or misaligned */
     SS_ECUDA = -5,       /* a CUDA launch or call failed (see ss_last_cuda_error) */
-    SS_ETIMEOUT = -6     /* a bounded device-side wait gave up (see ss_device_status) */
+    SS_ETIMEOUT = -6,    /* a bounded device-side wait gave up (see ss_device_status) */
+    SS_EBOUNDS = -7      /* a device-side index check failed (SS_DEBUG_BOUNDS build only) */
 } ss_status;
 
 /* Largest supported state size N. */
@@ -314,12 +315,35 @@ int ss_last_cuda_error(void);
  * The status word of the current device.  Kernels that wait on their own
  * asynchronous bulk copies bound every wait; one that gives up records it in
  * this word, skips the rest of its work and returns (its outputs are then not
- * valid) instead of hanging the device.  Returns SS_OK when no wait has given
- * up since the word was last cleared, SS_ETIMEOUT otherwise, SS_ECUDA if the
- * device could not be queried.  Synchronous: it first waits for all work on
- * the current device (cudaDeviceSynchronize).  clear != 0 resets the word.
+ * valid) instead of hanging the device.  In the debug build (below), a failed
+ * index check is recorded there too.  Returns SS_OK when nothing has been
+ * recorded since the word was last cleared, SS_EBOUNDS when an index check
+ * failed, SS_ETIMEOUT when a wait gave up, SS_ECUDA if the device could not be
+ * queried.  Synchronous: it first waits for all work on the current device
+ * (cudaDeviceSynchronize).  clear != 0 resets the word.
  */
 int ss_device_status(int clear);
+
+/*
+ * The debug build.  Compiled with SS_DEBUG_BOUNDS (python -m
+ * selective_state_space_117_b300.build --debug-bounds, which writes
+ * libssscan_debug.so beside libssscan.so), every kernel checks the index
+ * ranges it derives (rows of the inputs and outputs, the batch row of B and C,
+ * A rows, state rows, workspace entries, the channel order) against the sizes
+ * in ss_dims before using them.  A range outside its array is recorded in the
+ * device status word (ss_device_status then returns SS_EBOUNDS) and the
+ * accesses it guards are skipped: the kernel never traps and never touches
+ * memory outside the arrays the dims describe.  The checks cannot see the
+ * caller's allocation sizes, only the dims.  In the normal build they compile
+ * away.  ss_debug_bounds_build returns 1 in the debug build, 0 otherwise.
+ *
+ * ss_selftest_bounds launches one check of a span known to lie outside its
+ * array (nothing is accessed): in the debug build it records SS_EBOUNDS, in
+ * the normal build nothing.  Asynchronous on `stream`; SS_ECUDA if the launch
+ * failed.
+ */
+int ss_debug_bounds_build(void);
+int ss_selftest_bounds(ss_stream_t stream);
 
 /*
  * Diagnostic of the failure path above: launches one thread that waits, with

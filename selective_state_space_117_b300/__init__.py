@@ -27,7 +27,8 @@ __all__ = ["scan_fwd", "scan_chunked", "scan_bwd", "bwd_workspace_bytes", "state
            "F32", "BF16", "MAX_DSTATE", "LAUNCHES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "libssscan.so")
+# SS_LIBRARY=debug loads the debug build (device-side index checks, libssscan_debug.so).
+_LIB_PATH = os.path.join(_HERE, "libssscan_debug.so" if os.environ.get("SS_LIBRARY") == "debug" else "libssscan.so")
 _lib = None
 
 F32, BF16 = 0, 1
@@ -36,7 +37,7 @@ MAX_DSTATE = 64
 # (the first two only when there is more than one chunk).
 LAUNCHES = {"scan_fwd": 1, "scan_chunked": 4, "state_update": 1, "scan_bwd": 5}
 
-SS_OK, SS_EINVAL, SS_EALIGN, SS_EDTYPE, SS_EWORKSPACE, SS_ECUDA, SS_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
+SS_OK, SS_EINVAL, SS_EALIGN, SS_EDTYPE, SS_EWORKSPACE, SS_ECUDA, SS_ETIMEOUT, SS_EBOUNDS = 0, -1, -2, -3, -4, -5, -6, -7
 
 
 class SSError(RuntimeError):
@@ -104,6 +105,10 @@ def lib():
         L.ss_device_status.restype = ctypes.c_int
         L.ss_measure_ex2.argtypes = [i64, ctypes.c_int, vp, ctypes.POINTER(ctypes.c_uint64), vp]
         L.ss_measure_ex2.restype = ctypes.c_int
+        L.ss_selftest_bounds.argtypes = [vp]
+        L.ss_selftest_bounds.restype = ctypes.c_int
+        L.ss_debug_bounds_build.argtypes = []
+        L.ss_debug_bounds_build.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -365,9 +370,22 @@ def device_status(clear: bool = False) -> int:
     """Status word of the current device (ss_device_status): SS_OK, or SS_ETIMEOUT
     when a kernel's bounded wait gave up.  Synchronises the device first."""
     st = lib().ss_device_status(int(bool(clear)))
-    if st not in (SS_OK, SS_ETIMEOUT):
+    if st not in (SS_OK, SS_ETIMEOUT, SS_EBOUNDS):
         _check(st, "ss_device_status")
     return st
+
+
+def selftest_bounds(device=None, stream=None):
+    """Launch the diagnostic index check of a span outside its array (ss_selftest_bounds): the
+    debug build records SS_EBOUNDS, the normal build nothing; read it with device_status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib().ss_selftest_bounds(_stream(dev, stream)), "ss_selftest_bounds")
+
+
+def debug_bounds_build() -> bool:
+    """Whether the loaded library is the debug build (SS_DEBUG_BOUNDS)."""
+    return bool(lib().ss_debug_bounds_build())
 
 
 def selftest_wait_timeout(device=None, stream=None):

@@ -364,6 +364,7 @@ int ss_causal_conv1d(const ss_dims* dims, const void* x, const float* weight, co
   a.x = x; a.w = weight; a.bias = bias; a.out = out;
   a.rows = d.batch * d.dim; a.dim = d.dim; a.seqlen = d.seqlen;
   a.nseg = ssk::conv1d_segments(d.seqlen);
+  a.err = device_status_word(reinterpret_cast<cudaStream_t>(stream));
   a.vec = ((d.seqlen * (int64_t)es) % 16 == 0 && aligned(x, 16) && aligned(out, 16)) ? 1 : 0;
   if (ssk::launch_conv1d(a, d.in_dtype == SS_BF16, silu_flag != 0, reinterpret_cast<cudaStream_t>(stream)) != 0)
     return SS_EINVAL;
@@ -453,6 +454,7 @@ int ss_scan_bwd(const ss_dims* dims, const float* h0, const void* u, const void*
   a.batch = d.batch; a.dim = d.dim; a.dstate = d.dstate; a.seqlen = d.seqlen; a.nchunks = K;
   a.softplus = softplus_flag ? 1 : 0;
   a.zoh = (d.flags & SS_FLAG_ZOH) ? 1 : 0;
+  a.err = f.err;
   const size_t es = in_size(d.in_dtype);
   const bool rows16 = (d.seqlen * (int64_t)es) % 16 == 0 && (d.seqlen * 4) % 16 == 0;
   a.vec = (rows16 && aligned(u, 16) && aligned(delta, 16) && aligned(z, 16) && aligned(dy, 16) && aligned(du, 16) &&
@@ -473,6 +475,7 @@ const char* ss_status_string(int status) {
     case SS_EWORKSPACE: return "SS_EWORKSPACE: workspace missing, misaligned or too small";
     case SS_ECUDA: return "SS_ECUDA: CUDA launch or call failed";
     case SS_ETIMEOUT: return "SS_ETIMEOUT: a bounded device wait ran out";
+    case SS_EBOUNDS: return "SS_EBOUNDS: a device-side index check failed (debug build)";
     default: return "unknown ss_status";
   }
 }
@@ -508,7 +511,24 @@ int ss_device_status(int clear) {
     e = cudaMemset(word, 0, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e);
   }
+  if (v & ssk::kDevBounds) return SS_EBOUNDS;
   return v == 0 ? SS_OK : SS_ETIMEOUT;
+}
+
+int ss_selftest_bounds(ss_stream_t stream) {
+  cudaError_t e = cudaSuccess;
+  int* word = device_status_word(reinterpret_cast<cudaStream_t>(stream), &e);
+  if (!word) return cuda_fail(e);
+  ssk::launch_bounds_check(word, reinterpret_cast<cudaStream_t>(stream));
+  return launched();
+}
+
+int ss_debug_bounds_build(void) {
+#ifdef SS_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 }  // extern "C"

@@ -130,6 +130,13 @@ __global__ void __launch_bounds__(kCh) bwd_local_kernel(const BwdArgs a) {
   stage_bc<NT, BF>(sC, a.C, b * N * L, N, L, t0, t_end, a.vec_bc, tid, kCh);
   __syncthreads();
   if (!active) return;
+  // Debug build: the channel's rows of delta/dy/z, its A row and its entry of the adjoint sums.
+  {
+    const int64_t BD = a.batch * a.dim, bd = b * a.dim + d;
+    if (!span_ok(a.err, bd * L + t0, t_end - t0, BD * L) || !span_ok(a.err, d * N, N, a.dim * N) ||
+        !span_ok(a.err, (k * BD + bd) * N, N, a.nchunks * BD * N))
+      return;
+  }
 
   f2 A2[NP], acc[NP];
   const float* Arow = a.A + d * N;
@@ -185,6 +192,9 @@ __global__ void __launch_bounds__(256) bwd_carry_kernel(const BwdArgs a) {
   const int64_t n = i % N, bd = i / N, d = bd % a.dim;
   const float A2 = a.A[d * N + n] * kLog2e;
   const int64_t K = a.nchunks, BD = a.batch * a.dim;
+  // Debug build: the column of every chunk's entry (the last one farthest out).
+  if (!span_ok(a.err, (K - 1) * BD * N + bd * N + n, 1, K * BD * N) || !span_ok(a.err, (K - 1) * BD + bd, 1, K * BD))
+    return;
   float* G = a.ws_G + bd * N + n;            // chunk k at G[k * BD * N]
   const float* S = a.ws_S + bd;              // chunk k at S[k * BD]
   float mu = a.dlast ? a.dlast[bd * N + n] : 0.f;
@@ -275,6 +285,17 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   const int N = (int)a.dstate;
   const int64_t L = a.seqlen, t0 = k * kBwdChunk, t_end = min(L, t0 + kBwdChunk);
   const int64_t bc_row = b * N * L;
+  // Debug build: the block's rows (first to last channel) over the chunk, the batch row of
+  // B/C/dB/dC, its channels' A rows and their workspace entries (the whole block leaves before
+  // any barrier when one is outside).
+  {
+    const int64_t BD = a.batch * a.dim, dl = min(a.dim, d0 + kCpb) - 1;
+    const int64_t r0 = (b * a.dim + d0) * L + t0, r1 = (b * a.dim + dl) * L + t_end;
+    if (!span_ok(a.err, r0, r1 - r0, BD * L) || !span_ok(a.err, bc_row, N * L, a.batch * N * L) ||
+        !span_ok(a.err, d0 * N, (dl - d0 + 1) * N, a.dim * N) ||
+        !span_ok(a.err, (k * BD + b * a.dim + d0) * N, (dl - d0 + 1) * N, a.nchunks * BD * N))
+      return;
+  }
 
   // ---- prologue: B and C of the chunk, dt and du of every (channel, step), this
   // lane's A, entering state and carried gradient.  All of its global loads are

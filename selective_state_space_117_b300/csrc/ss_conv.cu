@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const ConvArgs a) 
   if (row >= a.rows) return;                       // whole warps leave together
   const int64_t d = row % a.dim;
   const int64_t base = row * a.seqlen;
+  // Debug build: the row and the channel's taps.
+  if (!span_ok(a.err, base, a.seqlen, a.rows * a.seqlen) || !span_ok(a.err, d * 4, 4, a.dim * 4)) return;
   const float4 w = *reinterpret_cast<const float4*>(a.w + d * 4);
   const float bias = a.bias ? a.bias[d] : 0.f;
   const int64_t t_seg = seg * (int64_t)kSegWindows * 256;

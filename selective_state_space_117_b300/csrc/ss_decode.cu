@@ -53,6 +53,10 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeArgs
   const int N = (int)a.dstate;
   const int64_t b = blockIdx.y;
   const int64_t c = b * a.dim + d;               // flattened (b, d)
+  // Debug build: this channel's inputs, state row, A row and the batch row of B and C.
+  if (!span_ok(a.err, c, 1, a.batch * a.dim) || !span_ok(a.err, c * N, N, a.batch * a.dim * N) ||
+      !span_ok(a.err, (int64_t)d * N, N, a.dim * N) || !span_ok(a.err, b * N, N, a.batch * N))
+    return;
   const int n0 = SPL * l;
   const uint64_t keep = policy_keep();
 
@@ -182,6 +186,11 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const Decod
   const int N = (int)a.dstate;
   const unsigned bytes = (unsigned)(nch * N * 4);
   float* gst = a.state + (b * a.dim + c0) * N;
+  // Debug build: the block's contiguous range of the state, and the batch row of B and C (the
+  // whole block leaves before any copy or barrier when one is outside).
+  if (!span_ok(a.err, (b * a.dim + c0) * N, (int64_t)nch * N, a.batch * a.dim * N) ||
+      !span_ok(a.err, b * N, N, a.batch * N))
+    return;
   const uint64_t keep = policy_keep();
   if (tid == 0) {
     mbar_init(&bar, 1);

@@ -14,9 +14,29 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ss_types.h"
+
 namespace ssk {
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Index checks of the debug build.  span_ok(err, start, count, total) says whether elements
+// [start, start + count) lie inside an array of `total` elements; a span outside is recorded in
+// the status word (kDevBounds) and the caller then skips the accesses it guards.  Compiled
+// with SS_DEBUG_BOUNDS only: in the normal build it is the constant true and the checks vanish.
+__device__ __forceinline__ void record_bounds(int* err) {
+  if (err) atomicOr(err, kDevBounds);
+}
+__device__ __forceinline__ bool span_ok(int* err, int64_t start, int64_t count, int64_t total) {
+#ifdef SS_DEBUG_BOUNDS
+  if (start >= 0 && count >= 0 && start <= total - count) return true;
+  record_bounds(err);
+  return false;
+#else
+  (void)err; (void)start; (void)count; (void)total;
+  return true;
+#endif
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float r;

@@ -101,6 +101,19 @@ __device__ __forceinline__ Unit unit_of(const ScanArgs& a) {
   return w;
 }
 
+// Debug-build bounds of a unit: its rows of u/delta/z/y, of B/C, its A row, its state rows
+// (h0, last_state) and its workspace entries.  Always true in the normal build.
+__device__ __forceinline__ bool unit_ok(const ScanArgs& a, const Unit& w) {
+  const int64_t N = a.dstate, BD = a.batch * a.dim;
+  bool ok = span_ok(a.err, w.row + w.t_begin, w.t_end - w.t_begin, BD * a.seqlen);
+  ok = span_ok(a.err, w.bc_row, N * a.seqlen, a.batch * N * a.seqlen) && ok;
+  ok = span_ok(a.err, w.d * N, N, a.dim * N) && ok;
+  ok = span_ok(a.err, w.bd * N, N, BD * N) && ok;
+  if (a.ws_H) ok = span_ok(a.err, (w.k * BD + w.bd) * N, N, a.nchunks * BD * N) && ok;
+  if (a.ws_S) ok = span_ok(a.err, w.k * BD + w.bd, 1, a.nchunks * BD) && ok;
+  return ok;
+}
+
 // Per-step scalars of one 8-step group: dt, du = dt*u as pairs (steps 2p, 2p+1).
 template <bool BF>
 __device__ __forceinline__ void step_scalars(const typename In<BF>::Raw8& ru, const typename In<BF>::Raw8& rd,
@@ -189,7 +202,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) scan_kernel(c
   __shared__ __align__(16) unsigned char sIn[RingT::kBytes];
 
   const int tid = threadIdx.x;
-  const Unit w = unit_of(a);
+  Unit w = unit_of(a);
+  w.active = w.active && unit_ok(a, w);
   const int N = (int)a.dstate;
 
   // Padding states n >= N keep B = C = 0 (their staged values are zero), A = 0 and h = 0.
@@ -352,7 +366,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value)) local_kernel(
   __shared__ __align__(16) unsigned char sIn[RingT::kBytes];
 
   const int tid = threadIdx.x;
-  const Unit w = unit_of(a);
+  Unit w = unit_of(a);
+  w.active = w.active && unit_ok(a, w);
   const int N = (int)a.dstate;
 
   f2 A2[NP], iA2[NP], wc[NP], acc[NP];

@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
 
   const int tid = threadIdx.x;
-  const Unit w = unit_of(a);
+  Unit w = unit_of(a);
+  w.active = w.active && unit_ok(a, w);
   const int N = (int)a.dstate;
   const int ct = blockIdx.x % a.ctiles;
   const int ntiles = (int)((w.t_end - w.t_begin + TS - 1) / TS);
@@ -255,7 +256,8 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
 
   const int tid = threadIdx.x;
-  const Unit w = unit_of(a);
+  Unit w = unit_of(a);
+  w.active = w.active && unit_ok(a, w);
   const int N = (int)a.dstate;
   const int ct = blockIdx.x % a.ctiles;
   const int ntiles = (int)((w.t_end - w.t_begin + TS - 1) / TS);

@@ -48,6 +48,9 @@ int launch_scan_warp(const ScanArgs& a, bool bf16, bool has_z, cudaStream_t s);
 
 // Diagnostic: one bounded mbarrier wait that runs out and records the timeout in *err.
 int launch_wait_timeout(int* err, cudaStream_t s);
+// Diagnostic: one debug-build index check of a span outside its array (nothing is accessed);
+// records kDevBounds in *err in the SS_DEBUG_BOUNDS build, nothing in the normal one.
+int launch_bounds_check(int* err, cudaStream_t s);
 
 // Measurement: `blocks` blocks of kEx2Threads threads, each thread running kEx2Chains
 // chains of `iters` ex2.approx.ftz.f32 links (ss_peak.cu); sink is written never.

@@ -53,25 +53,48 @@ constexpr float kDeadArg = -127.f;     // ex2 of anything below is under 2^-127:
 
 // Speed bucket of channel d: the slowest state's decay per step at the typical step size,
 // softplus(bias) * min_n(-A[d, n]), on a log scale (2 buckets per octave, slowest first).  A
-// channel with a state that does not decay (-A <= 0) goes to bucket 0.
+// channel with a state that does not decay (-A <= 0) goes to bucket 0.  The A row is read with
+// independent loads (16-byte ones when the row allows), so their latencies overlap.
 __device__ __forceinline__ int speed_bucket(const ScanArgs& a, int64_t d) {
   const int N = (int)a.dstate;
+  const float* row = a.A + d * N;
   float rate = INFINITY;
-  for (int n = 0; n < N; ++n) rate = fminf(rate, -a.A[d * N + n]);
+  if ((N & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 4
+    for (int q = 0; q < N / 4; ++q) {
+      const float4 v = __ldg(r4 + q);
+      rate = fminf(rate, fminf(fminf(-v.x, -v.y), fminf(-v.z, -v.w)));
+    }
+  } else {
+#pragma unroll 4
+    for (int n = 0; n < N; ++n) rate = fminf(rate, -__ldg(row + n));
+  }
   if (!(rate > 0.f)) return 0;
-  const float key = softplus(a.delta_bias ? a.delta_bias[d] : 0.f) * rate;
+  const float key = softplus(a.delta_bias ? __ldg(a.delta_bias + d) : 0.f) * rate;
   if (!(key > 0.f)) return 0;
   const int b = (int)floorf(__log2f(key) * 2.f) + 48;
   return min(max(b, 1), kBuckets - 1);
 }
 
-// perm[0 .. dim) = the channels in increasing speed bucket (one block).
+// Channels whose buckets the order kernel keeps in shared memory between its two passes (beyond
+// this, the second pass computes them again).
+constexpr int kOrderSmem = 32768;
+
+// perm[0 .. dim) = the channels in increasing speed bucket (one block): count the buckets, take
+// the running sums, then place every channel.
 __global__ void __launch_bounds__(1024) order_channels_kernel(const ScanArgs a, int* perm) {
   __shared__ int cnt[kBuckets];
+  __shared__ unsigned char sb[kOrderSmem];
   const int tid = threadIdx.x;
+  const bool keep = a.dim <= kOrderSmem;
   if (tid < kBuckets) cnt[tid] = 0;
   __syncthreads();
-  for (int64_t d = tid; d < a.dim; d += blockDim.x) atomicAdd(&cnt[speed_bucket(a, d)], 1);
+  for (int64_t d = tid; d < a.dim; d += blockDim.x) {
+    const int bk = speed_bucket(a, d);
+    if (keep) sb[d] = (unsigned char)bk;
+    atomicAdd(&cnt[bk], 1);
+  }
   __syncthreads();
   if (tid == 0) {
     int run = 0;
@@ -82,7 +105,10 @@ __global__ void __launch_bounds__(1024) order_channels_kernel(const ScanArgs a, 
     }
   }
   __syncthreads();
-  for (int64_t d = tid; d < a.dim; d += blockDim.x) perm[atomicAdd(&cnt[speed_bucket(a, d)], 1)] = (int)d;
+  for (int64_t d = tid; d < a.dim; d += blockDim.x) {
+    const int pos = atomicAdd(&cnt[keep ? sb[d] : speed_bucket(a, d)], 1);
+    if (span_ok(a.err, pos, 1, a.dim)) perm[pos] = (int)d;
+  }
 }
 
 // Tensor maps of one call: u and delta as 2-D (L, batch * dim) arrays gathered by row, B as the
@@ -164,11 +190,21 @@ __global__ void __launch_bounds__(32, kLsMinBlocks)
   const int64_t b = rem / kchunks, k = rem % kchunks;
   const int N = (int)a.dstate;
   const int64_t slot = g * 32 + lane;
-  const bool active = slot < a.dim;
-  const int64_t d = perm[active ? slot : a.dim - 1];
-  const int64_t bd = b * a.dim + d;
+  const int64_t BD = a.batch * a.dim;
+  bool active = slot < a.dim;
+  int64_t d = perm[active ? slot : a.dim - 1];
   const int64_t t_begin = k * a.chunk_len;
   const int ntiles = (int)(a.chunk_len / kLsSteps);   // the launcher guarantees whole tiles
+  // Debug build: the channel, its rows of u/delta and B, its A row and workspace entries.
+  if (!span_ok(a.err, d, 1, a.dim)) d = 0, active = false;
+  const int64_t bd = b * a.dim + d;
+  {
+    const int64_t N = a.dstate;
+    bool inb = span_ok(a.err, bd * a.seqlen + t_begin, a.chunk_len, BD * a.seqlen);
+    inb = span_ok(a.err, b * N * a.seqlen + t_begin, (N - 1) * a.seqlen + a.chunk_len, a.batch * N * a.seqlen) && inb;
+    inb = span_ok(a.err, (k * BD + bd) * N, N, a.nchunks * BD * N) && span_ok(a.err, k, 1, a.nchunks) && inb;
+    active = active && inb;
+  }
 
   // Per-state constants: A' = A * log2(e) (0 for padding states, which are never processed),
   // and each group's slowest A' (the last of its states to die).
@@ -346,7 +382,6 @@ __global__ void __launch_bounds__(32, kLsMinBlocks)
   __syncwarp();
 
   if (!active || !ok) return;
-  const int64_t BD = a.batch * a.dim;
   a.ws_S[k * BD + bd] = R;
   float* H = a.ws_H + (k * BD + bd) * N;
 #pragma unroll

@@ -19,6 +19,9 @@ __global__ void __launch_bounds__(256) carry_kernel(const ScanArgs a) {
   const int64_t n = i % N, bd = i / N, d = bd % a.dim;
   const float A2 = a.A[d * N + n] * kLog2e;
   const int64_t K = a.nchunks, BD = a.batch * a.dim;
+  // Debug build: the column of every chunk's entry (the last one farthest out), and h0.
+  if (!span_ok(a.err, (K - 1) * BD * N + bd * N + n, 1, K * BD * N) || !span_ok(a.err, (K - 1) * BD + bd, 1, K * BD))
+    return;
   float* H = a.ws_H + bd * N + n;            // chunk k at H[k * BD * N]
   const float* S = a.ws_S + bd;              // chunk k at S[k * BD]
   float c = a.h0 ? a.h0[bd * N + n] : 0.f;  // the state entering chunk 0

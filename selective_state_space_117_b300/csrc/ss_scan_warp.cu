@@ -90,9 +90,12 @@ __global__ void __launch_bounds__(32 * kWW, 1) scan_warp_kernel(const ScanArgs a
   const int64_t b = blockIdx.y;
   const int ww = blockDim.x >> 5;        // warps (channels) in this block
   const int64_t d = (int64_t)blockIdx.x * ww + warp;
-  const bool active = d < a.dim;
   const int N = (int)a.dstate;
   const int64_t Lsq = a.seqlen;
+  // Debug build: the channel's rows, its A row, its state rows and the batch row of B and C.
+  const bool active = d < a.dim && span_ok(a.err, (b * a.dim + d) * Lsq, Lsq, a.batch * a.dim * Lsq) &&
+                      span_ok(a.err, d * N, N, a.dim * N) && span_ok(a.err, (b * a.dim + d) * N, N, a.batch * a.dim * N) &&
+                      span_ok(a.err, b * N * Lsq, N * Lsq, a.batch * N * Lsq);
   const int64_t bd = b * a.dim + (active ? d : 0);
   const int64_t row = bd * Lsq;
   const int nseg = (int)((Lsq + kWS - 1) / kWS);

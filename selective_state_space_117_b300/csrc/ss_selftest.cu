@@ -19,7 +19,18 @@ __global__ void wait_timeout_kernel(int* err) {
   }
 }
 
+// The check of a span of 4 elements starting at 2 in an array of 5: outside, so the debug
+// build records it.  Nothing is accessed either way.
+__global__ void bounds_check_kernel(int* err) {
+  if (threadIdx.x == 0) (void)span_ok(err, 2, 4, 5);
+}
+
 }  // namespace
+
+int launch_bounds_check(int* err, cudaStream_t s) {
+  bounds_check_kernel<<<1, 32, 0, s>>>(err);
+  return 0;
+}
 
 int launch_wait_timeout(int* err, cudaStream_t s) {
   wait_timeout_kernel<<<1, 32, 0, s>>>(err);

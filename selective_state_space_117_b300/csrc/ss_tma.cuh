@@ -15,10 +15,6 @@
 
 namespace ssk {
 
-// Device status word values (shared with the host API).
-constexpr int kDevOk = 0;
-constexpr int kDevTimeout = 1;
-
 // A wait gives up after kWaitNs of the global timer.  A poll of an incomplete
 // phase can itself suspend the thread for a few microseconds, so the limit is
 // kept in time, not in polls; kMaxSpins only backs it up should the timer not
@@ -69,7 +65,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, int* e
     if (i > 64) __nanosleep(128);
     if ((i & 255) == 255 && global_ns() - t0 > kWaitNs) break;
   }
-  if (err) atomicExch(err, kDevTimeout);
+  if (err) atomicOr(err, kDevTimeout);
   return false;
 }
 

@@ -6,6 +6,11 @@
 namespace ssk {
 
 constexpr int kCh = 64;        // channels (threads) per scan block
+
+// Bits of the per-device status word that kernels write (atomicOr) instead of trapping.
+constexpr int kDevOk = 0;
+constexpr int kDevTimeout = 1;   // a bounded wait on an asynchronous copy gave up
+constexpr int kDevBounds = 2;    // a debug-build index check failed (SS_DEBUG_BOUNDS)
 constexpr int kGroup = 8;      // time steps per vector load
 constexpr int kDecodeThreads = 256;
 
@@ -73,6 +78,7 @@ struct BwdArgs {
   int vec;               // 1: u/delta/z rows, dy and the fp32 gradient rows allow 16-byte group loads
   int vec_bc;            // 1: B/C rows allow 16-byte loads of 8-step groups
   int zoh;               // 1: zero-order-hold input weight
+  int* err;              // device status word (debug-build index checks record here), may be null
 };
 
 // Causal depthwise conv1d of width 4 over (rows = batch * dim, seqlen).
@@ -83,6 +89,7 @@ struct ConvArgs {
   void* out;
   int64_t rows, dim, seqlen, nseg;
   int vec;             // 1: rows are 16-byte aligned for 8-element vectors
+  int* err;            // device status word (debug-build index checks record here), may be null
 };
 
 // One decode step, one thread per (b, d).
