@@ -152,33 +152,34 @@ constexpr float kLn2 = 0.6931471805599453f;
 // error of about 2^-22, so e - 1 is good to about 2.4e-7 / 0.1 = 2.4e-6 relative.
 // Below, where e - 1 would cancel, it is dt * E(dt A) with E(y) = (exp(y) - 1) / y
 // = 1 + y/2 + y^2/6 + y^3/24 + ..., cut after y^3 (truncation below 1e-6
-// relative for |y| < 1/10; the series also gives the limit dt at A = 0).
+// relative for |y| < 1/10; the series also gives the limit dt at A = 0).  The series
+// is evaluated in arg = y / ln 2 directly (its coefficients carry the powers of ln 2),
+// and the bound is taken on |arg| < 0.1 / ln 2.
 constexpr float kHoldSeriesBelow = 0.1f;
+constexpr float kHoldArgBelow = kHoldSeriesBelow / kLn2;
 
-__device__ __forceinline__ f2 hold_series2(f2 y) {
-  f2 p = splat(1.f / 24.f);
-  p = fma2(p, y, splat(1.f / 6.f));
-  p = fma2(p, y, splat(0.5f));
-  return fma2(p, y, splat(1.f));
+__device__ __forceinline__ f2 hold_series_arg2(f2 arg) {
+  f2 p = splat(kLn2 * kLn2 * kLn2 / 24.f);
+  p = fma2(p, arg, splat(kLn2 * kLn2 / 6.f));
+  p = fma2(p, arg, splat(kLn2 / 2.f));
+  return fma2(p, arg, splat(1.f));
 }
 
 __device__ __forceinline__ f2 hold2(f2 arg, f2 e, f2 dtp, f2 inv_a) {
-  const f2 y = mul2(arg, splat(kLn2));
-  const f2 small = mul2(hold_series2(y), dtp);
+  const f2 small = mul2(hold_series_arg2(arg), dtp);
   const f2 large = mul2(add2(e, splat(-1.f)), inv_a);
-  return pk(fabsf(lo(y)) < kHoldSeriesBelow ? lo(small) : lo(large),
-            fabsf(hi(y)) < kHoldSeriesBelow ? hi(small) : hi(large));
+  return pk(fabsf(lo(arg)) < kHoldArgBelow ? lo(small) : lo(large),
+            fabsf(hi(arg)) < kHoldArgBelow ? hi(small) : hi(large));
 }
 
 // The same weight when the two exponentials at the ends of the step are known:
 // w_next = exp(A (R + dt)) and w_cur = exp(A R) give (w_next - w_cur) / A =
-// w_cur * (exp(dt A) - 1) / A, used by the backward local pass.
+// w_cur * (exp(dt A) - 1) / A, used by the local passes.
 __device__ __forceinline__ f2 hold_between2(f2 w_next, f2 w_cur, f2 arg_dt, f2 dtp, f2 inv_a) {
-  const f2 y = mul2(arg_dt, splat(kLn2));
-  const f2 small = mul2(mul2(hold_series2(y), dtp), w_cur);
+  const f2 small = mul2(mul2(hold_series_arg2(arg_dt), dtp), w_cur);
   const f2 large = mul2(add2(w_next, mul2(w_cur, splat(-1.f))), inv_a);
-  return pk(fabsf(lo(y)) < kHoldSeriesBelow ? lo(small) : lo(large),
-            fabsf(hi(y)) < kHoldSeriesBelow ? hi(small) : hi(large));
+  return pk(fabsf(lo(arg_dt)) < kHoldArgBelow ? lo(small) : lo(large),
+            fabsf(hi(arg_dt)) < kHoldArgBelow ? hi(small) : hi(large));
 }
 
 // ---------------------------------------------------------------- bf16
