@@ -722,8 +722,8 @@ def bwd_counts(batch, dim, dstate, seqlen, in_bytes=2):
 
 def bench_bwd(ss, I, torch, p, pk, fwd_ms, reps=5):
     """ss_scan_bwd on the long-sequence workload: the gradients of sum(dy y) + sum(dlast h_last)
-    for every input (forward local pass and carry at 64-step chunks, adjoint local pass and
-    carry, main pass: five kernels and five memsets per call)."""
+    for every input (both local passes in one kernel at 64-step chunks, the forward and the
+    adjoint carry, main pass: four kernels and five memsets per call)."""
     ct = I.cotangents(seed=103, batch=p.batch, dim=p.dim, dstate=p.dstate, seqlen=p.seqlen, with_h0=False,
                       device="cuda", gen_device="cuda")
     ws = torch.empty((ss.bwd_workspace_bytes(p.batch, p.dim, p.dstate, p.seqlen, ss.BF16),), dtype=torch.uint8,
@@ -763,7 +763,7 @@ def bench_bwd(ss, I, torch, p, pk, fwd_ms, reps=5):
             "entry_point": "ss_scan_bwd", "ms": round(ms, 4), "elem_per_s": elems / (ms * 1e-3),
             "algorithmic_bytes": byts, "exps": exps, "roofline": roof,
             "time_vs_forward_step": round(ms / fwd_ms, 2) if fwd_ms else None,
-            "zoh_ms": round(zoh_ms, 4), "gpu_launches": 5 * (2 * reps + 1)}
+            "zoh_ms": round(zoh_ms, 4), "gpu_launches": 4 * (2 * reps + 1)}
 
 
 def bench_conv(ss, torch, pk, batch=1, dim=5120, seqlen=65536, reps=20):

@@ -426,23 +426,19 @@ int ss_scan_bwd(const ss_dims* dims, const float* h0, const void* u, const void*
     return e == cudaSuccess ? SS_OK : cuda_fail(e);
   }
 
-  // The state entering every chunk: the forward local pass and carry at the backward's chunk length.
+  // Workspace: the chunks' dt sums, forward end states (then the states entering them) and
+  // adjoint sums (then the gradients leaving them), at the backward's chunk length.
   ssk::ScanArgs f = make_scan_args(d, u, delta, A, B, C, D, z, delta_bias, softplus_flag, nullptr, nullptr,
                                    ssk::kBwdChunk, s);
   f.h0 = h0;
   const int64_t K = f.nchunks;
-  f.local_chunks = K;   // the adjoint carry also needs the last chunk's dt sum
+  f.local_chunks = K;   // the carry combines every chunk the local passes covered
   char* ws = static_cast<char*>(workspace);
   const size_t s_bytes = align_up((size_t)(d.batch * d.dim * K) * sizeof(float), kWsAlign);
   const size_t h_bytes = align_up((size_t)(d.batch * d.dim * K * d.dstate) * sizeof(float), kWsAlign);
   f.ws_S = reinterpret_cast<float*>(ws);
   f.ws_H = reinterpret_cast<float*>(ws + s_bytes);
   const bool bf = d.in_dtype == SS_BF16;
-  const dim3 grid((unsigned)(f.ctiles * K), (unsigned)d.batch);
-  if (!(ssk::tma_available(f, bf, ssk::kLocal) && ssk::launch_local_tma(f, bf, grid, s) == 0) &&
-      ssk::launch_scan_local(f, bf, grid, s) != 0)
-    return SS_EINVAL;
-  if (ssk::launch_carry(f, s) != 0) return SS_EINVAL;
 
   ssk::BwdArgs a{};
   a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias;
@@ -460,6 +456,8 @@ int ss_scan_bwd(const ss_dims* dims, const float* h0, const void* u, const void*
   a.vec = (rows16 && aligned(u, 16) && aligned(delta, 16) && aligned(z, 16) && aligned(dy, 16) && aligned(du, 16) &&
            aligned(ddelta, 16) && aligned(dz, 16) && aligned(dB, 8) && aligned(dC, 8)) ? 1 : 0;
   a.vec_bc = ((d.seqlen * (int64_t)es) % 16 == 0 && aligned(B, 16) && aligned(C, 16)) ? 1 : 0;
+  if (ssk::launch_bwd_locals(a, bf, z != nullptr, s) != 0) return SS_EINVAL;
+  if (ssk::launch_carry(f, s) != 0) return SS_EINVAL;
   const int lrc = ssk::launch_bwd(a, bf, z != nullptr, s);
   if (lrc < 0) return SS_EINVAL;                             // unsupported dstate (caught above)
   if (lrc > 0) return cuda_fail(cudaGetLastError());         // the kernel attribute could not be set

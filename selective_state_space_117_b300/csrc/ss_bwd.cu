@@ -8,11 +8,14 @@
 // total gradient of h_t, the adjoint runs backward in time,
 //     lambda_t = C_t ds_t + e_{t+1} lambda_{t+1},
 // the same kind of linear recurrence as the forward one, so it is chunked the
-// same way.  Four launches after the forward local pass and carry (reused at
-// kBwdChunk-step chunks, they give the state entering every chunk):
-//   bwd_local_kernel  per chunk, the adjoint's zero-start sum
-//                       G[n] = sum_{t in chunk} exp(A[n] P_t) C_t[n] ds_t,  P_t = sum_{r=t0..t} dt_r
-//                     (the forward local pass mirrored: it walks the chunk forward);
+// same way, at kBwdChunk-step chunks.  Four launches, with the forward carry between the
+// first two:
+//   bwd_locals_kernel per chunk, in one forward walk from a zero state, the forward pass's
+//                     zero-start end state H (what the forward local pass gives) and the
+//                     adjoint's zero-start sum
+//                       G[n] = sum_{t in chunk} exp(A[n] P_t) C_t[n] ds_t,  P_t = sum_{r=t0..t} dt_r,
+//                     each decay exp(dt A) computed once for both; the forward carry then
+//                     gives the state entering every chunk;
 //   bwd_carry_kernel  mu_{K-1} = dlast, mu_{k-1} = G_k + exp(A S_k) mu_k over the chunks, last
 //                     first: mu_k is the gradient reaching the chunk's last state from later
 //                     steps, and mu_{-1} = e_0 lambda_0 is dh0;
@@ -24,6 +27,7 @@
 #include "ss_dispatch.cuh"
 #include "ss_launch.h"
 #include "ss_occupancy.cuh"
+#include "ss_tma_launch.cuh"
 
 namespace ssk {
 
@@ -112,12 +116,21 @@ __device__ __forceinline__ void stage_bc(float* s, const void* src, int64_t row0
 
 }  // namespace
 
-// ---------------------------------------------------------------------------- adjoint local pass
+// ---------------------------------------------------------------------------- both local passes
 
-// One thread per (b, d, chunk), NT states as pairs; a block is kCh channels of one (b, chunk).
-template <int NT, bool BF, bool HAS_Z>
-__global__ void __launch_bounds__(kCh) bwd_local_kernel(const BwdArgs a) {
+// The forward local pass and the adjoint local pass of one chunk in a single walk: one thread
+// per (b, d, chunk), NT states as pairs; a block is kCh channels of one (b, chunk).  Walking the
+// chunk forward from a zero state, each state keeps
+//     h <- e_t h + w_t B_t u_t     (w_t = dt_t, or the zero-order-hold weight)
+//     W <- W e_t                   (= exp(A P_t), P_t the sum of dt up to and including t)
+//     G <- G + W C_t ds_t
+// with e_t = exp(dt_t A) computed once for all three.  At the chunk's end h is the forward
+// pass's zero-start end state H, G the adjoint's zero-start sum, and P the chunk's dt sum; the
+// two carries turn them into the state entering every chunk and the gradient leaving it.
+template <int NT, bool BF, bool HAS_Z, bool ZOH>
+__global__ void __launch_bounds__(kCh) bwd_locals_kernel(const BwdArgs a) {
   constexpr int NP = NT / 2;
+  __shared__ __align__(16) float sB[kBwdChunk * NT];
   __shared__ __align__(16) float sC[kBwdChunk * NT];
   const int tid = threadIdx.x;
   const int ct = blockIdx.x % a.ctiles;
@@ -127,32 +140,35 @@ __global__ void __launch_bounds__(kCh) bwd_local_kernel(const BwdArgs a) {
   const int N = (int)a.dstate;
   const int64_t L = a.seqlen, t0 = k * kBwdChunk, t_end = min(L, t0 + kBwdChunk);
 
+  stage_bc<NT, BF>(sB, a.B, b * N * L, N, L, t0, t_end, a.vec_bc, tid, kCh);
   stage_bc<NT, BF>(sC, a.C, b * N * L, N, L, t0, t_end, a.vec_bc, tid, kCh);
   __syncthreads();
   if (!active) return;
-  // Debug build: the channel's rows of delta/dy/z, its A row and its entry of the adjoint sums.
-  {
-    const int64_t BD = a.batch * a.dim, bd = b * a.dim + d;
-    if (!span_ok(a.err, bd * L + t0, t_end - t0, BD * L) || !span_ok(a.err, d * N, N, a.dim * N) ||
-        !span_ok(a.err, (k * BD + bd) * N, N, a.nchunks * BD * N))
-      return;
-  }
+  const int64_t BD = a.batch * a.dim, bd = b * a.dim + d;
+  // Debug build: the channel's rows of u/delta/dy/z, its A row and its workspace entries.
+  if (!span_ok(a.err, bd * L + t0, t_end - t0, BD * L) || !span_ok(a.err, d * N, N, a.dim * N) ||
+      !span_ok(a.err, (k * BD + bd) * N, N, a.nchunks * BD * N) || !span_ok(a.err, k * BD + bd, 1, a.nchunks * BD))
+    return;
 
-  f2 A2[NP], acc[NP];
+  f2 A2[NP], iA2[NP], h[NP], W[NP], G[NP];
   const float* Arow = a.A + d * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
-    A2[q] = pk(2 * q < N ? Arow[2 * q] * kLog2e : 0.f, 2 * q + 1 < N ? Arow[2 * q + 1] * kLog2e : 0.f);
-    acc[q] = pk(0.f, 0.f);
+    const float a0 = 2 * q < N ? Arow[2 * q] : 0.f, a1 = 2 * q + 1 < N ? Arow[2 * q + 1] : 0.f;
+    A2[q] = pk(a0 * kLog2e, a1 * kLog2e);
+    iA2[q] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
+    h[q] = G[q] = pk(0.f, 0.f);
+    W[q] = pk(1.f, 1.f);
   }
   const float bias = a.delta_bias ? a.delta_bias[d] : 0.f;
-  const int64_t row = (b * a.dim + d) * L;
+  const int64_t row = bd * L;
   float P = 0.f;
   for (int g = 0; g < kBwdChunk / 8; ++g) {
     const int64_t t = t0 + 8 * g;
     if (t >= t_end) break;
-    float xd[8], dyv[8], zv[8];
+    float xd[8], uv[8], dyv[8], zv[8];
     load_group<BF>(a.delta, row + t, t, t_end, a.vec, xd);
+    load_group<BF>(a.u, row + t, t, t_end, a.vec, uv);
     load_group_f32(a.dy, row + t, t, t_end, a.vec, dyv);
     if (HAS_Z) load_group<BF>(a.z, row + t, t, t_end, a.vec, zv);
 #pragma unroll
@@ -162,21 +178,218 @@ __global__ void __launch_bounds__(kCh) bwd_local_kernel(const BwdArgs a) {
         const float dt = a.softplus ? softplus(x) : x;
         const float ds = HAS_Z ? dyv[j] * silu(zv[j]) : dyv[j];
         P += dt;
-        const f2 Pp = pk(P, P), dsp = pk(ds, ds);
+        const f2 dtp = pk(dt, dt), dsp = pk(ds, ds);
+        const f2 wu = ZOH ? pk(uv[j], uv[j]) : pk(dt * uv[j], dt * uv[j]);
+        const float* rb = sB + (8 * g + j) * NT;
         const float* rc = sC + (8 * g + j) * NT;
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
+          const f2 b2 = *reinterpret_cast<const f2*>(rb + 2 * q);
           const f2 c2 = *reinterpret_cast<const f2*>(rc + 2 * q);
-          acc[q] = fma2(ex2x2(mul2(Pp, A2[q])), mul2(dsp, c2), acc[q]);
+          const f2 arg = mul2(dtp, A2[q]);
+          const f2 e = ex2x2(arg);
+          const f2 in = ZOH ? mul2(hold2(arg, e, dtp, iA2[q]), mul2(wu, b2)) : mul2(wu, b2);
+          h[q] = fma2(e, h[q], in);
+          W[q] = mul2(W[q], e);
+          G[q] = fma2(W[q], mul2(dsp, c2), G[q]);
         }
       }
     }
   }
-  float* G = a.ws_G + (k * a.batch * a.dim + b * a.dim + d) * N;
+  a.ws_S[k * BD + bd] = P;
+  float* H = a.ws_H + (k * BD + bd) * N;
+  float* Gd = a.ws_G + (k * BD + bd) * N;
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
-    if (2 * q < N) G[2 * q] = lo(acc[q]);
-    if (2 * q + 1 < N) G[2 * q + 1] = hi(acc[q]);
+    if (2 * q < N) H[2 * q] = lo(h[q]), Gd[2 * q] = lo(G[q]);
+    if (2 * q + 1 < N) H[2 * q + 1] = hi(h[q]), Gd[2 * q + 1] = hi(G[q]);
+  }
+}
+
+// The same two local passes with TMA-staged inputs, one block per (64 channels, batch row,
+// kLocChunks consecutive chunks).  Per 16-step tile one thread loads the block's rows of u,
+// delta, z (input dtype) and dy (fp32) and the tile's B and C rows as 3-D tensor boxes into a
+// ring of kLocSlots slots completed by mbarriers; the ring runs across the block's chunks, so
+// the next chunk's tiles are in flight while one chunk ends.  Each thread reads its channel's
+// row of every tile (swizzled, free of bank conflicts) and the tile's B and C widened to fp32
+// once per tile; the states are reset at every chunk start and written at its end.  Every wait
+// is bounded; once one gives up the block agrees at the tile's barrier, issues no further copy,
+// waits (bounded) for the copies in flight and returns.
+constexpr int kLocChunks = 8;   // chunks per block
+constexpr int kLocSlots = 2;    // tiles in flight (2 measured 0.8% faster than 3 over the whole backward)
+
+template <int NT, bool BF, bool HAS_Z>
+struct LocLayout {
+  static constexpr int ES = In<BF>::kBytes;
+  static constexpr int RB = kTmaSteps * ES;   // input row bytes: 32 (bf16) or 64 (fp32) = swizzle span
+  static constexpr int DB = kTmaSteps * 4;    // dy row bytes: 64
+  static constexpr int NA = HAS_Z ? 3 : 2;    // u, delta (, z)
+  static constexpr int kIn = kCh * RB;
+  static constexpr int kDy = kCh * DB;
+  static constexpr int kBC = NT * RB;
+  static constexpr int oDy = NA * kIn;
+  static constexpr int oB = oDy + kDy;
+  static constexpr int kSlot = align1k(oB + 2 * kBC);
+  static constexpr int kBCf = kTmaSteps * NT * 4;   // one fp32 B or C tile, [t][n]
+  static constexpr int oBCf = kLocSlots * kSlot;
+  static constexpr int oBar = oBCf + 4 * kBCf;      // two buffers of (B, C)
+  static constexpr int kBytes = oBar + kLocSlots * 8;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+template <int NT, bool BF, bool HAS_Z, bool ZOH>
+__global__ void __launch_bounds__(kCh) bwd_locals_tma_kernel(const BwdArgs a, const __grid_constant__ TmaMaps m) {
+  using Lin = In<BF>;
+  using Lay = LocLayout<NT, BF, HAS_Z>;
+  constexpr int NP = NT / 2, TS = kTmaSteps, S = kLocSlots, TPC = kBwdChunk / kTmaSteps;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+  float* bcf = reinterpret_cast<float*>(sm + Lay::oBCf);
+  constexpr int BCF = Lay::kBCf / 4;
+
+  const int tid = threadIdx.x;
+  const int ct = blockIdx.x % a.ctiles;
+  const int64_t grp = blockIdx.x / a.ctiles, b = blockIdx.y;
+  const int64_t d = (int64_t)ct * kCh + tid;
+  const bool active = d < a.dim;
+  const int N = (int)a.dstate;
+  const int64_t L = a.seqlen, BD = a.batch * a.dim, bd = b * a.dim + (active ? d : 0);
+  const int64_t c0 = grp * kLocChunks, c1 = min(a.nchunks, c0 + kLocChunks);
+  const int64_t tb = c0 * kBwdChunk, te = min(L, c1 * kBwdChunk);
+  const int ntiles = (int)((te - tb + TS - 1) / TS);
+  // Debug build: the block's rows over its steps, its batch row of B and C, its channels' A
+  // rows and their workspace entries (the whole block leaves before any copy or barrier).
+  {
+    const int64_t dl = min(a.dim, (int64_t)ct * kCh + kCh) - 1, d0 = (int64_t)ct * kCh;
+    const int64_t r0 = (b * a.dim + d0) * L + tb, r1 = (b * a.dim + dl) * L + te;
+    if (!span_ok(a.err, r0, r1 - r0, BD * L) || !span_ok(a.err, b * N * L, N * L, a.batch * N * L) ||
+        !span_ok(a.err, d0 * N, (dl - d0 + 1) * N, a.dim * N) ||
+        !span_ok(a.err, ((c1 - 1) * BD + b * a.dim + dl) * N, N, a.nchunks * BD * N))
+      return;
+  }
+
+  f2 A2[NP], iA2[NP], h[NP], W[NP], G[NP];
+  const float* Arow = a.A + (active ? d : 0) * N;
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    const float a0 = (active && 2 * q < N) ? Arow[2 * q] : 0.f, a1 = (active && 2 * q + 1 < N) ? Arow[2 * q + 1] : 0.f;
+    A2[q] = pk(a0 * kLog2e, a1 * kLog2e);
+    iA2[q] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
+    h[q] = G[q] = pk(0.f, 0.f);
+    W[q] = pk(1.f, 1.f);
+  }
+  const float bias = (a.delta_bias && active) ? a.delta_bias[d] : 0.f;
+  float P = 0.f;
+
+  const int y0 = ct * kCh, zb = (int)b;
+  auto issue = [&](int k) {   // thread 0: tile k of the block into slot k % S
+    unsigned char* slot = sm + (k % S) * Lay::kSlot;
+    uint64_t* br = &bar[k % S];
+    mbar_expect_tx(br, Lay::NA * Lay::kIn + Lay::kDy + 2 * N * Lay::RB);
+    const int x = (int)(tb + (int64_t)k * TS);
+    tma_load_3d(slot, &m.u, br, x, y0, zb);
+    tma_load_3d(slot + Lay::kIn, &m.delta, br, x, y0, zb);
+    if (HAS_Z) tma_load_3d(slot + 2 * Lay::kIn, &m.z, br, x, y0, zb);
+    tma_load_3d(slot + Lay::oDy, &m.y, br, x, y0, zb);
+    tma_load_3d(slot + Lay::oB, &m.B, br, x, 0, zb);
+    tma_load_3d(slot + Lay::oB + Lay::kBC, &m.C, br, x, 0, zb);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int k = 0; k < S && k < ntiles; ++k) issue(k);
+  int issued = min(S, ntiles);
+
+  bool ok = true;
+  int k = 0;
+  for (; k < ntiles; ++k) {
+    const int s = k % S;
+    const unsigned char* slot = sm + s * Lay::kSlot;
+    ok = mbar_wait(&bar[s], (k / S) & 1, a.err);
+    float* cB = bcf + (k & 1) * 2 * BCF;
+    float* const dst[2] = {cB, cB + BCF};
+    if (ok) tma_convert_rows<NT, BF, 2>(slot + Lay::oB, N, dst, tid);
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    const int64_t t0 = tb + (int64_t)k * TS;
+    const unsigned base = smem_addr(slot);
+#pragma unroll
+    for (int g = 0; g < TS / 8; ++g) {
+      const typename Lin::Raw8 cu = tile_row8<BF, Lay::RB>(base, tid, g);
+      const typename Lin::Raw8 rd = tile_row8<BF, Lay::RB>(base + Lay::kIn, tid, g);
+      typename Lin::Raw8 cz{};
+      if (HAS_Z) cz = tile_row8<BF, Lay::RB>(base + 2 * Lay::kIn, tid, g);
+      const In<false>::Raw8 cdy = tile_row8<false, Lay::DB>(base + Lay::oDy, tid, g);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const f2 u2 = Lin::pair(cu, p), x2 = Lin::pair(rd, p), z2 = HAS_Z ? Lin::pair(cz, p) : pk(0.f, 0.f);
+        const f2 dy2 = In<false>::pair(cdy, p);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = 8 * g + 2 * p + e;
+          if (t0 + j < te) {
+            const float x = (e ? hi(x2) : lo(x2)) + bias, uu = e ? hi(u2) : lo(u2);
+            const float dyv = e ? hi(dy2) : lo(dy2);
+            const float dt = a.softplus ? softplus(x) : x;
+            const float ds = HAS_Z ? dyv * silu(e ? hi(z2) : lo(z2)) : dyv;
+            P += dt;
+            const f2 dtp = pk(dt, dt), dsp = pk(ds, ds);
+            const f2 wu = ZOH ? pk(uu, uu) : pk(dt * uu, dt * uu);
+            const float* rb = cB + j * NT;
+            const float* rc = cB + BCF + j * NT;
+#pragma unroll
+            for (int q = 0; q < NP; q += 2) {
+              const float4 bv = *reinterpret_cast<const float4*>(rb + 2 * q);
+              const float4 cv = *reinterpret_cast<const float4*>(rc + 2 * q);
+              const f2 b2[2] = {pk(bv.x, bv.y), pk(bv.z, bv.w)}, c2[2] = {pk(cv.x, cv.y), pk(cv.z, cv.w)};
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const f2 arg = mul2(dtp, A2[q + r]);
+                const f2 ev = ex2x2(arg);
+                const f2 in = ZOH ? mul2(hold2(arg, ev, dtp, iA2[q + r]), mul2(wu, b2[r])) : mul2(wu, b2[r]);
+                h[q + r] = fma2(ev, h[q + r], in);
+                W[q + r] = mul2(W[q + r], ev);
+                G[q + r] = fma2(W[q + r], mul2(dsp, c2[r]), G[q + r]);
+              }
+            }
+          }
+        }
+      }
+    }
+    // A chunk ends with its fourth tile or with the sequence: its sums go to the workspace.
+    if ((k + 1) % TPC == 0 || k + 1 == ntiles) {
+      const int64_t kc = c0 + k / TPC;
+      if (active) {
+        a.ws_S[kc * BD + bd] = P;
+        float* H = a.ws_H + (kc * BD + bd) * N;
+        float* Gd = a.ws_G + (kc * BD + bd) * N;
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+          if (2 * q < N) H[2 * q] = lo(h[q]), Gd[2 * q] = lo(G[q]);
+          if (2 * q + 1 < N) H[2 * q + 1] = hi(h[q]), Gd[2 * q + 1] = hi(G[q]);
+        }
+      }
+      P = 0.f;
+#pragma unroll
+      for (int q = 0; q < NP; ++q) {
+        h[q] = G[q] = pk(0.f, 0.f);
+        W[q] = pk(1.f, 1.f);
+      }
+    }
+    __syncthreads();   // every thread is done with the slot (and with the other B/C buffer)
+    if (tid == 0 && k + S < ntiles) {
+      issue(k + S);
+      issued = k + S + 1;
+    }
+  }
+  if (tid == 0 && !ok) {
+    // After a failure at tile k, tiles k .. issued - 1 were issued and not all seen to land:
+    // wait for each (bounded; a completed phase returns at once) before the block exits.
+    for (int j = k; j < issued; ++j) mbar_wait(&bar[j % S], (j / S) & 1, nullptr);
   }
 }
 
@@ -735,10 +948,6 @@ static int go_bwd(const BwdArgs& a0, cudaStream_t s) {
   if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kBytes) != cudaSuccess)
     return 1;
   BwdArgs a = a0;
-  // adjoint local pass
-  a.ctiles = (int)((a.dim + kCh - 1) / kCh);
-  const dim3 g1((unsigned)(a.ctiles * a.nchunks), (unsigned)a.batch);
-  bwd_local_kernel<NT, BF, Z><<<g1, kCh, 0, s>>>(a);
   // adjoint carry
   const int64_t total = a.batch * a.dim * a.dstate;
   if (total > 0) bwd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(a);
@@ -747,6 +956,61 @@ static int go_bwd(const BwdArgs& a0, cudaStream_t s) {
   const dim3 g3((unsigned)(a.ctiles * a.nchunks), (unsigned)a.batch);
   k<<<g3, G::kThreads, G::kBytes, s>>>(a);
   return 0;
+}
+
+// The TMA version needs 16-byte aligned rows (L a multiple of 8 steps, so that every row of
+// u, delta, z, B, C and dy starts on a 16-byte boundary) and 16-byte aligned arrays.
+static bool bwd_locals_tma_usable(const BwdArgs& a, bool bf16) {
+  auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) % 16) == 0; };
+  const int64_t es = bf16 ? 2 : 4;
+  if (!encode_fn()) return false;
+  if ((a.seqlen * es) % 16 != 0 || (a.seqlen * 4) % 16 != 0) return false;
+  if (!al(a.u) || !al(a.delta) || !al(a.z) || !al(a.B) || !al(a.C) || !al(a.dy)) return false;
+  if (a.seqlen > (int64_t)INT32_MAX || a.dim > (int64_t)INT32_MAX || a.batch > (int64_t)INT32_MAX) return false;
+  return true;
+}
+
+template <int NT, bool BF, bool Z, bool ZOH>
+static int go_bwd_locals(const BwdArgs& a0, cudaStream_t s) {
+  BwdArgs a = a0;
+  a.ctiles = (int)((a.dim + kCh - 1) / kCh);
+  if (bwd_locals_tma_usable(a, BF)) {
+    using Lay = LocLayout<NT, BF, Z>;
+    TmaMaps m;
+    const CUtensorMapSwizzle sin = swizzle_for(Lay::RB);
+    if (encode3d(&m.u, BF, false, a.u, a.seqlen, a.dim, a.batch, kTmaSteps, kCh, sin) &&
+        encode3d(&m.delta, BF, false, a.delta, a.seqlen, a.dim, a.batch, kTmaSteps, kCh, sin) &&
+        encode3d(&m.y, BF, true, a.dy, a.seqlen, a.dim, a.batch, kTmaSteps, kCh, swizzle_for(Lay::DB)) &&
+        encode3d(&m.B, BF, false, a.B, a.seqlen, a.dstate, a.batch, kTmaSteps, (unsigned)a.dstate,
+                 CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        encode3d(&m.C, BF, false, a.C, a.seqlen, a.dstate, a.batch, kTmaSteps, (unsigned)a.dstate,
+                 CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        (!Z || encode3d(&m.z, BF, false, a.z, a.seqlen, a.dim, a.batch, kTmaSteps, kCh, sin))) {
+      if (!Z) m.z = m.u;
+      auto k = bwd_locals_tma_kernel<NT, BF, Z, ZOH>;
+      const int64_t groups = (a.nchunks + kLocChunks - 1) / kLocChunks;
+      const dim3 g((unsigned)(a.ctiles * groups), (unsigned)a.batch);
+      size_t dyn = Lay::kAlloc;
+      if (!balanced_smem((const void*)k, kCh, (int64_t)g.x * g.y, Lay::kAlloc, &dyn)) return 1;
+      k<<<g, kCh, dyn, s>>>(a, m);
+      return 0;
+    }
+  }
+  const dim3 g((unsigned)(a.ctiles * a.nchunks), (unsigned)a.batch);
+  bwd_locals_kernel<NT, BF, Z, ZOH><<<g, kCh, 0, s>>>(a);
+  return 0;
+}
+
+int launch_bwd_locals(const BwdArgs& a, bool bf16, bool has_z, cudaStream_t s) {
+  SSK_DISPATCH_NT(a.dstate, {
+    if (a.zoh) {
+      if (bf16) return has_z ? go_bwd_locals<NT, true, true, true>(a, s) : go_bwd_locals<NT, true, false, true>(a, s);
+      return has_z ? go_bwd_locals<NT, false, true, true>(a, s) : go_bwd_locals<NT, false, false, true>(a, s);
+    }
+    if (bf16) return has_z ? go_bwd_locals<NT, true, true, false>(a, s) : go_bwd_locals<NT, true, false, false>(a, s);
+    return has_z ? go_bwd_locals<NT, false, true, false>(a, s) : go_bwd_locals<NT, false, false, false>(a, s);
+  });
+  return -1;
 }
 
 int bwd_main_ctiles(int64_t dim, int64_t dstate) {

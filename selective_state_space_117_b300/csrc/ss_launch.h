@@ -36,6 +36,9 @@ int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStr
 
 // Backward pass after the forward local pass and carry: adjoint local pass, adjoint carry, main
 // pass (ss_bwd.cu).  Returns 0 when launched.
+// Backward pass: launch_bwd_locals (both local passes, fills ws_S, ws_H, ws_G), then the
+// forward carry (launch_carry), then launch_bwd (adjoint carry and main pass).
+int launch_bwd_locals(const BwdArgs& a, bool bf16, bool has_z, cudaStream_t s);
 int launch_bwd(const BwdArgs& a, bool bf16, bool has_z, cudaStream_t s);
 // Channel tiles of the main backward kernel (its grid is tiles x chunks x batch).
 int bwd_main_ctiles(int64_t dim, int64_t dstate);

@@ -69,8 +69,8 @@ struct BwdArgs {
   float* dD;             // (dim) or null, accumulated
   float* dbias;          // (dim) or null, accumulated
   float* dh0;            // (batch, dim, N) or null
-  const float* ws_S;
-  const float* ws_H;
+  float* ws_S;
+  float* ws_H;
   float* ws_G;
   int64_t batch, dim, dstate, seqlen, nchunks;
   int ctiles;            // channel tiles per (b, chunk) of the launched kernel

@@ -119,12 +119,17 @@ CASES = [
     (8, 2, 17, 16, 1, torch.float32, {}),                                     # one step
     (9, 1, 30, 16, 150, torch.float32, dict(softplus=False)),
     (10, 3, 100, 16, 520, torch.bfloat16, dict(h0=False)),
+    # 16 chunks in two groups of the local passes' blocks, the last chunk 40 steps (two and a
+    # half tiles), a partial last channel tile, padded states
+    (11, 2, 130, 12, 1000, torch.bfloat16, {}),
+    (12, 1, 200, 16, 1000, torch.float32, dict(with_bias=False)),
     # zero-order-hold input weight
     (20, 2, 70, 16, 200, torch.float32, dict(zoh=True)),
     (21, 1, 64, 16, 2048, torch.bfloat16, dict(zoh=True)),
     (22, 2, 33, 13, 77, torch.float32, dict(zoh=True, with_D=False)),
     (23, 1, 24, 64, 96, torch.bfloat16, dict(zoh=True, h0=False)),
     (24, 1, 30, 16, 150, torch.float32, dict(zoh=True, softplus=False)),
+    (26, 2, 130, 12, 1000, torch.bfloat16, dict(zoh=True)),
     # the medium fp32 configuration's shape
     (25, 2, 256, 16, 2048, torch.float32, {}),
 ]

@@ -476,6 +476,36 @@ def test_decode_ragged(N, dtype, shift):
     check(host(state).reshape(batch * dim, N), sref, dtype == torch.bfloat16, f"decode N={N} state")
 
 
+@pytest.mark.parametrize("zoh", [False, True], ids=["euler", "zoh"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_decode_many_ranges(dtype, zoh):
+    """More (batch row, channel range) blocks than the GPU holds at once, with a partial last
+    range in every batch row: 40 rows x 5000 channels (the last range of 128 channels holds
+    8), N = 16, from a random state, against the oracle."""
+    g = torch.Generator().manual_seed(211)
+    batch, dim, N, steps = 40, 5000, 16, 3
+    st0 = torch.randn((batch, dim, N), generator=g)
+    state = st0.to(DEV).clone()
+    A = (-torch.exp(torch.rand((dim, N), generator=g) * 3.0 - 1.5)).to(DEV)
+    D = torch.randn((dim,), generator=g).to(DEV)
+    bias = (torch.rand((dim,), generator=g) * 2.0 - 3.0).to(DEV)
+    sref = st0.double().numpy().reshape(batch * dim, N).copy()
+    w = I.to_wire
+    bf = dtype == torch.bfloat16
+    for t in range(steps):
+        u = torch.randn((batch, dim), generator=g).to(dtype).to(DEV)
+        dl = torch.randn((batch, dim), generator=g).to(dtype).to(DEV)
+        z = torch.randn((batch, dim), generator=g).to(dtype).to(DEV)
+        Bm = (torch.randn((batch, N), generator=g) * 0.5).to(dtype).to(DEV)
+        Cm = (torch.randn((batch, N), generator=g) * 0.5).to(dtype).to(DEV)
+        y = ss.state_update(state, u, dl, A, Bm, Cm, D=D, z=z, delta_bias=bias, zoh=zoh)
+        yr = oracle.state_update(sref, w(u), w(dl), w(A), w(Bm), w(Cm), D=w(D), z=w(z), delta_bias=w(bias),
+                                 dtype="bf16" if bf else "f32", zoh=zoh)
+        check(host(y).reshape(-1), yr, bf, f"decode many ranges step {t} y")
+    check(host(state).reshape(batch * dim, N), sref, bf, "decode many ranges state")
+    assert ss.device_status(clear=True) == ss.SS_OK
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 def test_chunked_local_pass_cutoff(dtype):
     """Large steps (dt ~ 2..5): every state's weight underflows a few dozen steps back from a
