@@ -448,9 +448,15 @@ struct BwdGeom {
   static constexpr int kLpc = NT / 4;
   static constexpr int kThreads = NT >= 8 ? 128 : 64;
   static constexpr int kCpb = kThreads / kLpc;
-  // dB/dC staging: [q][channel][step pair][n][2], channel rows padded by 2 floats
-  // so that the 16 lanes of a 64-bit store phase hit distinct banks.
+  // dB/dC staging: [q][channel pair][step pair][n][2]: the two channels of a pair add their
+  // partials by one shuffle, and the even one stores the dB sums, the odd one the dC sums;
+  // rows padded by 2 floats so that the 16 lanes of a 64-bit store phase hit distinct banks.
   static constexpr int kRedRow = 8 * NT + 2;
+  static constexpr int kPairs = kCpb / 2;
+  // With 4 lanes per channel (N = 16) the per-step sums P, Q, R cross the lanes by shuffles
+  // and land in registers of the lane whose (channel, step pair) item they finish; otherwise
+  // they go through shared memory (sPQR).
+  static constexpr bool kPqrShfl = kLpc == 4;
   // Items of a sub-block: (channel, step pair); kItemSlots = their count rounded up to the block.
   static constexpr int kItems = kCpb * (kSub / 2);
   static constexpr int kItemSlots = (kItems + kThreads - 1) / kThreads * kThreads;
@@ -458,8 +464,8 @@ struct BwdGeom {
                                  + 2 * kBwdChunk * kCpb      // sDt (dt, du)
                                  + 4 * kNsub * kThreads      // sCk checkpoints
                                  + kSub * kCpb               // sDs: ds = dy silu(z)
-                                 + 4 * kSub * kThreads       // sPQR partial sums
-                                 + 2 * kCpb * kRedRow        // sRed
+                                 + (kPqrShfl ? 0 : 4 * kSub * kThreads)   // sPQR partial sums
+                                 + 2 * kPairs * kRedRow      // sRed
                                  + 4 * 2 * kItemSlots;       // sRaw: 4 fields x 8 bytes per item
   static constexpr size_t kBytes = (size_t)kFloats * 4;
   // Slot of lane l's partial sums for step j of channel c in sPQR ([j][l][c] in
@@ -478,6 +484,8 @@ struct BwdGeom {
 template <int NT, bool BF, bool HAS_Z, bool ZOH>
 __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const BwdArgs a) {
   using G = BwdGeom<NT>;
+  static_assert(!G::kPqrShfl || (G::kItems == G::kThreads && G::kLpc == kSub / 2),
+                "with shuffled P, Q, R each thread finishes the item (its channel, its lane's step pair)");
   constexpr int kLpc = G::kLpc, kCpb = G::kCpb, kT = G::kThreads;
   extern __shared__ __align__(16) float smem[];
   float* sB = smem;
@@ -486,8 +494,8 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   float4* sCk = reinterpret_cast<float4*>(sDt + kBwdChunk * kCpb);       // [sb][tid]
   float* sDs = reinterpret_cast<float*>(sCk + kNsub * kT);                // [j][ci]: ds
   float4* sPQR = reinterpret_cast<float4*>(sDs + kSub * kCpb);            // G::pqr(j, l, c)
-  float* sRed = reinterpret_cast<float*>(sPQR + kSub * kT);               // [q][ci][jp][n][2]
-  uint2* sRaw = reinterpret_cast<uint2*>(sRed + 2 * kCpb * G::kRedRow);    // [field][item]
+  float* sRed = reinterpret_cast<float*>(sPQR + (G::kPqrShfl ? 0 : kSub * kT));   // [q][pair][jp][n][2]
+  uint2* sRaw = reinterpret_cast<uint2*>(sRed + 2 * G::kPairs * G::kRedRow);    // [field][item]
 
   const int tid = threadIdx.x;
   const int ct = blockIdx.x % a.ctiles;
@@ -708,7 +716,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   for (int r = 0; r < kRedSlots; ++r) {
     const int o = tid + r * kT;
     const int n = o % NT, jp = (o / NT) % (kSub / 2), q = (o / (NT * (kSub / 2))) & 1;
-    red_src[r] = q * kCpb * G::kRedRow + jp * NT * 2 + n * 2;
+    red_src[r] = q * G::kPairs * G::kRedRow + jp * NT * 2 + n * 2;
     red_dst[r] = (q ? a.dC : a.dB) + bc_row + (int64_t)(n < N ? n : 0) * L + t0 + 2 * jp;
   }
 
@@ -776,9 +784,13 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
     }
     __syncthreads();   // sDs written; the previous sub-block's sPQR / sRed readers are done
 
-    // walk the sub-block backward; every result stays in registers until the walk ends
+    // Walk the sub-block backward.  The dB and dC partials of a step pair go to shared memory
+    // as soon as both of its steps are done: the two channels of a pair (lanes kLpc apart)
+    // first swap halves with one shuffle each, so that the even channel's lane stores the
+    // pair's dB sums and the odd channel's lane its dC sums.
     float oP[kSub], oQ[kSub], oR[kSub];
-    f2 oB[kSub][2], oC[kSub][2];
+    f2 hB[2], hC[2];                             // the odd step's partials, until its pair is done
+    const bool odd_ch = (ci & 1) != 0;
 #pragma unroll
     for (int j = kSub - 1; j >= 0; --j) {
       const int t = sb * kSub + j;
@@ -791,7 +803,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
       const f2 C2[2] = {pk(cv.x, cv.y), pk(cv.z, cv.w)};
       const f2 hprev[2] = {j > 0 ? hv[j > 0 ? j - 1 : 0][0] : pk(ck.x, ck.y),
                            j > 0 ? hv[j > 0 ? j - 1 : 0][1] : pk(ck.z, ck.w)};
-      f2 lam[2], g[2], lw[2];
+      f2 lam[2], g[2], lw[2], oB[2], oC[2];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         lam[q] = fma2(dsp, C2[q], mu[q]);        // total gradient of h_t
@@ -804,12 +816,12 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
           const f2 w = hold2(arg, ev[j][q], dtp, iA2[q]);
           lw[q] = mul2(lam[q], w);                                          // lambda w
           dA[q] = fma2(mul2(lam[q], mul2(B2[q], dup)), hold_dA2(arg, ev[j][q], dtp, w, iA2[q]), dA[q]);
-          oB[j][q] = mul2(lw[q], dup);           // dB: lambda w u
+          oB[q] = mul2(lw[q], dup);              // dB: lambda w u
         } else {
           lw[q] = lam[q];
-          oB[j][q] = mul2(lam[q], dup);          // dB: lambda dt u
+          oB[q] = mul2(lam[q], dup);             // dB: lambda dt u
         }
-        oC[j][q] = mul2(dsp, hv[j][q]);          // dC: ds h_t
+        oC[q] = mul2(dsp, hv[j][q]);             // dC: ds h_t
       }
       // Euler: P = sum lambda B (du = D ds + dt P), Q = sum g A (ddt = u P + Q).
       // ZOH:   P = sum lambda w B (du = D ds + P), Q = sum g A + u sum mu B (ddt = Q),
@@ -827,20 +839,47 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
         const f2 R = fma2(C2[1], hv[j][1], mul2(C2[0], hv[j][0]));
         oR[j] = lo(R) + hi(R);
       }
-    }
+      if (j & 1) {
+        hB[0] = oB[0]; hB[1] = oB[1]; hC[0] = oC[0]; hC[1] = oC[1];
+      } else {
+        // states n0 .. n0 + 3, each as (step j, step j + 1)
+        const f2 bp[4] = {pk(lo(oB[0]), lo(hB[0])), pk(hi(oB[0]), hi(hB[0])), pk(lo(oB[1]), lo(hB[1])),
+                          pk(hi(oB[1]), hi(hB[1]))};
+        const f2 cp[4] = {pk(lo(oC[0]), lo(hC[0])), pk(hi(oC[0]), hi(hC[0])), pk(lo(oC[1]), lo(hC[1])),
+                          pk(hi(oC[1]), hi(hC[1]))};
+        float* r = sRed + (odd_ch ? G::kPairs * G::kRedRow : 0) + (ci >> 1) * G::kRedRow + (j / 2) * NT * 2 + n0 * 2;
 #pragma unroll
-    for (int j = 0; j < kSub; ++j) sPQR[G::pqr(j, li, ci)] = make_float4(oP[j], oQ[j], oR[j], 0.f);
-#pragma unroll
-    for (int jp = 0; jp < kSub / 2; ++jp) {
-      float* rB = sRed + ci * G::kRedRow + jp * NT * 2 + n0 * 2;
-      float* rC = rB + kCpb * G::kRedRow;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        *reinterpret_cast<float2*>(rB + 4 * q) = make_float2(lo(oB[2 * jp][q]), lo(oB[2 * jp + 1][q]));
-        *reinterpret_cast<float2*>(rB + 4 * q + 2) = make_float2(hi(oB[2 * jp][q]), hi(oB[2 * jp + 1][q]));
-        *reinterpret_cast<float2*>(rC + 4 * q) = make_float2(lo(oC[2 * jp][q]), lo(oC[2 * jp + 1][q]));
-        *reinterpret_cast<float2*>(rC + 4 * q + 2) = make_float2(hi(oC[2 * jp][q]), hi(oC[2 * jp + 1][q]));
+        for (int e = 0; e < 4; ++e) {
+          const f2 keep = odd_ch ? cp[e] : bp[e], give = odd_ch ? bp[e] : cp[e];
+          const float gx = __shfl_xor_sync(0xffffffffu, lo(give), kLpc);
+          const float gy = __shfl_xor_sync(0xffffffffu, hi(give), kLpc);
+          *reinterpret_cast<float2*>(r + 2 * e) = make_float2(lo(keep) + gx, hi(keep) + gy);
+        }
       }
+    }
+    // P, Q, R of every step summed over the channel's lanes.  With 4 lanes per channel, a
+    // reduce-scatter by shuffles leaves lane li the sums of steps 2 li and 2 li + 1, the step
+    // pair of the item this thread finishes below; otherwise through shared memory.
+    float sP[2], sQ[2], sR[2];
+    if constexpr (G::kPqrShfl) {
+      const bool b1 = (li >> 1) != 0, b0 = (li & 1) != 0;
+      float P4[4], Q4[4], R4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {   // lanes with bit 1 set keep steps 4..7, the others 0..3
+        P4[i] = (b1 ? oP[4 + i] : oP[i]) + __shfl_xor_sync(0xffffffffu, b1 ? oP[i] : oP[4 + i], 2);
+        Q4[i] = (b1 ? oQ[4 + i] : oQ[i]) + __shfl_xor_sync(0xffffffffu, b1 ? oQ[i] : oQ[4 + i], 2);
+        R4[i] = (b1 ? oR[4 + i] : oR[i]) + __shfl_xor_sync(0xffffffffu, b1 ? oR[i] : oR[4 + i], 2);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {   // then bit 0 picks the pair
+        sP[i] = (b0 ? P4[2 + i] : P4[i]) + __shfl_xor_sync(0xffffffffu, b0 ? P4[i] : P4[2 + i], 1);
+        sQ[i] = (b0 ? Q4[2 + i] : Q4[i]) + __shfl_xor_sync(0xffffffffu, b0 ? Q4[i] : Q4[2 + i], 1);
+        sR[i] = (b0 ? R4[2 + i] : R4[i]) + __shfl_xor_sync(0xffffffffu, b0 ? R4[i] : R4[2 + i], 1);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kSub; ++j) sPQR[G::pqr(j, li, ci)] = make_float4(oP[j], oQ[j], oR[j], 0.f);
+      sP[0] = sP[1] = sQ[0] = sQ[1] = sR[0] = sR[1] = 0.f;
     }
     __syncthreads();
 
@@ -857,10 +896,14 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
         for (int s = 0; s < 2; ++s) {
           const int j = 2 * jp + s;
           float P = 0.f, Q = 0.f, R = 0.f;
+          if constexpr (G::kPqrShfl) {          // this thread's item is (ci, li): see above
+            P = sP[s]; Q = sQ[s]; R = sR[s];
+          } else {
 #pragma unroll
-          for (int l = 0; l < kLpc; ++l) {
-            const float4 v = sPQR[G::pqr(j, l, c)];
-            P += v.x; Q += v.y; R += v.z;
+            for (int l = 0; l < kLpc; ++l) {
+              const float4 v = sPQR[G::pqr(j, l, c)];
+              P += v.x; Q += v.y; R += v.z;
+            }
           }
           const float dt = sDt[(sb * kSub + j) * kCpb + c].x;
           const float ddt = ZOH ? Q : fmaf(e_u[r][s], P, Q * kLn2);   // see P and Q above
@@ -898,7 +941,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
         const float* src = sRed + red_src[r];
         f2 acc = pk(0.f, 0.f);
 #pragma unroll 8
-        for (int c = 0; c < kCpb; ++c) acc = add2(acc, *reinterpret_cast<const f2*>(src + c * G::kRedRow));
+        for (int c = 0; c < G::kPairs; ++c) acc = add2(acc, *reinterpret_cast<const f2*>(src + c * G::kRedRow));
         float* dst = red_dst[r] + sb * kSub;
         if (a.vec && t + 2 <= t_end) {            // 8-byte aligned: dB, dC checked, L % 8 == 0, t even
           atomicAdd(reinterpret_cast<float2*>(dst), make_float2(lo(acc), hi(acc)));
