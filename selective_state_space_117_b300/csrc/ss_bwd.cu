@@ -449,10 +449,12 @@ struct BwdGeom {
   static constexpr int kThreads = NT >= 8 ? 128 : 64;
   static constexpr int kCpb = kThreads / kLpc;
   // dB/dC staging: [q][channel pair][step pair][n][2]: the two channels of a pair add their
-  // partials by one shuffle, and the even one stores the dB sums, the odd one the dC sums;
-  // rows padded by 2 floats so that the 16 lanes of a 64-bit store phase hit distinct banks.
+  // partials by one shuffle, and the even one stores the dB sums, the odd one the dC sums.
+  // Rows are padded by 2 floats and the dC part starts 4 floats further (kRedC), so that in
+  // each 16-lane phase of a 64-bit store the dB and the dC lanes fall on disjoint banks.
   static constexpr int kRedRow = 8 * NT + 2;
   static constexpr int kPairs = kCpb / 2;
+  static constexpr int kRedC = kPairs * kRedRow + 4;
   // With 4 lanes per channel (N = 16) the per-step sums P, Q, R cross the lanes by shuffles
   // and land in registers of the lane whose (channel, step pair) item they finish; otherwise
   // they go through shared memory (sPQR).
@@ -465,7 +467,7 @@ struct BwdGeom {
                                  + 4 * kNsub * kThreads      // sCk checkpoints
                                  + kSub * kCpb               // sDs: ds = dy silu(z)
                                  + (kPqrShfl ? 0 : 4 * kSub * kThreads)   // sPQR partial sums
-                                 + 2 * kPairs * kRedRow      // sRed
+                                 + kRedC + kPairs * kRedRow  // sRed
                                  + 4 * 2 * kItemSlots;       // sRaw: 4 fields x 8 bytes per item
   static constexpr size_t kBytes = (size_t)kFloats * 4;
   // Slot of lane l's partial sums for step j of channel c in sPQR ([j][l][c] in
@@ -495,7 +497,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   float* sDs = reinterpret_cast<float*>(sCk + kNsub * kT);                // [j][ci]: ds
   float4* sPQR = reinterpret_cast<float4*>(sDs + kSub * kCpb);            // G::pqr(j, l, c)
   float* sRed = reinterpret_cast<float*>(sPQR + (G::kPqrShfl ? 0 : kSub * kT));   // [q][pair][jp][n][2]
-  uint2* sRaw = reinterpret_cast<uint2*>(sRed + 2 * G::kPairs * G::kRedRow);    // [field][item]
+  uint2* sRaw = reinterpret_cast<uint2*>(sRed + G::kRedC + G::kPairs * G::kRedRow);    // [field][item]
 
   const int tid = threadIdx.x;
   const int ct = blockIdx.x % a.ctiles;
@@ -716,7 +718,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
   for (int r = 0; r < kRedSlots; ++r) {
     const int o = tid + r * kT;
     const int n = o % NT, jp = (o / NT) % (kSub / 2), q = (o / (NT * (kSub / 2))) & 1;
-    red_src[r] = q * G::kPairs * G::kRedRow + jp * NT * 2 + n * 2;
+    red_src[r] = q * G::kRedC + jp * NT * 2 + n * 2;
     red_dst[r] = (q ? a.dC : a.dB) + bc_row + (int64_t)(n < N ? n : 0) * L + t0 + 2 * jp;
   }
 
@@ -847,7 +849,7 @@ __global__ void __launch_bounds__(BwdGeom<NT>::kThreads) bwd_main_kernel(const B
                           pk(hi(oB[1]), hi(hB[1]))};
         const f2 cp[4] = {pk(lo(oC[0]), lo(hC[0])), pk(hi(oC[0]), hi(hC[0])), pk(lo(oC[1]), lo(hC[1])),
                           pk(hi(oC[1]), hi(hC[1]))};
-        float* r = sRed + (odd_ch ? G::kPairs * G::kRedRow : 0) + (ci >> 1) * G::kRedRow + (j / 2) * NT * 2 + n0 * 2;
+        float* r = sRed + (odd_ch ? G::kRedC : 0) + (ci >> 1) * G::kRedRow + (j / 2) * NT * 2 + n0 * 2;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const f2 keep = odd_ch ? cp[e] : bp[e], give = odd_ch ? bp[e] : cp[e];
