@@ -3,6 +3,7 @@
 // contract of every entry point.
 #include <cstdint>
 #include <mutex>
+#include <unordered_map>
 
 #include <cuda_runtime.h>
 
@@ -286,6 +287,17 @@ int chunked_impl(const ss_dims* dims, const float* h0, const void* u, const void
   return SS_OK;
 }
 
+// Alternates, per state array, the order in which a decode step takes the state's ranges
+// (see launch_decode).  Only the order changes, never a result; a step captured into a CUDA
+// graph keeps the order it was captured with, so consecutive captured steps alternate too.
+int decode_reverse(const float* state) {
+  static std::mutex mu;
+  static std::unordered_map<const float*, unsigned> steps;
+  std::lock_guard<std::mutex> lock(mu);
+  if (steps.size() > 4096) steps.clear();   // bound the table; an order reset only costs L2 hits
+  return (int)(steps[state]++ & 1u);
+}
+
 }  // namespace
 
 extern "C" {
@@ -344,8 +356,7 @@ int ss_state_update(const ss_dims* dims, float* state, const void* u, const void
   a.vec = (d.dstate % 4 == 0 && aligned(state, 16) && aligned(A, 16) && aligned(B, bc_align) && aligned(C, bc_align))
               ? 1 : 0;
   if (d.dim > (int64_t)INT32_MAX / 16) return SS_EINVAL;   // (channel, lane) index of a batch row fits int
-  const dim3 grid(1);
-  if (ssk::launch_decode(a, d.in_dtype == SS_BF16, z != nullptr, grid, s) != 0) return SS_EINVAL;
+  if (ssk::launch_decode(a, d.in_dtype == SS_BF16, z != nullptr, decode_reverse(state), s) != 0) return SS_EINVAL;
   return launched();
 }
 

@@ -33,6 +33,14 @@ __device__ __forceinline__ void st_keep4(float* p, float4 v, uint64_t pol) {
                : "memory");
 }
 
+// The (x, y) block this block stands for: itself, or with `reverse` the block at the mirrored
+// position of the grid's linear order, so that the state's ranges are taken last first.
+__device__ __forceinline__ uint2 block_of(int reverse) {
+  if (!reverse) return make_uint2(blockIdx.x, blockIdx.y);
+  const unsigned n = gridDim.x * gridDim.y, lin = n - 1 - (blockIdx.y * gridDim.x + blockIdx.x);
+  return make_uint2(lin % gridDim.x, lin / gridDim.x);
+}
+
 // One decode step.  A lane owns SPL = min(NT, kDecodeSpl) consecutive states of
 // one channel (G = NT / SPL lanes per channel: 2 for N = 16), keeps them in
 // registers as f32x2 pairs and reads and writes them as 16-byte vectors.  Grid:
@@ -41,17 +49,18 @@ __device__ __forceinline__ void st_keep4(float* p, float4 v, uint64_t pol) {
 // each lane computes dt itself (no cross-lane wait) and the readout sum crosses
 // the lanes with xor shuffles.
 template <int NT, bool BF, bool HAS_Z, bool ZOH>
-__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(const DecodeArgs a, int reverse) {
   using L = In<BF>;
   constexpr int SPL = NT < kDecodeSpl ? NT : kDecodeSpl;
   constexpr int G = NT / SPL;
   constexpr int NP = SPL / 2;
-  const int i = blockIdx.x * kDecodeThreads + threadIdx.x;
+  const uint2 blk = block_of(reverse);
+  const int i = (int)blk.x * kDecodeThreads + threadIdx.x;
   const int d = i / G;
   const int l = i % G;
   if (d >= a.dim) return;                        // the lanes of a channel leave together
   const int N = (int)a.dstate;
-  const int64_t b = blockIdx.y;
+  const int64_t b = blk.y;
   const int64_t c = b * a.dim + d;               // flattened (b, d)
   // Debug build: this channel's inputs, state row, A row and the batch row of B and C.
   if (!span_ok(a.err, c, 1, a.batch * a.dim) || !span_ok(a.err, c * N, N, a.batch * a.dim * N) ||
@@ -175,13 +184,14 @@ __device__ __forceinline__ void bulk_store_hint(void* dst, const void* src, unsi
 // a timeout in the device status word); if any thread's wait gives up, the whole block
 // skips the step, so the state is left unchanged and y is not written.
 template <int NT, bool BF, bool HAS_Z, bool ZOH>
-__global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const DecodeArgs a, int reverse) {
   using L = In<BF>;
   constexpr int SPL = kDecodeSpl, G = NT / SPL, CPB = kDecodeThreads / G, NP = SPL / 2;
   __shared__ __align__(128) float sst[CPB * NT];
   __shared__ __align__(8) uint64_t bar;
   const int tid = threadIdx.x;
-  const int64_t b = blockIdx.y, c0 = (int64_t)blockIdx.x * CPB;
+  const uint2 blk = block_of(reverse);
+  const int64_t b = blk.y, c0 = (int64_t)blk.x * CPB;
   const int nch = (int)min((int64_t)CPB, a.dim - c0);
   const int N = (int)a.dstate;
   const unsigned bytes = (unsigned)(nch * N * 4);
@@ -301,30 +311,29 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const Decod
 }
 
 template <int NT, bool BF, bool Z>
-static void go_decode(const DecodeArgs& a, cudaStream_t s) {
+static void go_decode(const DecodeArgs& a, int rev, cudaStream_t s) {
   constexpr int G = NT < kDecodeSpl ? 1 : NT / kDecodeSpl;
   const int64_t threads = a.dim * G;
   const dim3 g2((unsigned)((threads + kDecodeThreads - 1) / kDecodeThreads), (unsigned)a.batch);
   if constexpr (NT >= kDecodeSpl) {
     if (a.vec) {   // bulk copies of the state need 16-byte rows (N % 4 == 0) and 16-byte alignment
-      if (a.zoh) decode_bulk_kernel<NT, BF, Z, true><<<g2, kDecodeThreads, 0, s>>>(a);
-      else decode_bulk_kernel<NT, BF, Z, false><<<g2, kDecodeThreads, 0, s>>>(a);
+      if (a.zoh) decode_bulk_kernel<NT, BF, Z, true><<<g2, kDecodeThreads, 0, s>>>(a, rev);
+      else decode_bulk_kernel<NT, BF, Z, false><<<g2, kDecodeThreads, 0, s>>>(a, rev);
       return;
     }
   }
-  if (a.zoh) decode_kernel<NT, BF, Z, true><<<g2, kDecodeThreads, 0, s>>>(a);
-  else decode_kernel<NT, BF, Z, false><<<g2, kDecodeThreads, 0, s>>>(a);
+  if (a.zoh) decode_kernel<NT, BF, Z, true><<<g2, kDecodeThreads, 0, s>>>(a, rev);
+  else decode_kernel<NT, BF, Z, false><<<g2, kDecodeThreads, 0, s>>>(a, rev);
 }
 
-int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s) {
-  (void)grid;
+int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, int reverse, cudaStream_t s) {
   SSK_DISPATCH_NT(a.dstate, {
     if (bf16) {
-      if (has_z) go_decode<NT, true, true>(a, s);
-      else go_decode<NT, true, false>(a, s);
+      if (has_z) go_decode<NT, true, true>(a, reverse, s);
+      else go_decode<NT, true, false>(a, reverse, s);
     } else {
-      if (has_z) go_decode<NT, false, true>(a, s);
-      else go_decode<NT, false, false>(a, s);
+      if (has_z) go_decode<NT, false, true>(a, reverse, s);
+      else go_decode<NT, false, false>(a, reverse, s);
     }
   });
   return 0;

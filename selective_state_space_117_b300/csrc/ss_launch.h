@@ -32,7 +32,10 @@ int launch_carry(const ScanArgs& a, cudaStream_t s);
 // per chunk and a.perm; returns 0 when launched.
 bool local_sorted_available(const ScanArgs& a, bool bf16);
 int launch_local_sorted(const ScanArgs& a, bool bf16, cudaStream_t s);
-int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, dim3 grid, cudaStream_t s);
+// One decode step.  `reverse`: the blocks take the state's ranges in the opposite order
+// (the caller alternates it from step to step so that a step first reads the part of the
+// state that the previous step wrote last, which is the part most likely still in L2).
+int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, int reverse, cudaStream_t s);
 
 // Backward pass after the forward local pass and carry: adjoint local pass, adjoint carry, main
 // pass (ss_bwd.cu).  Returns 0 when launched.
