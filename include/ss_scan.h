@@ -202,7 +202,11 @@ int ss_scan_chunked_h0(const ss_dims* dims, const float* h0, const void* u, cons
  *   state   (batch, dim, dstate) fp32, read and updated in place
  *   u, delta, z, y : (batch, dim)      B, C : (batch, dstate)
  * Other arguments as ss_scan_fwd.  Running L steps from a zero state gives
- * the same y and final state as ss_scan_fwd over those L steps.
+ * the same y and final state as ss_scan_fwd over those L steps.  Consecutive
+ * calls on the same state pointer walk the state in opposite orders (a step
+ * first reads what the previous one wrote last, while it is still in L2); the
+ * order never changes a result.  Thread-safe; the per-pointer alternation is
+ * kept on the host, so steps captured into a CUDA graph alternate as captured.
  */
 int ss_state_update(const ss_dims* dims, float* state, const void* u, const void* delta,
                     const float* A, const void* B, const void* C, const float* D,

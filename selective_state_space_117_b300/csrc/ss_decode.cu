@@ -183,8 +183,17 @@ __device__ __forceinline__ void bulk_store_hint(void* dst, const void* src, unsi
 // stores from every thread.  The wait on the mbarrier is bounded (mbar_wait records
 // a timeout in the device status word); if any thread's wait gives up, the whole block
 // skips the step, so the state is left unchanged and y is not written.
+// With bf16 inputs the kernel is held to 32 registers, 8 blocks (64 warps) per SM: 32.4 us per
+// 256 x 5120 x 16 step against 34.1 us at its own 36 registers and 6 blocks (a few bytes
+// spilled; 45.8 against 46.5 us with the zero-order hold).  fp32 inputs keep the compiler's choice.
+template <bool BF>
+struct DecodeMinBlocks {
+  static constexpr int value = BF ? 8 : 1;
+};
+
 template <int NT, bool BF, bool HAS_Z, bool ZOH>
-__global__ void __launch_bounds__(kDecodeThreads) decode_bulk_kernel(const DecodeArgs a, int reverse) {
+__global__ void __launch_bounds__(kDecodeThreads, DecodeMinBlocks<BF>::value)
+    decode_bulk_kernel(const DecodeArgs a, int reverse) {
   using L = In<BF>;
   constexpr int SPL = kDecodeSpl, G = NT / SPL, CPB = kDecodeThreads / G, NP = SPL / 2;
   __shared__ __align__(128) float sst[CPB * NT];
