@@ -506,6 +506,36 @@ def test_decode_many_ranges(dtype, zoh):
     assert ss.device_status(clear=True) == ss.SS_OK
 
 
+@pytest.mark.parametrize("zoh", [False, True], ids=["euler", "zoh"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("N", [16, 5], ids=["bulk", "per_thread"])
+def test_decode_order_does_not_change_results(N, dtype, zoh):
+    """Consecutive ss_state_update calls on one state array take its ranges in opposite
+    orders.  The same step from the same state on a second array, twice in a row (its
+    contents restored in between, so the two runs take opposite orders and one of them the
+    order opposite to the first array's), must give bitwise equal states and outputs."""
+    g = torch.Generator().manual_seed(900 + N)
+    batch, dim = 37, 700
+    st0 = torch.randn((batch, dim, N), generator=g).to(DEV)
+    A = (-torch.exp(torch.rand((dim, N), generator=g) * 2.0 - 1.0)).to(DEV)
+    D = torch.randn((dim,), generator=g).to(DEV)
+    bias = (torch.rand((dim,), generator=g) * 2.0 - 3.0).to(DEV)
+    ins = [torch.randn((batch, dim), generator=g).to(dtype).to(DEV) for _ in range(3)]
+    Bm = (torch.randn((batch, N), generator=g) * 0.5).to(dtype).to(DEV)
+    Cm = (torch.randn((batch, N), generator=g) * 0.5).to(dtype).to(DEV)
+    kw = dict(D=D, z=ins[2], delta_bias=bias, zoh=zoh)
+    p = st0.clone()
+    y_p = ss.state_update(p, ins[0], ins[1], A, Bm, Cm, **kw)
+    q = st0.clone()
+    for _ in range(2):
+        q.copy_(st0)
+        y_q = ss.state_update(q, ins[0], ins[1], A, Bm, Cm, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(p, q)
+        assert torch.equal(y_p, y_q)
+    assert ss.device_status(clear=True) == ss.SS_OK
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 def test_chunked_local_pass_cutoff(dtype):
     """Large steps (dt ~ 2..5): every state's weight underflows a few dozen steps back from a
