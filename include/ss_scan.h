@@ -298,7 +298,7 @@ int ss_causal_conv1d(const ss_dims* dims, const void* x, const float* weight, co
  * Workspace: ss_scan_bwd_workspace_bytes(dims) bytes, 256-byte aligned, owned by
  * the caller (for batch 1, dim 5120, N 16, L 65536: 692 MB).  Errors as
  * ss_scan_chunked; SS_EALIGN if an fp32 array is not 4-byte aligned.
- * Six kernels and up to five memsets on `stream`, asynchronous.
+ * Four kernels and up to five memsets on `stream`, asynchronous.
  */
 size_t ss_scan_bwd_workspace_bytes(const ss_dims* dims);
 

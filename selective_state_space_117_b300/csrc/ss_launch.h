@@ -37,10 +37,9 @@ int launch_local_sorted(const ScanArgs& a, bool bf16, cudaStream_t s);
 // state that the previous step wrote last, which is the part most likely still in L2).
 int launch_decode(const DecodeArgs& a, bool bf16, bool has_z, int reverse, cudaStream_t s);
 
-// Backward pass after the forward local pass and carry: adjoint local pass, adjoint carry, main
-// pass (ss_bwd.cu).  Returns 0 when launched.
-// Backward pass: launch_bwd_locals (both local passes, fills ws_S, ws_H, ws_G), then the
-// forward carry (launch_carry), then launch_bwd (adjoint carry and main pass).
+// Backward pass (ss_bwd.cu): launch_bwd_locals (both local passes in one kernel; fills ws_S,
+// ws_H and ws_G), then the forward carry (launch_carry), then launch_bwd (adjoint carry and
+// main pass).  Each returns 0 when launched.
 int launch_bwd_locals(const BwdArgs& a, bool bf16, bool has_z, cudaStream_t s);
 int launch_bwd(const BwdArgs& a, bool bf16, bool has_z, cudaStream_t s);
 // Channel tiles of the main backward kernel (its grid is tiles x chunks x batch).
