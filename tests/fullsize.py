@@ -3,7 +3,7 @@
 The oracle computes every channel of the workload (channels are independent, so
 it runs block by block over lists of flattened channel indices b * dim + d), and
 each block of every GPU output is compared with it under the rules of
-tests/parity.py (StreamCheck gives the verdict of a whole-array check).  Nothing
+tests/parity.py (StreamCheck gives the outcome of a whole-array check).  Nothing
 is sampled: every output element and every final state is compared.
 """
 from __future__ import annotations

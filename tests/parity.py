@@ -21,7 +21,7 @@ most 2^-9 relative.  Such outputs pass iff every element has
 fp32 arithmetic before it, plus a floor for outputs that cancel to ~0).
 
 Outputs too large to hold twice on the host (the full-size workloads) are
-compared block by block with StreamCheck, which reaches exactly the verdict of
+compared block by block with StreamCheck, which reaches exactly the outcome of
 check() on the whole array without keeping it.
 """
 from __future__ import annotations
@@ -106,14 +106,14 @@ def check(y, ref, bf16: bool, what: str):
 class StreamCheck:
     """check() over an output delivered in blocks (any split of the elements).
 
-    bf16 rule: max |err| and sum(ref^2) accumulate, so the verdict is exact.
+    bf16 rule: max |err| and sum(ref^2) accumulate, so the outcome is exact.
     fp32 rule: an element passes outright when |err| <= tol * |ref|; otherwise
     it needs |err| <= tol * rms(ref).  The largest |err| among the elements that
     did not pass outright is kept, and finish() compares it with tol * rms, which
-    is the verdict of check() on the whole array.  The reported figures that
+    is the outcome of check() on the whole array.  The reported figures that
     depend on the final rms (the floored error, the unfloored relative error's
     threshold) use each block's own rms for the split, which only matters for
-    the report, not for the verdict."""
+    the report, not for the outcome."""
 
     def __init__(self, what: str, bf16: bool, tol: float | None = None):
         self.what, self.bf16 = what, bf16
@@ -158,7 +158,7 @@ class StreamCheck:
 class StreamCheckBf16Out:
     """check_bf16_out() over an output delivered in blocks: an element passes outright
     when |err| <= 2^-8 |ref|; the largest excess |err| - 2^-8 |ref| among the others is
-    compared with 1e-5 * rms(ref) at the end, the verdict of check_bf16_out on the whole."""
+    compared with 1e-5 * rms(ref) at the end, the outcome of check_bf16_out on the whole."""
 
     def __init__(self, what: str):
         self.what, self.n, self.ss, self.excess, self.max_err = what, 0, 0.0, 0.0, 0.0

@@ -1,4 +1,4 @@
-"""The streamed comparisons of tests/parity.py reach the same verdict as the
+"""The streamed comparisons of tests/parity.py reach the same outcome as the
 whole-array ones, whatever the split into blocks (no GPU needed)."""
 import numpy as np
 import pytest
