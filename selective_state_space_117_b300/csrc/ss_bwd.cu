@@ -122,7 +122,8 @@ __device__ __forceinline__ void stage_bc(float* s, const void* src, int64_t row0
 // per (b, d, chunk), NT states as pairs; a block is kCh channels of one (b, chunk).  Walking the
 // chunk forward from a zero state, each state keeps
 //     h <- e_t h + w_t B_t u_t     (w_t = dt_t, or the zero-order-hold weight)
-//     W <- W e_t                   (= exp(A P_t), P_t the sum of dt up to and including t)
+//     W <- W e_t                   (= exp(A P_t), P_t the sum of dt up to and including t;
+//                                   restarted as exp(A P) at every 8-step group)
 //     G <- G + W C_t ds_t
 // with e_t = exp(dt_t A) computed once for all three.  At the chunk's end h is the forward
 // pass's zero-start end state H, G the adjoint's zero-start sum, and P the chunk's dt sum; the
@@ -166,6 +167,11 @@ __global__ void __launch_bounds__(kCh) bwd_locals_kernel(const BwdArgs a) {
   for (int g = 0; g < kBwdChunk / 8; ++g) {
     const int64_t t = t0 + 8 * g;
     if (t >= t_end) break;
+    if (g > 0) {   // the decay product restarts from exp(A P) at every group (as the TMA version's)
+      const f2 Pp = pk(P, P);
+#pragma unroll
+      for (int q = 0; q < NP; ++q) W[q] = ex2x2(mul2(Pp, A2[q]));
+    }
     float xd[8], uv[8], dyv[8], zv[8];
     load_group<BF>(a.delta, row + t, t, t_end, a.vec, xd);
     load_group<BF>(a.u, row + t, t, t_end, a.vec, uv);
@@ -317,6 +323,14 @@ __global__ void __launch_bounds__(kCh) bwd_locals_tma_kernel(const BwdArgs a, co
     if (!ok) break;
     const int64_t t0 = tb + (int64_t)k * TS;
     const unsigned base = smem_addr(slot);
+    // The decay product restarts from exp(A P) at every tile, so that its rounding does not
+    // build up over a whole chunk (the long sequence's largest ddelta error 4.6e-5 of the
+    // tolerance's scale without it, 2.6e-5 with it; 0.3% more time).
+    if (k % TPC != 0) {
+      const f2 Pp = pk(P, P);
+#pragma unroll
+      for (int q = 0; q < NP; ++q) W[q] = ex2x2(mul2(Pp, A2[q]));
+    }
 #pragma unroll
     for (int g = 0; g < TS / 8; ++g) {
       const typename Lin::Raw8 cu = tile_row8<BF, Lay::RB>(base, tid, g);
