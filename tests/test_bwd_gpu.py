@@ -123,6 +123,9 @@ CASES = [
     # half tiles), a partial last channel tile, padded states
     (11, 2, 130, 12, 1000, torch.bfloat16, {}),
     (12, 1, 200, 16, 1000, torch.float32, dict(with_bias=False)),
+    # the narrowest state width through the TMA local passes (one lane per channel in the
+    # main pass, N padded from 3 to 4)
+    (13, 2, 50, 3, 136, torch.bfloat16, {}),
     # zero-order-hold input weight
     (20, 2, 70, 16, 200, torch.float32, dict(zoh=True)),
     (21, 1, 64, 16, 2048, torch.bfloat16, dict(zoh=True)),
@@ -130,6 +133,7 @@ CASES = [
     (23, 1, 24, 64, 96, torch.bfloat16, dict(zoh=True, h0=False)),
     (24, 1, 30, 16, 150, torch.float32, dict(zoh=True, softplus=False)),
     (26, 2, 130, 12, 1000, torch.bfloat16, dict(zoh=True)),
+    (27, 1, 70, 4, 200, torch.float32, dict(zoh=True)),
     # the medium fp32 configuration's shape
     (25, 2, 256, 16, 2048, torch.float32, {}),
 ]
