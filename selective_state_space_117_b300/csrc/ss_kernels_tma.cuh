@@ -168,7 +168,10 @@ __global__ void __launch_bounds__(kCh, (MinBlocks<NT, BF>::value))
     const int64_t t0 = w.t_begin + (int64_t)k * TS;
     if (w.active) {
       const unsigned ybase = smem_addr(yt);
-#pragma unroll
+      // With the zero-order hold one 8-step group is already a long stretch of code; unrolling
+      // the tile's two groups as well overflowed the instruction cache (ncu: a warp per issue
+      // waiting for instructions) and cost 5.6% of the long-sequence fix-up.
+#pragma unroll(ZOH ? 1 : TS / kGroup)
       for (int g = 0; g < TS / kGroup; ++g) {
         if (t0 + g * kGroup >= w.t_end) break;
         const typename L::Raw8 cu = tile_row8<BF, Lay::RB>(slot, tid, g);
