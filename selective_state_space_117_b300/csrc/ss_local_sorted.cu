@@ -338,39 +338,52 @@ __global__ void __launch_bounds__(32, kLsMinBlocks)
       R = R_in + (ps[0] + after[0]);
     }
 
+    // One state of the tile: its terms for the 16 steps added to acc[n].
+    auto state_tile = [&](int n) {
+      const float4* brow = reinterpret_cast<const float4*>(Bt + n * kLsSteps);
+      const f2 A2 = pk(Ap[n], Ap[n]);
+      f2 sum = acc[n];
+      if constexpr (ZOH) {
+        // Weights at the points R_{-1} = R (before the tile), R_0, ..., R_{kLsSteps-1}: the hold
+        // weight of step s is (w(R_{s-1}) - w(R_s)) / A with w(R) = exp(A R).
+        const f2 iA2 = pk(iAs[n], iAs[n]);
+        float w_prev = ex2(Ap[n] * R);   // w(R_{-1})
+#pragma unroll
+        for (int p = 0; p < NPAIR; ++p) {
+          const float4 bv = brow[p >> 1];
+          const f2 Bp = (p & 1) ? pk(bv.z, bv.w) : pk(bv.x, bv.y);
+          const f2 wc = ex2x2(mul2(R2[p], A2));
+          const f2 wn = pk(w_prev, lo(wc));
+          w_prev = hi(wc);
+          const f2 hold = hold_between2(wn, wc, mul2(dt2[p], A2), dt2[p], iA2);
+          sum = fma2(hold, mul2(w2[p], Bp), sum);
+        }
+      } else {
+#pragma unroll
+        for (int p = 0; p < NPAIR; ++p) {
+          const float4 bv = brow[p >> 1];
+          const f2 Bp = (p & 1) ? pk(bv.z, bv.w) : pk(bv.x, bv.y);
+          sum = fma2(ex2x2(mul2(R2[p], A2)), mul2(w2[p], Bp), sum);
+        }
+      }
+      acc[n] = sum;
+    };
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
       if (!((live >> gi) & 1u)) continue;
+      if constexpr (ZOH) {
+        // With the hold a state's tile is a long stretch of code; unrolled over the group's
+        // states it overflowed the instruction cache (ncu: a warp per issue waiting for
+        // instructions), so this loop stays rolled (its per-state constants come from local
+        // memory): the long-sequence ZOH local pass 1.33 -> 1.20 ms.
+#pragma unroll 1
+        for (int n = gi * kLsGroup; n < (gi + 1) * kLsGroup && n < N; ++n) state_tile(n);
+      } else {
 #pragma unroll
-      for (int n = gi * kLsGroup; n < (gi + 1) * kLsGroup && n < NT; ++n) {
-        if (n >= N) break;
-        const float4* brow = reinterpret_cast<const float4*>(Bt + n * kLsSteps);
-        const f2 A2 = pk(Ap[n], Ap[n]);
-        f2 sum = acc[n];
-        if constexpr (ZOH) {
-          // Weights at the points R_{-1} = R (before the tile), R_0, ..., R_{kLsSteps-1}: the hold
-          // weight of step s is (w(R_{s-1}) - w(R_s)) / A with w(R) = exp(A R).
-          const f2 iA2 = pk(iAs[n], iAs[n]);
-          float w_prev = ex2(Ap[n] * R);   // w(R_{-1})
-#pragma unroll
-          for (int p = 0; p < NPAIR; ++p) {
-            const float4 bv = brow[p >> 1];
-            const f2 Bp = (p & 1) ? pk(bv.z, bv.w) : pk(bv.x, bv.y);
-            const f2 wc = ex2x2(mul2(R2[p], A2));
-            const f2 wn = pk(w_prev, lo(wc));
-            w_prev = hi(wc);
-            const f2 hold = hold_between2(wn, wc, mul2(dt2[p], A2), dt2[p], iA2);
-            sum = fma2(hold, mul2(w2[p], Bp), sum);
-          }
-        } else {
-#pragma unroll
-          for (int p = 0; p < NPAIR; ++p) {
-            const float4 bv = brow[p >> 1];
-            const f2 Bp = (p & 1) ? pk(bv.z, bv.w) : pk(bv.x, bv.y);
-            sum = fma2(ex2x2(mul2(R2[p], A2)), mul2(w2[p], Bp), sum);
-          }
+        for (int n = gi * kLsGroup; n < (gi + 1) * kLsGroup && n < NT; ++n) {
+          if (n >= N) break;
+          state_tile(n);
         }
-        acc[n] = sum;
       }
     }
     __syncwarp();   // every lane is done with this slot and the fp32 B tile before they are refilled
