@@ -331,7 +331,10 @@ __global__ void __launch_bounds__(kCh) bwd_locals_tma_kernel(const BwdArgs a, co
 #pragma unroll
       for (int q = 0; q < NP; ++q) W[q] = ex2x2(mul2(Pp, A2[q]));
     }
-#pragma unroll
+    // With the zero-order hold one 8-step group is a long stretch of code: the tile's two
+    // groups stay a rolled loop so that they fit the instruction cache (the long sequence's
+    // ZOH backward 17.67 -> 16.81 ms).
+#pragma unroll(ZOH ? 1 : TS / 8)
     for (int g = 0; g < TS / 8; ++g) {
       const typename Lin::Raw8 cu = tile_row8<BF, Lay::RB>(base, tid, g);
       const typename Lin::Raw8 rd = tile_row8<BF, Lay::RB>(base + Lay::kIn, tid, g);
